@@ -1,0 +1,244 @@
+"""FP64 CPU oracle for the positions-aware cached GQA + RoPE decode step and
+the equal-length prefill into empty cache rows.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import or call this module.  The product
+path (the CUDA library and its Python binding) never imports it, and this
+module imports nothing from the product package: the two share no code.
+
+What it computes is the plain definition of each step, in float64, with plain
+numpy operations (a matrix product is the only library primitive used):
+
+* split-half rotary position embedding (microLLM-rocm ARCHITECTURE.md, section
+  "Attention layout boundary": the bias + split-half RoPE kernel requires an even
+  head width D, a nonnegative position offset and a positive base);
+* the positions-aware K/V store and cached attention of the active-row decode
+  step (same page, section "Tensor ownership boundary": device ``positions[A]``
+  and ``cache_rows[A]`` parameterise decode RoPE, K/V store and cached attention;
+  inactive full-capacity rows stay untouched);
+* the equal-length prefill whose prefixes land in their target empty cache rows
+  (same section: one [A, T] batch runs, then each prefix is mapped into its
+  target empty shared-cache row).
+
+Storage is BF16 (16-bit patterns in numpy ``uint16`` arrays); arithmetic is
+float64; results that the path stores as BF16 are rounded once, directly from
+float64, to nearest-even.
+
+Readings taken where the pages are silent (each is listed in the design doc):
+  - pair i of a head is (x[i], x[i + D/2]) and rotates by angle pos * theta^(-2i/D),
+    y[i] = x[i] cos - x[i+D/2] sin, y[i+D/2] = x[i+D/2] cos + x[i] sin;
+  - the decode token attends to keys 0..pos inclusive (its own K/V is stored first);
+  - q is rounded to BF16 after rotation, before attention;
+  - the softmax scale multiplies the float score q.k (it is not folded into q);
+  - query head h reads KV head floor(h / G), G = H_q / H_kv;
+  - prefill positions start at 0 (the target rows are empty).
+
+Parity pins: every function here is checked by ``tests/test_oracle_pins.py``
+against closed forms, invariants and brute force; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "bf16_to_f64", "f64_to_bf16", "rope_inv_freq", "rope_split_half",
+    "rope_split_half_bf16", "rope_kv_store", "cached_gqa_attention",
+    "cached_gqa_attention_one", "prefill_gqa_cached_rows",
+    "prefill_attention_one", "ulp_distance_bf16",
+]
+
+
+# ---------------------------------------------------------------- BF16 codec
+def bf16_to_f64(bits) -> np.ndarray:
+    """BF16 bit patterns -> float64 (exact: BF16 is the top half of FP32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(x) -> np.ndarray:
+    """Round float64 values to BF16, nearest-even, in one rounding step.
+
+    BF16 keeps 8 significant bits and FP32's exponent range (normal numbers
+    down to 2^-126, subnormal spacing 2^-133).  A value is scaled by a power of
+    two so that its last kept bit has weight 1, rounded with ``np.rint`` (ties
+    to even), scaled back, and reinterpreted.  Rounding happens once, from
+    float64: there is no intermediate FP32 rounding.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    _, e = np.frexp(ax)                       # ax = m * 2^e, m in [0.5, 1)
+    quantum = np.where(e >= -125, e - 8, -133)
+    y = np.ldexp(np.rint(np.ldexp(ax, -quantum)), quantum)
+    with np.errstate(over="ignore", invalid="ignore"):
+        y32 = y.astype(np.float32)            # exact: y has at most 8 significant bits
+    bits = (y32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    bits = np.where(np.isnan(x), np.uint16(0x7FC0), bits)
+    bits = np.where(np.signbit(x), bits | np.uint16(0x8000), bits)
+    return bits.astype(np.uint16)
+
+
+def ulp_distance_bf16(a_bits, b_bits) -> np.ndarray:
+    """Distance between BF16 patterns counted in representable values
+    (ordered-integer difference; +0 and -0 are the same point)."""
+    def ordered(b):
+        b = np.asarray(b, dtype=np.uint16).astype(np.int64)
+        mag = b & 0x7FFF
+        return np.where(b & 0x8000, -mag, mag)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+# ---------------------------------------------------------------- RoPE
+def rope_inv_freq(D: int, theta: float) -> np.ndarray:
+    """Angular frequency of pair i: theta^(-2i/D), i = 0..D/2-1."""
+    if D % 2:
+        raise ValueError("split-half RoPE needs an even head width")
+    if not theta > 0:
+        raise ValueError("RoPE base must be positive")
+    i = np.arange(D // 2, dtype=np.float64)
+    return np.power(np.float64(theta), -2.0 * i / D)
+
+
+def rope_split_half(x, positions, theta: float) -> np.ndarray:
+    """Split-half rotation of float64 vectors.
+
+    ``x`` has shape [..., D]; ``positions`` broadcasts against x[..., 0].
+    Pair i is (x[i], x[i + D/2]); it turns by phi = pos * theta^(-2i/D):
+        y[i]       = x[i] cos(phi) - x[i + D/2] sin(phi)
+        y[i + D/2] = x[i + D/2] cos(phi) + x[i] sin(phi)
+    """
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    pos = np.asarray(positions)
+    if np.any(pos < 0):
+        raise ValueError("RoPE positions must be nonnegative")
+    phi = pos.astype(np.float64)[..., None] * rope_inv_freq(D, theta)
+    c, s = np.cos(phi), np.sin(phi)
+    x1, x2 = x[..., : D // 2], x[..., D // 2:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def rope_split_half_bf16(x_bits, positions, theta: float) -> np.ndarray:
+    """BF16 in, BF16 out: widen, rotate in float64, round once."""
+    return f64_to_bf16(rope_split_half(bf16_to_f64(x_bits), positions, theta))
+
+
+# ---------------------------------------------------------------- decode store
+def rope_kv_store(q, k, v, positions, cache_rows, theta, k_cache, v_cache):
+    """Decode RoPE + K/V store for A active tokens.
+
+    q [A, H_q, D], k/v [A, H_kv, D] (BF16 bits); positions, cache_rows [A];
+    k_cache/v_cache [S, H_kv, max_seq, D] (BF16 bits, not modified).
+    Returns (q_rot, k_cache', v_cache'): q rotated at its own position, and
+    copies of the caches in which cell [cache_rows[a], :, positions[a], :] of
+    each active token holds its rotated K and its V bytes unchanged.  Every
+    other byte of the caches is left as it was.
+    """
+    positions = np.asarray(positions, dtype=np.int64)
+    rows = np.asarray(cache_rows, dtype=np.int64)
+    S, H_kv, max_seq, D = k_cache.shape
+    if np.any((positions < 0) | (positions >= max_seq)) or np.any((rows < 0) | (rows >= S)):
+        raise ValueError("position or cache row out of range")
+    if len(set(rows.tolist())) != len(rows):
+        raise ValueError("cache rows of one step must be distinct")
+    q_rot = rope_split_half_bf16(q, positions[:, None], theta)
+    k_rot = rope_split_half_bf16(k, positions[:, None], theta)
+    kc = np.array(k_cache, dtype=np.uint16, copy=True)
+    vc = np.array(v_cache, dtype=np.uint16, copy=True)
+    for a in range(len(rows)):
+        kc[rows[a], :, positions[a], :] = k_rot[a]
+        vc[rows[a], :, positions[a], :] = np.asarray(v[a], dtype=np.uint16)
+    return q_rot, kc, vc
+
+
+# ---------------------------------------------------------------- attention
+def softmax(s: np.ndarray) -> np.ndarray:
+    """Softmax over the last axis in float64 (max-shifted, exact definition)."""
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def cached_gqa_attention_one(q_vec, keys, values, scale: float) -> np.ndarray:
+    """softmax(keys @ q * scale) @ values for one query (all float64)."""
+    s = (keys @ q_vec) * scale
+    return softmax(s) @ values
+
+
+def cached_gqa_attention(q_rot, k_cache, v_cache, positions, cache_rows,
+                         scale: float, heads=None) -> np.ndarray:
+    """Cached GQA attention of the decode step, float64 result.
+
+    Token a, query head h attends to keys 0..positions[a] (inclusive) of KV head
+    floor(h / G) in cache row cache_rows[a].  ``heads`` optionally lists the
+    (a, h) pairs to compute; the others stay NaN.  Result [A, H_q, D].
+    """
+    q_rot = np.asarray(q_rot, dtype=np.uint16)
+    A, H_q, D = q_rot.shape
+    H_kv = k_cache.shape[1]
+    G = H_q // H_kv
+    out = np.full((A, H_q, D), np.nan)
+    pairs = [(a, h) for a in range(A) for h in range(H_q)] if heads is None else heads
+    for a, h in pairs:
+        r, p, g = int(cache_rows[a]), int(positions[a]), h // G
+        keys = bf16_to_f64(k_cache[r, g, : p + 1])
+        vals = bf16_to_f64(v_cache[r, g, : p + 1])
+        out[a, h] = cached_gqa_attention_one(bf16_to_f64(q_rot[a, h]), keys, vals, scale)
+    return out
+
+
+# ---------------------------------------------------------------- prefill
+def prefill_attention_one(q_rot_bits, k_rows, v_rows, t: int, scale: float) -> np.ndarray:
+    """Causal attention of prompt position t over cached positions 0..t."""
+    return cached_gqa_attention_one(bf16_to_f64(q_rot_bits), bf16_to_f64(k_rows[: t + 1]),
+                                    bf16_to_f64(v_rows[: t + 1]), scale)
+
+
+def prefill_gqa_cached_rows(q, k, v, cache_rows, theta, scale, k_cache, v_cache,
+                            select=None):
+    """Equal-length prefill of A prompts into empty cache rows.
+
+    q [A, T, H_q, D], k/v [A, T, H_kv, D] (BF16 bits, token-major BTHD), positions
+    0..T-1.  Rotated K and raw V of prompt a go to cache row cache_rows[a],
+    positions [0, T); nothing else in the caches changes.  Causal GQA attention
+    (position t sees 0..t) reads them back from the cache rows.
+
+    Returns (q_rot [A, T, H_q, D] bits, out float64 [A, T, H_q, D], k_cache',
+    v_cache').  ``select`` optionally lists the (a, t, h) outputs to compute
+    (others NaN); without it every output is computed, one (a, h) at a time.
+    """
+    q = np.asarray(q, dtype=np.uint16)
+    A, T, H_q, D = q.shape
+    S, H_kv, max_seq, _ = k_cache.shape
+    G = H_q // H_kv
+    rows = np.asarray(cache_rows, dtype=np.int64)
+    if T > max_seq:
+        raise ValueError("prompt longer than the cache")
+    if np.any((rows < 0) | (rows >= S)) or len(set(rows.tolist())) != len(rows):
+        raise ValueError("cache rows must be distinct and in range")
+    pos = np.arange(T)
+    q_rot = rope_split_half_bf16(q, pos[None, :, None], theta)
+    k_rot = rope_split_half_bf16(k, pos[None, :, None], theta)
+    kc = np.array(k_cache, dtype=np.uint16, copy=True)
+    vc = np.array(v_cache, dtype=np.uint16, copy=True)
+    for a in range(A):
+        kc[rows[a], :, :T, :] = np.transpose(k_rot[a], (1, 0, 2))
+        vc[rows[a], :, :T, :] = np.transpose(np.asarray(v[a], dtype=np.uint16), (1, 0, 2))
+    out = np.full((A, T, H_q, D), np.nan)
+    if select is None:
+        mask = np.tril(np.ones((T, T), dtype=bool))
+        for a in range(A):
+            for h in range(H_q):
+                g = h // G
+                Q = bf16_to_f64(q_rot[a, :, h])
+                K = bf16_to_f64(kc[rows[a], g, :T])
+                V = bf16_to_f64(vc[rows[a], g, :T])
+                s = (Q @ K.T) * scale
+                s = np.where(mask, s, -np.inf)
+                out[a, :, h] = softmax(s) @ V
+    else:
+        for a, t, h in select:
+            g = h // G
+            out[a, t, h] = prefill_attention_one(q_rot[a, t, h], kc[rows[a], g, :T],
+                                                 vc[rows[a], g, :T], t, scale)
+    return q_rot, out, kc, vc
