@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 cached GQA + RoPE path.
+
+A step is one decode step of one layer on the Llama-style workload (64 cache
+slots x 4096 positions, A = 32 active rows at distinct slots, positions uniform
+in [1, 4096), H_q = 32, H_kv = 8, D = 128, theta = 5e5): split-half RoPE + K/V
+store of the 32 new tokens (rope_kv_store_out_), then cached GQA attention of
+each token over its row's prefix (cached_gqa_attention_out_).  Headline value:
+decode tokens/s (A tokens per step).  Beside it: the KV-cache bytes per second
+of the attention call against the measured HBM copy bandwidth, and the causal
+prefill of 16 prompts x 1024 tokens into empty rows (TFLOP/s against the
+measured BF16 dense peak).
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream; L2 (129 MB) is flushed between timed steps by writing
+a 256 MB buffer outside the events.  ``e2e`` repeats the step through the
+public API from pinned host buffers: H2D of the step's inputs, the two calls,
+D2H of the attention output, all inside a host wall-clock timer.
+
+Multi-GPU: the path has no exchange step; with N ranks (torchrun) every rank
+runs its own replica on its own GPU, ranks meet at a barrier around the timed
+region and the value is all tokens over the slowest rank's time.
+
+``--impl reference`` times the FP64 CPU oracle on a bounded sample of the same
+workload instead (the only CPU arm there is: the pages ship no code).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from kv_cached_gqa_rope_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode tokens/s + KV-cache HBM GB/s (% of peak); prefill TFLOP/s (% BF16 peak)"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            target = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            target = str(self.dev)
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", target, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2], *parts[3:7]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        busy = [r[0] for r in rows]
+        return {"sm_mhz": float(np.median(busy)), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------- profiles
+def profile_traffic(kernel_source: str, summary_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if that summary was
+    taken on the current source of the kernel (its sha256 matches)."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    if not os.path.exists(path):
+        return None
+    src = open(os.path.join(ROOT, "kv_cached_gqa_rope_gb300", "csrc", kernel_source), "rb").read()
+    sha = hashlib.sha256(src).hexdigest()
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_workload"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------- decode
+def decode_bytes(wl, positions):
+    """Algorithmic HBM bytes of one decode step: the attention call reads each
+    active row's K and V prefix (p+1 keys, all KV heads) and the rotated Q, and
+    writes the output; the store reads q, k, v and writes q_rot and one K and
+    one V cell per KV head."""
+    p = positions.astype(np.int64)
+    kv_prefix = int(np.sum(p + 1)) * wl.H_kv * wl.D * 2 * 2
+    q_bytes = wl.A * wl.H_q * wl.D * 2
+    attn = kv_prefix + 2 * q_bytes
+    store = 2 * (wl.A * (wl.H_q + 2 * wl.H_kv) * wl.D * 2)
+    return attn, attn + store
+
+
+def prefill_flops(wl):
+    return 4.0 * wl.D * wl.H_q * wl.A * wl.T * (wl.T + 1) / 2.0
+
+
+def run_ours(args, rank, world, local):
+    import kv_cached_gqa_rope_gb300 as kv
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+    wl = W.LLAMA_DECODE
+    inp = W.make_decode_inputs(wl)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    pos, rows = inp.positions.to(dev), inp.cache_rows.to(dev)
+    kc, vc = inp.build_cache(dev)
+    q_rot = torch.empty_like(q)
+    out = torch.empty_like(q)
+    ws1 = kv.new_workspace(kv.rope_kv_store_workspace_size(), dev)
+    ws2 = kv.new_workspace(kv.cached_gqa_attention_workspace_size(wl.A, wl.H_q, wl.H_kv, wl.D), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kv.rope_kv_store_out_(q, k, v, pos, rows, wl.theta, q_rot, kc, vc, ws1, stream)
+        kv.cached_gqa_attention_out_(q_rot, kc, vc, pos, rows, wl.scale, out, ws2, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if kv.kvgqa_read_status(ws1) or kv.kvgqa_read_status(ws2):
+        raise RuntimeError("device status flags set during warm-up")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        kv.rope_kv_store_out_(q, k, v, pos, rows, wl.theta, q_rot, kc, vc, ws1, stream)
+        e1.record(stream)
+        kv.cached_gqa_attention_out_(q_rot, kc, vc, pos, rows, wl.scale, out, ws2, stream)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    store_ms = [a.elapsed_time(b) for a, b, c in ev]
+    total_ms = max_over_ranks(float(sum(step_ms)), world)
+    flags = kv.kvgqa_read_status(ws1) | kv.kvgqa_read_status(ws2)
+    if flags:
+        raise RuntimeError(f"device status flags {flags} after the timed region")
+
+    attn_bytes, step_bytes = decode_bytes(wl, inp.positions.numpy())
+    tokens_per_s = wl.A * K * world / (total_ms / 1e3)
+    attn_avg_s = float(np.mean(attn_ms)) / 1e3
+    achieved = attn_bytes / attn_avg_s / 1e9
+
+    # ---- end to end: pinned host inputs -> device -> two calls -> host output
+    h_q, h_k, h_v = inp.q.pin_memory(), inp.k.pin_memory(), inp.v.pin_memory()
+    h_pos, h_rows = inp.positions.pin_memory(), inp.cache_rows.pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    d_pos, d_rows = torch.empty_like(pos), torch.empty_like(rows)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_pos, h_rows))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True); d_k.copy_(h_k, non_blocking=True); d_v.copy_(h_v, non_blocking=True)
+        d_pos.copy_(h_pos, non_blocking=True); d_rows.copy_(h_rows, non_blocking=True)
+        kv.rope_kv_store_out_(d_q, d_k, d_v, d_pos, d_rows, wl.theta, q_rot, kc, vc, ws1, stream)
+        kv.cached_gqa_attention_out_(q_rot, kc, vc, d_pos, d_rows, wl.scale, out, ws2, stream)
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    e2e_total = 0.0
+    barrier(world)
+    for _ in range(K):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_total += time.perf_counter() - t0
+    e2e_total = max_over_ranks(e2e_total, world)
+    e2e_value = wl.A * K * world / e2e_total
+
+    # ---- prefill: 16 prompts x 1024 tokens into empty rows
+    prefill = None
+    if not args.no_prefill:
+        prefill = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
+    clocks = sampler.stop() if sampler else None
+
+    if rank != 0:
+        return None
+    traffic = profile_traffic("flash_decode.cu", "flash_decode_splitk_llama_decode.md")
+    line = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "slots": wl.slots, "max_seq": wl.max_seq, "active_rows": wl.A,
+                   "H_q": wl.H_q, "H_kv": wl.H_kv, "head_dim": wl.D, "theta": wl.theta,
+                   "positions": "uniform [1,4096), seed 20261203", "l2": "flushed between timed steps (256 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "decode": {"attention_ms": round(attn_avg_s * 1e3, 5), "store_ms": round(float(np.mean(store_ms)), 5),
+                   "kv_bytes_per_step": attn_bytes, "step_bytes": step_bytes,
+                   "kv_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm_peak, 4),
+                   "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1)},
+        "roofline": {"kernel": "flash_decode_splitk + decode_combine (one cached_gqa_attention_out_ call)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    if prefill is not None:
+        line["prefill"] = prefill
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src):
+    pw = W.PREFILL
+    pin = W.make_prefill_inputs(pw)
+    q, k, v, rows = pin.q.to(dev), pin.k.to(dev), pin.v.to(dev), pin.cache_rows.to(dev)
+    kc, vc = pin.build_cache(dev)
+    out = torch.empty(pw.A, pw.T, pw.H_q, pw.D, dtype=torch.bfloat16, device=dev)
+    ws = kv.new_workspace(kv.prefill_gqa_cached_rows_workspace_size(pw.A, pw.T, pw.H_q, pw.H_kv, pw.D), dev)
+
+    def call():
+        kv.prefill_gqa_cached_rows_out_(q, k, v, rows, pw.theta, pw.scale, kc, vc, out, ws, stream)
+
+    try:
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+    except kv.KvgqaError as e:
+        return {"workload": pw.name, "unavailable": str(e)}
+    K = max(10, min(args.steps, 100))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    avg = max_over_ranks(float(np.mean(ms)), world)
+    flops = prefill_flops(pw)
+    tflops = flops / (avg / 1e3) / 1e12
+    if kv.kvgqa_read_status(ws):
+        raise RuntimeError("device status flags set in prefill")
+    return {"workload": pw.name, "ms_per_call": round(avg, 5), "causal_flops": flops,
+            "tflops": round(tflops, 1), "frac_of_bf16_peak": round(tflops / bf16_peak, 4),
+            "peak": bf16_peak, "peak_source": f"{peak_src} burst bf16_tflops",
+            "note": "whole call: RoPE + store of all prompts, then causal attention", "gpu_launches": 2 * K}
+
+
+# ---------------------------------------------------------------------- CPU oracle
+def oracle_decode_sample(target_seconds: float):
+    """Time the FP64 oracle on the decode step of the same workload: RoPE +
+    store of all 32 tokens, then attention of every (token, head), on a host
+    cache holding the 32 active rows.  Repeats whole steps until about
+    ``target_seconds`` have passed; returns (tokens, seconds, steps)."""
+    import oracle
+    wl = W.LLAMA_DECODE
+    inp = W.make_decode_inputs(wl)
+    rows = list(range(wl.A))
+    kc, vc = inp.compact_cache(rows, length=wl.max_seq)
+    kc_b, vc_b = W.bf16_bits(kc), W.bf16_bits(vc)
+    qb, kb, vb = W.bf16_bits(inp.q), W.bf16_bits(inp.k), W.bf16_bits(inp.v)
+    pos = inp.positions.numpy()
+    crow = np.arange(wl.A)
+    tokens, steps = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        q_rot, kc2, vc2 = oracle.rope_kv_store(qb, kb, vb, pos, crow, wl.theta, kc_b, vc_b)
+        oracle.cached_gqa_attention(q_rot, kc2, vc2, pos, crow, wl.scale)
+        tokens += wl.A
+        steps += 1
+        if time.perf_counter() - t0 >= target_seconds:
+            break
+    return tokens, time.perf_counter() - t0, steps
+
+
+def cpu_baseline(target_seconds: float):
+    tokens, secs, steps = oracle_decode_sample(target_seconds)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(tokens / secs, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{steps} whole decode step(s) of the same workload (32 tokens each) by the FP64 numpy "
+                      f"oracle in {secs:.1f} s; numpy/BLAS may use up to {cores} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    tokens, secs, steps = oracle_decode_sample(args.cpu_seconds)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    value = tokens / secs
+    wl = W.LLAMA_DECODE
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": 0, "ms_per_step": round(secs / steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "slots": wl.slots, "max_seq": wl.max_seq, "active_rows": wl.A,
+                       "H_q": wl.H_q, "H_kv": wl.H_kv, "head_dim": wl.D},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{steps} whole decode step(s), {secs:.1f} s"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    rank, world, local = dist_setup()
+    line = run_ours(args, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

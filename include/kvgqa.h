@@ -1,0 +1,219 @@
+/*
+ * kvgqa.h -- C ABI of the GB300 (sm_103a) cached GQA + RoPE decode/prefill path.
+ *
+ * One shared library, libkvgqa.so, exports the three operations of the
+ * positions-aware active-batch decode step over a shared slot KV cache and of
+ * its dense case, the equal-length prefill into empty cache rows
+ * (microLLM-rocm ARCHITECTURE.md, section "Tensor ownership boundary"):
+ *
+ *   rope_kv_store_out_            decode-only RoPE of Q/K at each row's own
+ *                                 position + K/V store into that row's cell
+ *   cached_gqa_attention_out_     GQA attention of each query over its row's
+ *                                 cached prefix (split-K + combine)
+ *   prefill_gqa_cached_rows_out_  A prompts of T tokens: RoPE, store into the
+ *                                 target empty rows, causal GQA attention
+ *
+ * Boundary conventions (same page, sections "Tensor ownership boundary" and
+ * "Stable integration boundary"):
+ *  - Every tensor crosses as a non-owning descriptor: pointer, accessible
+ *    bytes, shape, element strides, dtype and device.  The library never
+ *    allocates, frees or keeps a pointer after a call returns.
+ *  - Outputs, workspace, device and stream are explicit arguments; ownership
+ *    is never inferred from a pointer.
+ *  - Unsupported layouts are rejected with a status code, never copied into a
+ *    supported one behind the caller's back.
+ *  - Every check the host can make (dtype, rank, shape, contiguity, alignment,
+ *    device, aliasing, workspace size, scalar ranges) is made before any work
+ *    is queued, and failure returns a status with a message from
+ *    kvgqa_last_error(); nothing is launched then.
+ *  - Values that live only on the device (positions, cache rows) are checked
+ *    by the kernels: a row whose metadata is out of range is skipped (nothing
+ *    of it is read or written) and a flag is set in the workspace status block,
+ *    which kvgqa_read_status() returns on request.  The default path never
+ *    synchronises the stream.
+ *
+ * Data types: Q, K, V, the caches and the outputs are BF16; positions and cache
+ * rows are int32; softmax and accumulation run in FP32.
+ *
+ * Layouts (row-major, contiguous, element strides):
+ *   decode  q, q_out, out   [A, H_q, D]          k, v  [A, H_kv, D]
+ *   prefill q, out          [A, T, H_q, D]       k, v  [A, T, H_kv, D]   (BTHD)
+ *   caches  k_cache, v_cache [S, H_kv, max_seq, D]   (one layer; S cache slots)
+ *   positions, cache_rows   [A] int32
+ * with G = H_q / H_kv query heads per KV head, query head h reading KV head
+ * floor(h / G), and D in {64, 128}.
+ *
+ * Thread safety: calls are reentrant; kvgqa_last_error() is per host thread.
+ */
+#ifndef KVGQA_H_
+#define KVGQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVGQA_ABI_VERSION 1
+#define KVGQA_MAX_DIMS 6
+
+/* Element types of a descriptor. */
+typedef enum kvgqa_dtype {
+  KVGQA_BF16 = 1,
+  KVGQA_I32 = 2,
+  KVGQA_F32 = 3,
+  KVGQA_U8 = 4
+} kvgqa_dtype;
+
+/* Non-owning tensor descriptor.  `data` is a device pointer on `device` (it may
+ * be NULL only when the tensor has no elements); `bytes` is how many bytes are
+ * accessible from `data` on (the view must lie inside them); `strides` are in
+ * elements.  The caller keeps the memory alive until the queued work is done. */
+typedef struct kvgqa_tensor {
+  void* data;
+  int64_t bytes;
+  int32_t ndim;
+  int32_t dtype;   /* kvgqa_dtype */
+  int32_t device;  /* CUDA device ordinal */
+  int32_t reserved;
+  int64_t shape[KVGQA_MAX_DIMS];
+  int64_t strides[KVGQA_MAX_DIMS];
+} kvgqa_tensor;
+
+/* Return codes.  Anything but KVGQA_OK means nothing was queued. */
+typedef enum kvgqa_status {
+  KVGQA_OK = 0,
+  KVGQA_EINVAL = 1,      /* bad rank/shape/size/scalar, null descriptor */
+  KVGQA_EDTYPE = 2,      /* wrong element type */
+  KVGQA_ELAYOUT = 3,     /* non-contiguous strides or misaligned pointer */
+  KVGQA_EDEVICE = 4,     /* tensor not on the current device, or not device memory */
+  KVGQA_EALIAS = 5,      /* a written tensor overlaps another operand */
+  KVGQA_EWORKSPACE = 6,  /* workspace too small or misaligned */
+  KVGQA_ECUDA = 7,       /* a CUDA runtime call failed (message has the CUDA error) */
+  KVGQA_EUNSUPPORTED = 8 /* a legal shape this build has no kernel for (e.g. D = 96) */
+} kvgqa_status;
+
+/* Bits of the device status word (first 4 bytes of every workspace). */
+#define KVGQA_FLAG_POSITION_RANGE 0x1 /* some positions[a] outside [0, max_seq) */
+#define KVGQA_FLAG_ROW_RANGE 0x2      /* some cache_rows[a] outside [0, S) */
+#define KVGQA_FLAG_TIMEOUT 0x4        /* a bounded in-kernel wait expired; that work was dropped */
+
+/* Every workspace starts with a 256-byte status block; its first int32 is the
+ * status word.  Kernels only OR bits into it.  It must be zero before first use
+ * (a zero-filled workspace is ready); kvgqa_read_status() clears it. */
+#define KVGQA_STATUS_BYTES 256
+
+int kvgqa_abi_version(void);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* kvgqa_last_error(void);
+
+/* Workspace of rope_kv_store_out_: just the status block. */
+kvgqa_status rope_kv_store_workspace_size(size_t* bytes);
+
+/*
+ * rope_kv_store_out_ -- decode RoPE + K/V store for A active tokens.
+ *
+ * For every active token a with position p = positions[a] and row
+ * r = cache_rows[a]:
+ *   q_out[a, h, :]            = RoPE(q[a, h, :], p)    for h < H_q
+ *   k_cache[r, g, p, :]       = RoPE(k[a, g, :], p)    for g < H_kv
+ *   v_cache[r, g, p, :]       = v[a, g, :]             (bytes copied unchanged)
+ * and no other byte of the caches is written, so inactive rows and every other
+ * position stay as they were.  RoPE is split-half: pair i = (x[i], x[i+D/2])
+ * turns by angle p * theta^(-2i/D) (ARCHITECTURE.md, "Attention layout
+ * boundary": even D, nonnegative position, positive base).
+ *
+ *   q [A,H_q,D] bf16, k/v [A,H_kv,D] bf16, positions/cache_rows [A] int32  (read)
+ *   theta  RoPE base, finite and > 0
+ *   q_out [A,H_q,D] bf16  (written)
+ *   k_cache, v_cache [S,H_kv,max_seq,D] bf16  (one cell per token written)
+ *   workspace  >= rope_kv_store_workspace_size() bytes, 256-byte aligned
+ *   stream  cudaStream_t (NULL = legacy default stream)
+ * Preconditions the host cannot see: cache_rows distinct within the call
+ * (duplicates race); 0 <= positions[a] < max_seq and 0 <= cache_rows[a] < S, or
+ * the token is skipped and the status word flagged.  A = 0 is a no-op.
+ */
+kvgqa_status rope_kv_store_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
+                                const kvgqa_tensor* v, const kvgqa_tensor* positions,
+                                const kvgqa_tensor* cache_rows, double theta,
+                                const kvgqa_tensor* q_out, const kvgqa_tensor* k_cache,
+                                const kvgqa_tensor* v_cache, const kvgqa_tensor* workspace,
+                                void* stream);
+
+/* Workspace of cached_gqa_attention_out_ for these sizes on `device`: the
+ * status block plus FP32 split-K partials (it depends on the device's SM
+ * count, not on max_seq or the positions). */
+kvgqa_status cached_gqa_attention_workspace_size(int64_t A, int64_t H_q, int64_t H_kv,
+                                                 int64_t D, int32_t device, size_t* bytes);
+
+/*
+ * cached_gqa_attention_out_ -- cached GQA attention of the decode step.
+ *
+ * For every active token a and query head h, with p = positions[a],
+ * r = cache_rows[a], g = floor(h / G):
+ *   out[a,h,:] = sum_{j=0..p} softmax_j( scale * q_rot[a,h,:] . k_cache[r,g,j,:] )
+ *                * v_cache[r,g,j,:]
+ * i.e. the token attends to its row's prefix including its own position (the
+ * cell rope_kv_store_out_ just wrote).  Scores, softmax and the weighted sum
+ * are FP32; out is rounded to BF16 once.  Nothing past position p of a row is
+ * read.  The work is split over the whole GPU by key ranges; partial results
+ * meet in a combine kernel.
+ *
+ *   q_rot [A,H_q,D] bf16, k_cache/v_cache [S,H_kv,max_seq,D] bf16,
+ *   positions/cache_rows [A] int32  (read)
+ *   scale  finite (1/sqrt(D) is the usual choice)
+ *   out [A,H_q,D] bf16 (written; rows with invalid metadata are left unwritten)
+ *   workspace  >= cached_gqa_attention_workspace_size(...) bytes, 256-byte aligned
+ * Limits: D in {64,128}; G a divisor pattern with G <= 16 (G <= 8 for D = 64);
+ * A <= 2048; A * H_kv * max_seq < 2^31.  A = 0 is a no-op.
+ */
+kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_tensor* k_cache,
+                                       const kvgqa_tensor* v_cache,
+                                       const kvgqa_tensor* positions,
+                                       const kvgqa_tensor* cache_rows, float scale,
+                                       const kvgqa_tensor* out, const kvgqa_tensor* workspace,
+                                       void* stream);
+
+/* Workspace of prefill_gqa_cached_rows_out_: the status block plus the rotated
+ * queries (A*T*H_q*D bf16). */
+kvgqa_status prefill_gqa_cached_rows_workspace_size(int64_t A, int64_t T, int64_t H_q,
+                                                    int64_t H_kv, int64_t D, size_t* bytes);
+
+/*
+ * prefill_gqa_cached_rows_out_ -- equal-length prefill into empty rows.
+ *
+ * A prompts of T tokens each, at positions 0..T-1 (the target rows are empty;
+ * ARCHITECTURE.md, "Tensor ownership boundary": equal-length pending prompts run
+ * as one batch and each prefix lands in its target empty shared-cache row).
+ * With r = cache_rows[a]:
+ *   k_cache[r, g, t, :] = RoPE(k[a, t, g, :], t),  v_cache[r, g, t, :] = v[a, t, g, :]
+ *   for t < T; nothing else in the caches is written;
+ *   out[a, t, h, :] = causal GQA attention of RoPE(q[a,t,h,:], t) over cached
+ *   positions 0..t of row r, KV head floor(h/G), scores scaled by `scale`.
+ * The prompts are written straight into their rows (no temporary cache).
+ *
+ *   q [A,T,H_q,D], k/v [A,T,H_kv,D] bf16 (BTHD), cache_rows [A] int32 (read)
+ *   theta > 0, scale finite
+ *   k_cache/v_cache [S,H_kv,max_seq,D] bf16 with T <= max_seq (rows r written)
+ *   out [A,T,H_q,D] bf16 (written)
+ *   workspace >= prefill_gqa_cached_rows_workspace_size(...) bytes, 256-byte aligned
+ * Precondition: cache_rows distinct.  A = 0 or T = 0 is a no-op.
+ */
+kvgqa_status prefill_gqa_cached_rows_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
+                                          const kvgqa_tensor* v, const kvgqa_tensor* cache_rows,
+                                          double theta, float scale, const kvgqa_tensor* k_cache,
+                                          const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
+                                          const kvgqa_tensor* workspace, void* stream);
+
+/* Opt-in: synchronise `stream`, return the status word of `workspace` in
+ * *flags (KVGQA_FLAG_* bits; 0 = every device-side check passed) and clear it.
+ * This is the only call that waits for the device. */
+kvgqa_status kvgqa_read_status(const kvgqa_tensor* workspace, void* stream, int32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVGQA_H_ */

@@ -1,0 +1,182 @@
+"""Python binding of libkvgqa, the GB300 cached GQA + RoPE decode/prefill path.
+
+Argument marshalling only: torch tensors become non-owning C descriptors
+(pointer, accessible bytes, shape, element strides, dtype, device) and the
+current torch CUDA stream is passed explicitly.  Every step of the path runs
+in the library's CUDA kernels; there is no fallback of any kind.  If the
+library has not been built, importing this package raises.
+
+Functions keep the names of the C entry points:
+
+    rope_kv_store_out_(q, k, v, positions, cache_rows, theta, q_out, k_cache, v_cache, workspace)
+    cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_rows, scale, out, workspace)
+    prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_cache, out, workspace)
+
+plus the workspace-size queries and ``kvgqa_read_status``.  Shapes, layouts
+and the meaning of every argument are documented in ``include/kvgqa.h``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libkvgqa.so")
+
+KVGQA_BF16, KVGQA_I32, KVGQA_F32, KVGQA_U8 = 1, 2, 3, 4
+STATUS_NAMES = {0: "OK", 1: "EINVAL", 2: "EDTYPE", 3: "ELAYOUT", 4: "EDEVICE", 5: "EALIAS",
+                6: "EWORKSPACE", 7: "ECUDA", 8: "EUNSUPPORTED"}
+FLAG_POSITION_RANGE, FLAG_ROW_RANGE, FLAG_TIMEOUT = 0x1, 0x2, 0x4
+STATUS_BYTES = 256
+_DTYPES = {torch.bfloat16: KVGQA_BF16, torch.int32: KVGQA_I32, torch.float32: KVGQA_F32,
+           torch.uint8: KVGQA_U8}
+
+
+class KvgqaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("bytes", ctypes.c_int64), ("ndim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("device", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 6), ("strides", ctypes.c_int64 * 6)]
+
+
+class KvgqaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.code = STATUS_NAMES.get(status, str(status))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` "
+                          "or `python kv_cached_gqa_rope_gb300/build.py`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(KvgqaTensor)
+    st = ctypes.c_int
+    lib.kvgqa_abi_version.restype = ctypes.c_int
+    lib.kvgqa_last_error.restype = ctypes.c_char_p
+    lib.rope_kv_store_workspace_size.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+    lib.rope_kv_store_workspace_size.restype = st
+    lib.rope_kv_store_out_.argtypes = [P, P, P, P, P, ctypes.c_double, P, P, P, P, ctypes.c_void_p]
+    lib.rope_kv_store_out_.restype = st
+    lib.cached_gqa_attention_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.cached_gqa_attention_workspace_size.restype = st
+    lib.cached_gqa_attention_out_.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_void_p]
+    lib.cached_gqa_attention_out_.restype = st
+    lib.prefill_gqa_cached_rows_workspace_size.argtypes = [ctypes.c_int64] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.prefill_gqa_cached_rows_workspace_size.restype = st
+    lib.prefill_gqa_cached_rows_out_.argtypes = [P, P, P, P, ctypes.c_double, ctypes.c_float, P, P, P, P, ctypes.c_void_p]
+    lib.prefill_gqa_cached_rows_out_.restype = st
+    lib.kvgqa_read_status.argtypes = [P, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    lib.kvgqa_read_status.restype = st
+    return lib
+
+
+_lib = _load()
+
+EXPORTED_SYMBOLS = ("kvgqa_abi_version", "kvgqa_last_error", "rope_kv_store_workspace_size",
+                    "rope_kv_store_out_", "cached_gqa_attention_workspace_size",
+                    "cached_gqa_attention_out_", "prefill_gqa_cached_rows_workspace_size",
+                    "prefill_gqa_cached_rows_out_", "kvgqa_read_status")
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def abi_version() -> int:
+    return _lib.kvgqa_abi_version()
+
+
+def describe(t: torch.Tensor) -> KvgqaTensor:
+    """Non-owning descriptor of a torch tensor (no copy, no check)."""
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    d = KvgqaTensor()
+    d.data = t.data_ptr() if t.numel() else None
+    st = t.untyped_storage()
+    d.bytes = st.nbytes() - t.storage_offset() * t.element_size()
+    d.ndim = t.dim()
+    d.dtype = _DTYPES[t.dtype]
+    d.device = t.device.index if t.device.type == "cuda" else -1
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.strides[i] = t.stride(i)
+    return d
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        # Without a usable CUDA device there is no current stream; pass the
+        # default stream and let the library report the device error.
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else 0
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int):
+    if status != 0:
+        raise KvgqaError(status, _lib.kvgqa_last_error().decode())
+
+
+def _ref(d: KvgqaTensor):
+    return ctypes.byref(d)
+
+
+def rope_kv_store_workspace_size() -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.rope_kv_store_workspace_size(ctypes.byref(n)))
+    return n.value
+
+
+def cached_gqa_attention_workspace_size(A: int, H_q: int, H_kv: int, D: int, device: int = None) -> int:
+    if device is None:
+        device = torch.cuda.current_device()
+    n = ctypes.c_size_t()
+    _check(_lib.cached_gqa_attention_workspace_size(A, H_q, H_kv, D, device, ctypes.byref(n)))
+    return n.value
+
+
+def prefill_gqa_cached_rows_workspace_size(A: int, T: int, H_q: int, H_kv: int, D: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.prefill_gqa_cached_rows_workspace_size(A, T, H_q, H_kv, D, ctypes.byref(n)))
+    return n.value
+
+
+def rope_kv_store_out_(q, k, v, positions, cache_rows, theta, q_out, k_cache, v_cache, workspace,
+                       stream=None) -> None:
+    ds = [describe(t) for t in (q, k, v, positions, cache_rows)]
+    outs = [describe(t) for t in (q_out, k_cache, v_cache, workspace)]
+    _check(_lib.rope_kv_store_out_(*map(_ref, ds), float(theta), *map(_ref, outs), _stream(stream)))
+
+
+def cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_rows, scale, out, workspace,
+                              stream=None) -> None:
+    ds = [describe(t) for t in (q_rot, k_cache, v_cache, positions, cache_rows)]
+    o, w = describe(out), describe(workspace)
+    _check(_lib.cached_gqa_attention_out_(*map(_ref, ds), float(scale), _ref(o), _ref(w), _stream(stream)))
+
+
+def prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_cache, out, workspace,
+                                 stream=None) -> None:
+    ds = [describe(t) for t in (q, k, v, cache_rows)]
+    outs = [describe(t) for t in (k_cache, v_cache, out, workspace)]
+    _check(_lib.prefill_gqa_cached_rows_out_(*map(_ref, ds), float(theta), float(scale),
+                                             *map(_ref, outs), _stream(stream)))
+
+
+def kvgqa_read_status(workspace, stream=None) -> int:
+    """Synchronise the stream, return and clear the workspace status word."""
+    w = describe(workspace)
+    flags = ctypes.c_int32()
+    _check(_lib.kvgqa_read_status(_ref(w), _stream(stream), ctypes.byref(flags)))
+    return flags.value
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace (status word clear), 256-byte aligned."""
+    return torch.zeros(max(int(nbytes), STATUS_BYTES), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")

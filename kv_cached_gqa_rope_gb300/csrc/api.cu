@@ -1,0 +1,422 @@
+// C ABI of libkvgqa: descriptor validation and kernel dispatch.
+//
+// Boundary rules (microLLM-rocm ARCHITECTURE.md, sections "Tensor ownership
+// boundary", "Tensor N0 invariants" and "Stable integration boundary";
+// operator-development.md, "Public interfaces"): tensors arrive as non-owning
+// descriptors; outputs, workspace, device and stream are explicit; zero-sized
+// dimensions are valid; negative sizes are rejected; unsupported layouts are
+// rejected rather than copied; alias, shape, dtype, device and contiguity
+// errors are explicit.  Every check here reads host memory only, so a call
+// never waits for the device (except kvgqa_read_status, which exists to wait).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "kvgqa.h"
+#include "kvgqa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+struct Fail {
+  kvgqa_status code;
+};
+
+[[noreturn]] void fail(kvgqa_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  throw Fail{code};
+}
+
+void check_cuda(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) fail(KVGQA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int64_t elem_size(int32_t dtype) {
+  switch (dtype) {
+    case KVGQA_BF16: return 2;
+    case KVGQA_I32: return 4;
+    case KVGQA_F32: return 4;
+    case KVGQA_U8: return 1;
+  }
+  return 0;
+}
+
+const char* dtype_name(int32_t dtype) {
+  switch (dtype) {
+    case KVGQA_BF16: return "bf16";
+    case KVGQA_I32: return "int32";
+    case KVGQA_F32: return "float32";
+    case KVGQA_U8: return "uint8";
+  }
+  return "unknown";
+}
+
+int64_t numel(const kvgqa_tensor& t) {
+  int64_t n = 1;
+  for (int i = 0; i < t.ndim; ++i) n *= t.shape[i];
+  return n;
+}
+
+// A view: its name, descriptor and the byte range it touches.
+struct View {
+  const char* name;
+  const kvgqa_tensor* t;
+  uintptr_t lo = 0, hi = 0;  // [lo, hi) bytes used
+};
+
+// Checks common to every operand that read only the descriptor: rank, dtype,
+// non-negative sizes, row-major contiguity, accessible bytes and alignment.
+View check_tensor(const char* name, const kvgqa_tensor* t, int ndim, int32_t dtype, int64_t align) {
+  if (!t) fail(KVGQA_EINVAL, "%s: null descriptor", name);
+  if (t->ndim != ndim) fail(KVGQA_EINVAL, "%s: expected rank %d, got %d", name, ndim, t->ndim);
+  if (t->dtype != dtype)
+    fail(KVGQA_EDTYPE, "%s: expected %s, got %s", name, dtype_name(dtype), dtype_name(t->dtype));
+  int64_t expect = 1;
+  for (int i = ndim - 1; i >= 0; --i) {
+    if (t->shape[i] < 0) fail(KVGQA_EINVAL, "%s: negative size in dim %d", name, i);
+    if (t->strides[i] < 0) fail(KVGQA_ELAYOUT, "%s: negative stride in dim %d", name, i);
+    if (t->shape[i] > 1 && t->strides[i] != expect)
+      fail(KVGQA_ELAYOUT, "%s: not contiguous row-major (dim %d stride %lld, expected %lld)", name,
+           i, (long long)t->strides[i], (long long)expect);
+    expect *= t->shape[i];
+  }
+  View v{name, t};
+  const int64_t bytes = numel(*t) * elem_size(dtype);
+  if (bytes == 0) return v;
+  if (!t->data) fail(KVGQA_EINVAL, "%s: null data with %lld elements", name, (long long)numel(*t));
+  if (t->bytes < bytes)
+    fail(KVGQA_EINVAL, "%s: view needs %lld bytes, descriptor allows %lld", name, (long long)bytes,
+         (long long)t->bytes);
+  if (reinterpret_cast<uintptr_t>(t->data) % align)
+    fail(KVGQA_ELAYOUT, "%s: data pointer not %lld-byte aligned", name, (long long)align);
+  v.lo = reinterpret_cast<uintptr_t>(t->data);
+  v.hi = v.lo + static_cast<uintptr_t>(bytes);
+  return v;
+}
+
+// The device checks: the declared device is the current one, and CUDA knows
+// the pointer as device (or managed) memory of that device.
+void check_device(std::initializer_list<const View*> views, int device) {
+  for (const View* v : views) {
+    if (v->lo == v->hi) continue;
+    const kvgqa_tensor* t = v->t;
+    if (t->device != device)
+      fail(KVGQA_EDEVICE, "%s: on device %d, current device is %d", v->name, t->device, device);
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, t->data) != cudaSuccess) {
+      cudaGetLastError();
+      fail(KVGQA_EDEVICE, "%s: pointer not known to CUDA", v->name);
+    }
+    if ((attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) ||
+        attr.device != device)
+      fail(KVGQA_EDEVICE, "%s: not device memory of device %d", v->name, device);
+  }
+}
+
+void require_shape(const View& v, std::initializer_list<int64_t> dims) {
+  int i = 0;
+  for (int64_t d : dims) {
+    if (v.t->shape[i] != d)
+      fail(KVGQA_EINVAL, "%s: dim %d is %lld, expected %lld", v.name, i, (long long)v.t->shape[i],
+           (long long)d);
+    ++i;
+  }
+}
+
+bool overlap(const View& a, const View& b) {
+  return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+// A written view must not share a byte with any other operand.
+void check_no_alias(std::initializer_list<const View*> written,
+                    std::initializer_list<const View*> all) {
+  for (const View* w : written)
+    for (const View* o : all)
+      if (w != o && overlap(*w, *o)) fail(KVGQA_EALIAS, "%s overlaps %s", w->name, o->name);
+}
+
+int current_device() {
+  int dev = -1;
+  check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+  return dev;
+}
+
+void check_head_dim(int64_t D) {
+  if (D <= 0 || D % 2) fail(KVGQA_EINVAL, "head width D=%lld must be even and positive", (long long)D);
+  if (D != 64 && D != 128) fail(KVGQA_EUNSUPPORTED, "head width D=%lld: kernels exist for 64 and 128", (long long)D);
+}
+
+void check_heads(int64_t H_q, int64_t H_kv) {
+  if (H_q <= 0 || H_kv <= 0 || H_q % H_kv)
+    fail(KVGQA_EINVAL, "H_q=%lld must be a positive multiple of H_kv=%lld", (long long)H_q, (long long)H_kv);
+}
+
+void check_theta(double theta) {
+  if (!(theta > 0.0) || !std::isfinite(theta)) fail(KVGQA_EINVAL, "RoPE base theta must be finite and > 0");
+}
+
+void fill_inv_freq(double* out, int D, double theta) {
+  for (int i = 0; i < D / 2; ++i) out[i] = std::pow(theta, -2.0 * i / D);
+}
+
+View check_workspace(const kvgqa_tensor* ws, size_t need) {
+  if (!ws) fail(KVGQA_EINVAL, "workspace: null descriptor");
+  if (ws->ndim != 1 || ws->dtype != KVGQA_U8)
+    fail(KVGQA_EWORKSPACE, "workspace: expected a rank-1 uint8 buffer");
+  if (ws->shape[0] < static_cast<int64_t>(need))
+    fail(KVGQA_EWORKSPACE, "workspace: %lld bytes, need %zu", (long long)ws->shape[0], need);
+  if (reinterpret_cast<uintptr_t>(ws->data) % 256)
+    fail(KVGQA_EWORKSPACE, "workspace: data pointer not 256-byte aligned");
+  return check_tensor("workspace", ws, 1, KVGQA_U8, 256);
+}
+
+template <typename F>
+kvgqa_status guarded(F&& f) {
+  try {
+    f();
+    g_last_error.clear();
+    return KVGQA_OK;
+  } catch (const Fail& e) {
+    return e.code;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvgqa_abi_version(void) { return KVGQA_ABI_VERSION; }
+
+const char* kvgqa_last_error(void) { return g_last_error.c_str(); }
+
+kvgqa_status rope_kv_store_workspace_size(size_t* bytes) {
+  return guarded([&] {
+    if (!bytes) fail(KVGQA_EINVAL, "bytes: null");
+    *bytes = KVGQA_STATUS_BYTES;
+  });
+}
+
+kvgqa_status rope_kv_store_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
+                                const kvgqa_tensor* v, const kvgqa_tensor* positions,
+                                const kvgqa_tensor* cache_rows, double theta,
+                                const kvgqa_tensor* q_out, const kvgqa_tensor* k_cache,
+                                const kvgqa_tensor* v_cache, const kvgqa_tensor* workspace,
+                                void* stream) {
+  return guarded([&] {
+    if (!q || !k_cache) fail(KVGQA_EINVAL, "null descriptor");
+    if (q->ndim != 3 || k_cache->ndim != 4) fail(KVGQA_EINVAL, "q must be [A,H_q,D], caches [S,H_kv,max_seq,D]");
+    const int64_t A = q->shape[0], H_q = q->shape[1], D = q->shape[2];
+    const int64_t S = k_cache->shape[0], H_kv = k_cache->shape[1], max_seq = k_cache->shape[2];
+    check_head_dim(D);
+    check_heads(H_q, H_kv);
+    check_theta(theta);
+    View vq = check_tensor("q", q, 3, KVGQA_BF16, 16);
+    View vk = check_tensor("k", k, 3, KVGQA_BF16, 16);
+    View vv = check_tensor("v", v, 3, KVGQA_BF16, 16);
+    View vp = check_tensor("positions", positions, 1, KVGQA_I32, 4);
+    View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
+    View vqo = check_tensor("q_out", q_out, 3, KVGQA_BF16, 16);
+    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+    View vws = check_workspace(workspace, KVGQA_STATUS_BYTES);
+    require_shape(vk, {A, H_kv, D});
+    require_shape(vv, {A, H_kv, D});
+    require_shape(vp, {A});
+    require_shape(vr, {A});
+    require_shape(vqo, {A, H_q, D});
+    require_shape(vkc, {S, H_kv, max_seq, D});
+    require_shape(vvc, {S, H_kv, max_seq, D});
+    check_no_alias({&vqo, &vkc, &vvc, &vws}, {&vq, &vk, &vv, &vp, &vr, &vqo, &vkc, &vvc, &vws});
+    const int dev = current_device();
+    check_device({&vq, &vk, &vv, &vp, &vr, &vqo, &vkc, &vvc, &vws}, dev);
+    if (A == 0) return;
+    if (A > (1ll << 31) - 1) fail(KVGQA_EINVAL, "A too large");
+    kvgqa::RopeStoreParams p{};
+    p.q = static_cast<const uint16_t*>(q->data);
+    p.k = static_cast<const uint16_t*>(k->data);
+    p.v = static_cast<const uint16_t*>(v->data);
+    p.positions = static_cast<const int32_t*>(positions->data);
+    p.cache_rows = static_cast<const int32_t*>(cache_rows->data);
+    p.q_out = static_cast<uint16_t*>(q_out->data);
+    p.k_cache = static_cast<uint16_t*>(k_cache->data);
+    p.v_cache = static_cast<uint16_t*>(v_cache->data);
+    p.status = static_cast<int32_t*>(workspace->data);
+    p.A = (int)A; p.T = 1; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.D = (int)D;
+    p.S = (int)S; p.max_seq = (int)max_seq;
+    fill_inv_freq(p.inv_freq, (int)D, theta);
+    check_cuda(kvgqa::launch_rope_kv_store(p, false, static_cast<cudaStream_t>(stream)),
+               "rope_kv_store launch");
+  });
+}
+
+kvgqa_status cached_gqa_attention_workspace_size(int64_t A, int64_t H_q, int64_t H_kv, int64_t D,
+                                                 int32_t device, size_t* bytes) {
+  return guarded([&] {
+    if (!bytes) fail(KVGQA_EINVAL, "bytes: null");
+    if (A < 0) fail(KVGQA_EINVAL, "A < 0");
+    check_head_dim(D);
+    check_heads(H_q, H_kv);
+    const int G = (int)(H_q / H_kv);
+    if (G > 8) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 8", G);
+    int ctas = 0;
+    size_t part = 0;
+    check_cuda(kvgqa::decode_launch_shape(device, (int)D, kvgqa::decode_group_pad(G), &ctas, &part),
+               "decode kernel set-up");
+    *bytes = KVGQA_STATUS_BYTES + part;
+  });
+}
+
+kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_tensor* k_cache,
+                                       const kvgqa_tensor* v_cache, const kvgqa_tensor* positions,
+                                       const kvgqa_tensor* cache_rows, float scale,
+                                       const kvgqa_tensor* out, const kvgqa_tensor* workspace,
+                                       void* stream) {
+  return guarded([&] {
+    if (!q_rot || !k_cache) fail(KVGQA_EINVAL, "null descriptor");
+    if (q_rot->ndim != 3 || k_cache->ndim != 4) fail(KVGQA_EINVAL, "q_rot must be [A,H_q,D], caches [S,H_kv,max_seq,D]");
+    const int64_t A = q_rot->shape[0], H_q = q_rot->shape[1], D = q_rot->shape[2];
+    const int64_t S = k_cache->shape[0], H_kv = k_cache->shape[1], max_seq = k_cache->shape[2];
+    check_head_dim(D);
+    check_heads(H_q, H_kv);
+    if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
+    const int G = (int)(H_q / H_kv);
+    if (G > 8) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 8", G);
+    if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
+    if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
+    View vq = check_tensor("q_rot", q_rot, 3, KVGQA_BF16, 16);
+    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+    View vp = check_tensor("positions", positions, 1, KVGQA_I32, 4);
+    View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
+    View vo = check_tensor("out", out, 3, KVGQA_BF16, 16);
+    require_shape(vvc, {S, H_kv, max_seq, D});
+    require_shape(vp, {A});
+    require_shape(vr, {A});
+    require_shape(vo, {A, H_q, D});
+    View vws0 = check_workspace(workspace, KVGQA_STATUS_BYTES);
+    check_no_alias({&vo, &vws0}, {&vq, &vkc, &vvc, &vp, &vr, &vo, &vws0});
+    const int dev = current_device();
+    int ctas = 0;
+    size_t part = 0;
+    check_cuda(kvgqa::decode_launch_shape(dev, (int)D, kvgqa::decode_group_pad(G), &ctas, &part),
+               "decode kernel set-up");
+    View vws = check_workspace(workspace, KVGQA_STATUS_BYTES + part);
+    check_device({&vq, &vkc, &vvc, &vp, &vr, &vo, &vws}, dev);
+    if (A == 0) return;
+    kvgqa::DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q_rot->data);
+    p.k_cache = static_cast<const uint16_t*>(k_cache->data);
+    p.v_cache = static_cast<const uint16_t*>(v_cache->data);
+    p.positions = static_cast<const int32_t*>(positions->data);
+    p.cache_rows = static_cast<const int32_t*>(cache_rows->data);
+    p.out = static_cast<uint16_t*>(out->data);
+    p.status = static_cast<int32_t*>(workspace->data);
+    p.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace->data) + KVGQA_STATUS_BYTES);
+    p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
+    p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = ctas;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    check_cuda(kvgqa::launch_cached_gqa_attention(p, static_cast<cudaStream_t>(stream)),
+               "cached_gqa_attention launch");
+  });
+}
+
+kvgqa_status prefill_gqa_cached_rows_workspace_size(int64_t A, int64_t T, int64_t H_q, int64_t H_kv,
+                                                    int64_t D, size_t* bytes) {
+  return guarded([&] {
+    if (!bytes) fail(KVGQA_EINVAL, "bytes: null");
+    if (A < 0 || T < 0) fail(KVGQA_EINVAL, "negative size");
+    check_head_dim(D);
+    check_heads(H_q, H_kv);
+    *bytes = KVGQA_STATUS_BYTES + static_cast<size_t>(A) * T * H_q * D * 2;
+  });
+}
+
+kvgqa_status prefill_gqa_cached_rows_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
+                                          const kvgqa_tensor* v, const kvgqa_tensor* cache_rows,
+                                          double theta, float scale, const kvgqa_tensor* k_cache,
+                                          const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
+                                          const kvgqa_tensor* workspace, void* stream) {
+  return guarded([&] {
+    if (!q || !k_cache) fail(KVGQA_EINVAL, "null descriptor");
+    if (q->ndim != 4 || k_cache->ndim != 4) fail(KVGQA_EINVAL, "q must be [A,T,H_q,D], caches [S,H_kv,max_seq,D]");
+    const int64_t A = q->shape[0], T = q->shape[1], H_q = q->shape[2], D = q->shape[3];
+    const int64_t S = k_cache->shape[0], H_kv = k_cache->shape[1], max_seq = k_cache->shape[2];
+    check_head_dim(D);
+    check_heads(H_q, H_kv);
+    check_theta(theta);
+    if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
+    if (T > max_seq) fail(KVGQA_EINVAL, "T=%lld exceeds max_seq=%lld", (long long)T, (long long)max_seq);
+    View vq = check_tensor("q", q, 4, KVGQA_BF16, 16);
+    View vk = check_tensor("k", k, 4, KVGQA_BF16, 16);
+    View vv = check_tensor("v", v, 4, KVGQA_BF16, 16);
+    View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
+    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+    View vo = check_tensor("out", out, 4, KVGQA_BF16, 16);
+    require_shape(vk, {A, T, H_kv, D});
+    require_shape(vv, {A, T, H_kv, D});
+    require_shape(vr, {A});
+    require_shape(vvc, {S, H_kv, max_seq, D});
+    require_shape(vo, {A, T, H_q, D});
+    const size_t need = KVGQA_STATUS_BYTES + static_cast<size_t>(A) * T * H_q * D * 2;
+    View vws = check_workspace(workspace, need);
+    check_no_alias({&vkc, &vvc, &vo, &vws}, {&vq, &vk, &vv, &vr, &vkc, &vvc, &vo, &vws});
+    const int dev = current_device();
+    check_device({&vq, &vk, &vv, &vr, &vkc, &vvc, &vo, &vws}, dev);
+    if (A == 0 || T == 0) return;
+    kvgqa::RopeStoreParams rp{};
+    unsigned char* ws = static_cast<unsigned char*>(workspace->data);
+    uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + KVGQA_STATUS_BYTES);
+    rp.q = static_cast<const uint16_t*>(q->data);
+    rp.k = static_cast<const uint16_t*>(k->data);
+    rp.v = static_cast<const uint16_t*>(v->data);
+    rp.positions = nullptr;
+    rp.cache_rows = static_cast<const int32_t*>(cache_rows->data);
+    rp.q_out = q_rot;
+    rp.k_cache = static_cast<uint16_t*>(k_cache->data);
+    rp.v_cache = static_cast<uint16_t*>(v_cache->data);
+    rp.status = reinterpret_cast<int32_t*>(ws);
+    rp.A = (int)A; rp.T = (int)T; rp.H_q = (int)H_q; rp.H_kv = (int)H_kv; rp.D = (int)D;
+    rp.S = (int)S; rp.max_seq = (int)max_seq;
+    fill_inv_freq(rp.inv_freq, (int)D, theta);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    check_cuda(kvgqa::launch_rope_kv_store(rp, true, st), "prefill rope_kv_store launch");
+    kvgqa::PrefillParams pp{};
+    pp.q_rot = q_rot;
+    pp.k_cache = rp.k_cache;
+    pp.v_cache = rp.v_cache;
+    pp.cache_rows = rp.cache_rows;
+    pp.out = static_cast<uint16_t*>(out->data);
+    pp.status = rp.status;
+    pp.A = (int)A; pp.T = (int)T; pp.H_q = (int)H_q; pp.H_kv = (int)H_kv; pp.G = (int)(H_q / H_kv);
+    pp.D = (int)D; pp.S = (int)S; pp.max_seq = (int)max_seq;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+    check_cuda(kvgqa::launch_prefill_attention(pp, st), "prefill attention launch");
+  });
+}
+
+kvgqa_status kvgqa_read_status(const kvgqa_tensor* workspace, void* stream, int32_t* flags) {
+  return guarded([&] {
+    if (!flags) fail(KVGQA_EINVAL, "flags: null");
+    View vws = check_workspace(workspace, KVGQA_STATUS_BYTES);
+    check_device({&vws}, current_device());
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t h = 0;
+    check_cuda(cudaMemcpyAsync(&h, workspace->data, sizeof h, cudaMemcpyDeviceToHost, st), "status read");
+    check_cuda(cudaMemsetAsync(workspace->data, 0, sizeof h, st), "status clear");
+    check_cuda(cudaStreamSynchronize(st), "stream synchronize");
+    *flags = h;
+  });
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvgqa {
+
+constexpr int kMaxHeadDim = 128;
+constexpr int kMaxActiveRows = 2048;  // decode attention keeps a prefix table of A+1 ints in smem
+
+// ------------------------------------------------------------------ RoPE + store
+struct RopeStoreParams {
+  const uint16_t* q;         // decode [A,H_q,D]; prefill [A,T,H_q,D]
+  const uint16_t* k;         // decode [A,H_kv,D]; prefill [A,T,H_kv,D]
+  const uint16_t* v;
+  const int32_t* positions;  // decode [A]; prefill: nullptr (positions are 0..T-1)
+  const int32_t* cache_rows; // [A]
+  uint16_t* q_out;           // rotated Q, same layout as q
+  uint16_t* k_cache;         // [S,H_kv,max_seq,D]
+  uint16_t* v_cache;
+  int32_t* status;
+  int A, T, H_q, H_kv, D, S, max_seq;
+  double inv_freq[kMaxHeadDim / 2];  // theta^(-2i/D), computed on the host in double
+};
+
+cudaError_t launch_rope_kv_store(const RopeStoreParams& p, bool prefill, cudaStream_t stream);
+
+// ------------------------------------------------------------------ decode attention
+struct DecodeParams {
+  const uint16_t* q;          // [A,H_q,D] rotated queries
+  const uint16_t* k_cache;    // [S,H_kv,max_seq,D]
+  const uint16_t* v_cache;
+  const int32_t* positions;   // [A]
+  const int32_t* cache_rows;  // [A]
+  uint16_t* out;              // [A,H_q,D]
+  float* partials;            // split-K partial results (workspace)
+  int32_t* status;
+  int A, H_q, H_kv, G, D, S, max_seq;
+  int num_ctas;               // grid size of the split-K kernel
+  float scale_log2;           // scale * log2(e)
+};
+
+// Padded group size used by the decode kernels: the next power of two >= G.
+int decode_group_pad(int G);
+// Grid size of the split-K kernel on `device`, and the partial-buffer bytes.
+cudaError_t decode_launch_shape(int device, int D, int GP, int* num_ctas, size_t* partial_bytes);
+cudaError_t launch_cached_gqa_attention(const DecodeParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------ prefill attention
+struct PrefillParams {
+  const uint16_t* q_rot;      // [A,T,H_q,D] rotated queries (workspace)
+  const uint16_t* k_cache;    // [S,H_kv,max_seq,D]
+  const uint16_t* v_cache;
+  const int32_t* cache_rows;  // [A]
+  uint16_t* out;              // [A,T,H_q,D]
+  int32_t* status;
+  int A, T, H_q, H_kv, G, D, S, max_seq;
+  float scale_log2;
+};
+
+cudaError_t launch_prefill_attention(const PrefillParams& p, cudaStream_t stream);
+
+}  // namespace kvgqa

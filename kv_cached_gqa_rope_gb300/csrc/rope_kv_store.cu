@@ -1,0 +1,166 @@
+// K1: split-half RoPE of Q and K at each token's own position, fused with the
+// K/V store into the token's cache cell.
+//
+// microLLM-rocm ARCHITECTURE.md, section "Tensor ownership boundary": device
+// positions[A] and cache_rows[A] parameterise decode-only RoPE and the K/V
+// store; inactive full-capacity rows stay untouched.  Section "Attention layout
+// boundary": split-half RoPE needs an even head width, a nonnegative position
+// and a positive base.  The same kernel serves the prefill into empty rows,
+// where token (a, t) sits at position t of row cache_rows[a].
+//
+// One CTA owns one position.  It evaluates the D/2 angles pos * theta^(-2i/D)
+// once, in FP64, and keeps cos/sin as FP32 hi+lo pairs in shared memory; every
+// token at that position (one in decode, A in prefill) then streams its heads
+// through 16-byte vector loads and stores.  The rotation is evaluated with
+// FP32 error-free products so that the BF16 result is within one rounding of
+// the exact value even where x cos - y sin cancels.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kvgqa_internal.h"
+#include "ptx.cuh"
+
+namespace kvgqa {
+namespace {
+
+struct CosSin {
+  float ch, cl, sh, sl;  // cos = ch + cl, sin = sh + sl
+};
+
+// x1 * C - x2 * S with C, S given as hi+lo pairs.  Products are split exactly
+// with FMA; intrinsics keep the compiler from contracting them differently.
+__device__ __forceinline__ float rot_first(float x1, float x2, const CosSin& cs) {
+  const float p = __fmul_rn(x1, cs.ch);
+  const float pe = __fmaf_rn(x1, cs.ch, -p);
+  const float q = __fmul_rn(x2, cs.sh);
+  const float qe = __fmaf_rn(x2, cs.sh, -q);
+  const float lo = __fmaf_rn(x1, cs.cl, __fmaf_rn(-x2, cs.sl, __fsub_rn(pe, qe)));
+  return __fadd_rn(__fsub_rn(p, q), lo);
+}
+
+// x2 * C + x1 * S.
+__device__ __forceinline__ float rot_second(float x1, float x2, const CosSin& cs) {
+  const float p = __fmul_rn(x2, cs.ch);
+  const float pe = __fmaf_rn(x2, cs.ch, -p);
+  const float q = __fmul_rn(x1, cs.sh);
+  const float qe = __fmaf_rn(x1, cs.sh, -q);
+  const float lo = __fmaf_rn(x2, cs.cl, __fmaf_rn(x1, cs.sl, __fadd_rn(pe, qe)));
+  return __fadd_rn(__fadd_rn(p, q), lo);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Rotate the 8 pairs (a[i], b[i]) held in two 16-byte chunks.
+__device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const CosSin* cs,
+                                        uint4& ya, uint4& yb) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+  uint32_t oa[4], ob[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float2 x1 = bf16x2_to_f2(aw[w]);
+    const float2 x2 = bf16x2_to_f2(bw[w]);
+    const CosSin c0 = cs[2 * w], c1 = cs[2 * w + 1];
+    oa[w] = pack_bf16x2(rot_first(x1.x, x2.x, c0), rot_first(x1.y, x2.y, c1));
+    ob[w] = pack_bf16x2(rot_second(x1.x, x2.x, c0), rot_second(x1.y, x2.y, c1));
+  }
+  ya = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+  yb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constant__ RopeStoreParams p,
+                                                            int prefill) {
+  constexpr int HALF = D / 2;
+  constexpr int RU = D / 16;  // rotation units per head: 8 pairs each
+  constexpr int VU = D / 8;   // copy units per head: 8 elements (16 bytes) each
+  __shared__ CosSin cs[HALF];
+
+  int pos, ntok;
+  if (prefill) {
+    pos = blockIdx.x;  // position t, shared by all A prompts
+    ntok = p.A;
+  } else {
+    pos = p.positions[blockIdx.x];
+    ntok = 1;
+    const int row = p.cache_rows[blockIdx.x];
+    const bool pos_ok = pos >= 0 && pos < p.max_seq;
+    const bool row_ok = row >= 0 && row < p.S;
+    if (!pos_ok || !row_ok) {
+      if (threadIdx.x == 0)
+        atomicOr(p.status, (pos_ok ? 0 : KVGQA_FLAG_POSITION_RANGE) | (row_ok ? 0 : KVGQA_FLAG_ROW_RANGE));
+      return;
+    }
+  }
+
+  for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
+    double s, c;
+    sincos(static_cast<double>(pos) * p.inv_freq[i], &s, &c);
+    CosSin v;
+    v.ch = static_cast<float>(c);
+    v.cl = static_cast<float>(c - static_cast<double>(v.ch));
+    v.sh = static_cast<float>(s);
+    v.sl = static_cast<float>(s - static_cast<double>(v.sh));
+    cs[i] = v;
+  }
+  __syncthreads();
+
+  const int units = (p.H_q + p.H_kv) * RU + p.H_kv * VU;
+  for (int u = threadIdx.x; u < ntok * units; u += blockDim.x) {
+    const int ti = u / units;
+    const int r = u - ti * units;
+    const int a = prefill ? ti : blockIdx.x;
+    const int row = p.cache_rows[a];
+    if (prefill && (row < 0 || row >= p.S)) {
+      if (r == 0) atomicOr(p.status, KVGQA_FLAG_ROW_RANGE);
+      continue;
+    }
+    const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : static_cast<size_t>(a);
+    const size_t q_base = tok * p.H_q * D;
+    const size_t kv_base = tok * p.H_kv * D;
+    if (r < (p.H_q + p.H_kv) * RU) {
+      const int h = r / RU, c = r - (r / RU) * RU;
+      const uint16_t* src;
+      uint16_t* dst;
+      if (h < p.H_q) {
+        src = p.q + q_base + static_cast<size_t>(h) * D;
+        dst = p.q_out + q_base + static_cast<size_t>(h) * D;
+      } else {
+        const int g = h - p.H_q;
+        src = p.k + kv_base + static_cast<size_t>(g) * D;
+        dst = p.k_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D;
+      }
+      const uint4 a8 = *reinterpret_cast<const uint4*>(src + c * 8);
+      const uint4 b8 = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
+      uint4 ya, yb;
+      rotate8(a8, b8, cs + c * 8, ya, yb);
+      *reinterpret_cast<uint4*>(dst + c * 8) = ya;
+      *reinterpret_cast<uint4*>(dst + HALF + c * 8) = yb;
+    } else {
+      const int rr = r - (p.H_q + p.H_kv) * RU;
+      const int g = rr / VU, c = rr - (rr / VU) * VU;
+      const uint16_t* src = p.v + kv_base + static_cast<size_t>(g) * D + c * 8;
+      uint16_t* dst = p.v_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D + c * 8;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rope_kv_store(const RopeStoreParams& p, bool prefill, cudaStream_t stream) {
+  const unsigned grid = prefill ? static_cast<unsigned>(p.T) : static_cast<unsigned>(p.A);
+  if (grid == 0) return cudaSuccess;
+  if (p.D == 128)
+    rope_kv_store_kernel<128><<<grid, 256, 0, stream>>>(p, prefill ? 1 : 0);
+  else if (p.D == 64)
+    rope_kv_store_kernel<64><<<grid, 256, 0, stream>>>(p, prefill ? 1 : 0);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace kvgqa
