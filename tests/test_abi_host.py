@@ -113,7 +113,9 @@ def test_store_alias_rejected():
     a["k_cache"], a["v_cache"] = both[0], both[0]
     assert code_of(kv.rope_kv_store_out_, **a) == "EALIAS"
     a = decode_args()
-    a["workspace"] = a["v_cache"].view(torch.uint8).view(-1)[:256]
+    vbuf = aligned_bytes(4 * 2 * 32 * 64 * 2)
+    a["v_cache"] = vbuf.view(torch.bfloat16).view(4, 2, 32, 64)
+    a["workspace"] = vbuf[:256]                     # aligned, and inside v_cache
     assert code_of(kv.rope_kv_store_out_, **a) == "EALIAS"
 
 
