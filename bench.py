@@ -194,6 +194,30 @@ def decode_bytes(wl, positions):
     return attn, attn + store
 
 
+def hold_gpu(us: float):
+    """Keep the GPU busy for about `us` microseconds (a spin kernel) so that
+    the host queues every timed step before the first one starts: the CUDA
+    events then see device time only, never a host launch gap."""
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is None:
+        return
+    sleep(int(min(us, 2e6) * 2000))   # cycles at about 2 GHz; the length only needs to be rough
+
+
+def host_call_us(*calls, n=200):
+    """Host time of one prepared C-ABI call (validation + launch), in us."""
+    names = ["store", "attention", "prefill"]
+    out = {}
+    for name, c in zip(names, calls):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            c()
+        out[name] = round((time.perf_counter() - t0) / n * 1e6, 2)
+        torch.cuda.synchronize()
+    return out
+
+
 def prefill_flops(wl):
     return 4.0 * wl.D * wl.H_q * wl.A * wl.T * (wl.T + 1) / 2.0
 
@@ -214,13 +238,14 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        kv.rope_kv_store_out_(q, k, v, pos, rows, wl.theta, q_rot, kc, vc, ws1, stream)
-        kv.cached_gqa_attention_out_(q_rot, kc, vc, pos, rows, wl.scale, out, ws2, stream)
+    store = kv.prepare_rope_kv_store_out_(q, k, v, pos, rows, wl.theta, q_rot, kc, vc, ws1, stream)
+    attend = kv.prepare_cached_gqa_attention_out_(q_rot, kc, vc, pos, rows, wl.scale, out, ws2, stream)
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        store()
+        attend()
     torch.cuda.synchronize()
+    host_us = host_call_us(store, attend)
     if kv.kvgqa_read_status(ws1) or kv.kvgqa_read_status(ws2):
         raise RuntimeError("device status flags set during warm-up")
 
@@ -232,13 +257,14 @@ def run_ours(args, rank, world, local):
         sampler.start()
     barrier(world)
     torch.cuda.synchronize()
+    hold_gpu(K * (host_us["store"] + host_us["attention"] + 40.0))
     for i in range(K):
         flush.zero_()
         e0, e1, e2 = ev[i]
         e0.record(stream)
-        kv.rope_kv_store_out_(q, k, v, pos, rows, wl.theta, q_rot, kc, vc, ws1, stream)
+        store()
         e1.record(stream)
-        kv.cached_gqa_attention_out_(q_rot, kc, vc, pos, rows, wl.scale, out, ws2, stream)
+        attend()
         e2.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -264,11 +290,14 @@ def run_ours(args, rank, world, local):
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_pos, h_rows))
     d2h = h_out.numel() * h_out.element_size()
 
+    e2e_store = kv.prepare_rope_kv_store_out_(d_q, d_k, d_v, d_pos, d_rows, wl.theta, q_rot, kc, vc, ws1, stream)
+    e2e_attend = kv.prepare_cached_gqa_attention_out_(q_rot, kc, vc, d_pos, d_rows, wl.scale, out, ws2, stream)
+
     def e2e_step():
         d_q.copy_(h_q, non_blocking=True); d_k.copy_(h_k, non_blocking=True); d_v.copy_(h_v, non_blocking=True)
         d_pos.copy_(h_pos, non_blocking=True); d_rows.copy_(h_rows, non_blocking=True)
-        kv.rope_kv_store_out_(d_q, d_k, d_v, d_pos, d_rows, wl.theta, q_rot, kc, vc, ws1, stream)
-        kv.cached_gqa_attention_out_(q_rot, kc, vc, d_pos, d_rows, wl.scale, out, ws2, stream)
+        e2e_store()
+        e2e_attend()
         h_out.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -312,6 +341,7 @@ def run_ours(args, rank, world, local):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * K,
+        "host_us_per_call": host_us,
         "clocks": clocks,
     }
     if prefill is not None:
@@ -329,8 +359,7 @@ def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_
     out = torch.empty(pw.A, pw.T, pw.H_q, pw.D, dtype=torch.bfloat16, device=dev)
     ws = kv.new_workspace(kv.prefill_gqa_cached_rows_workspace_size(pw.A, pw.T, pw.H_q, pw.H_kv, pw.D), dev)
 
-    def call():
-        kv.prefill_gqa_cached_rows_out_(q, k, v, rows, pw.theta, pw.scale, kc, vc, out, ws, stream)
+    call = kv.prepare_prefill_gqa_cached_rows_out_(q, k, v, rows, pw.theta, pw.scale, kc, vc, out, ws, stream)
 
     try:
         for _ in range(3):
@@ -341,6 +370,8 @@ def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_
     K = max(10, min(args.steps, 100))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     barrier(world)
+    torch.cuda.synchronize()
+    hold_gpu(K * 100.0)
     for i in range(K):
         flush.zero_()
         ev[i][0].record(stream)

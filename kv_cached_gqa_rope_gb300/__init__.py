@@ -168,6 +168,46 @@ def prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_c
                                              *map(_ref, outs), _stream(stream)))
 
 
+class Prepared:
+    """One C-ABI call with its descriptors built once.
+
+    Calling it crosses ctypes and runs the library's host checks and kernel
+    launches; nothing is re-marshalled.  It keeps the tensors alive, so their
+    addresses stay valid for as long as the object exists (the pattern a
+    serving loop with fixed buffers, or a CUDA graph capture, wants)."""
+
+    def __init__(self, fn, args, keep):
+        self._fn, self._args, self._keep = fn, args, keep
+
+    def __call__(self) -> None:
+        _check(self._fn(*self._args))
+
+
+def prepare_rope_kv_store_out_(q, k, v, positions, cache_rows, theta, q_out, k_cache, v_cache, workspace,
+                               stream=None) -> Prepared:
+    ds = [describe(t) for t in (q, k, v, positions, cache_rows, q_out, k_cache, v_cache, workspace)]
+    args = (*map(_ref, ds[:5]), ctypes.c_double(theta), *map(_ref, ds[5:]), ctypes.c_void_p(_stream(stream)))
+    return Prepared(_lib.rope_kv_store_out_, args,
+                    (ds, q, k, v, positions, cache_rows, q_out, k_cache, v_cache, workspace))
+
+
+def prepare_cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_rows, scale, out, workspace,
+                                      stream=None) -> Prepared:
+    ds = [describe(t) for t in (q_rot, k_cache, v_cache, positions, cache_rows, out, workspace)]
+    args = (*map(_ref, ds[:5]), ctypes.c_float(scale), *map(_ref, ds[5:]), ctypes.c_void_p(_stream(stream)))
+    return Prepared(_lib.cached_gqa_attention_out_, args,
+                    (ds, q_rot, k_cache, v_cache, positions, cache_rows, out, workspace))
+
+
+def prepare_prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_cache, out, workspace,
+                                         stream=None) -> Prepared:
+    ds = [describe(t) for t in (q, k, v, cache_rows, k_cache, v_cache, out, workspace)]
+    args = (*map(_ref, ds[:4]), ctypes.c_double(theta), ctypes.c_float(scale), *map(_ref, ds[4:]),
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared(_lib.prefill_gqa_cached_rows_out_, args,
+                    (ds, q, k, v, cache_rows, k_cache, v_cache, out, workspace))
+
+
 def kvgqa_read_status(workspace, stream=None) -> int:
     """Synchronise the stream, return and clear the workspace status word."""
     w = describe(workspace)

@@ -47,6 +47,12 @@ constexpr int W_MIN = 256;              // fewest keys a CTA is given
 constexpr unsigned FULL = 0xffffffffu;
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// One split-K partial result: o[GP][D], then m[GP], then l[GP] (each of the
+// last two padded to at least 2 floats) so that every slot starts on a
+// 16-byte boundary for the float4 accesses.
+__host__ __device__ constexpr int slot_floats(int GP, int D) { return GP * D + 2 * (GP < 2 ? 2 : GP); }
+__host__ __device__ constexpr int slot_l_offset(int GP, int D) { return GP * D + (GP < 2 ? 2 : GP); }
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int D, int GP>
@@ -386,7 +392,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p) {
       }
       named_bar_sync(1, NCW * 32);
       const bool whole = cur.whole();
-      float* slotp = p.partials + static_cast<size_t>(blockIdx.x * 2 + cur.slot()) * GP * (D + 2);
+      float* slotp = p.partials + static_cast<size_t>(blockIdx.x * 2 + cur.slot()) * slot_floats(GP, D);
       for (int item = threadIdx.x; item < p.G * (D / 8); item += NCW * 32) {
         const int h = item / (D / 8), c8 = item - h * (D / 8);
         float M = -INFINITY;
@@ -422,7 +428,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p) {
           dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
           if (c8 == 0) {
             slotp[GP * D + h] = M;
-            slotp[GP * D + GP + h] = lsum;
+            slotp[slot_l_offset(GP, D) + h] = lsum;
           }
         }
       }
@@ -451,21 +457,21 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   const int b0 = seg_lo / W, b1 = (seg_lo + n - 1) / W;
   if (b0 == b1) return;  // finished by the split-K kernel
   const int slot0 = (b0 * W == seg_lo) ? 0 : 1;
-  const size_t slot_floats = static_cast<size_t>(GP) * (D + 2);
+  constexpr size_t SLOT = slot_floats(GP, D);
   for (int item = threadIdx.x; item < p.G * (D / 8); item += blockDim.x) {
     const int h = item / (D / 8), c8 = item - h * (D / 8);
     float M = -INFINITY;
     for (int b = b0; b <= b1; ++b) {
-      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? slot0 : 0)) * slot_floats;
+      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? slot0 : 0)) * SLOT;
       M = fmaxf(M, sp[GP * D + h]);
     }
     float lsum = 0.f, acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     for (int b = b0; b <= b1; ++b) {
-      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? slot0 : 0)) * slot_floats;
+      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? slot0 : 0)) * SLOT;
       const float sc = exp2f(sp[GP * D + h] - M);
-      lsum += sp[GP * D + GP + h] * sc;
+      lsum += sp[slot_l_offset(GP, D) + h] * sc;
       const float4 u0 = *reinterpret_cast<const float4*>(sp + h * D + c8 * 8);
       const float4 u1 = *reinterpret_cast<const float4*>(sp + h * D + c8 * 8 + 4);
       acc[0] += u0.x * sc; acc[1] += u0.y * sc; acc[2] += u0.z * sc; acc[3] += u0.w * sc;
@@ -548,7 +554,7 @@ cudaError_t decode_launch_shape(int device, int D, int GP, int* num_ctas, size_t
   const cudaError_t e = dispatch(D, GP, [&](auto k) { return decltype(k)::prepare(device, &n); });
   if (e != cudaSuccess) return e;
   *num_ctas = n;
-  *partial_bytes = static_cast<size_t>(n) * 2 * GP * (D + 2) * sizeof(float);
+  *partial_bytes = static_cast<size_t>(n) * 2 * slot_floats(GP, D) * sizeof(float);
   return cudaSuccess;
 }
 
