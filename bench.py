@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+                    help="run just the timed decode steps or just the prefill calls (for profiler captures)")
     return ap.parse_args()
 
 
@@ -245,14 +247,17 @@ def run_ours(args, rank, world, local):
         store()
         attend()
     torch.cuda.synchronize()
-    host_us = host_call_us(store, attend)
+    if args.only == "prefill":
+        res = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
+        return {"impl": "ours", "only": "prefill", "prefill": res} if rank == 0 else None
+    host_us = host_call_us(store, attend, n=min(200, 10 * args.steps))
     if kv.kvgqa_read_status(ws1) or kv.kvgqa_read_status(ws2):
         raise RuntimeError("device status flags set during warm-up")
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    sampler = ClockSampler(dev.index) if rank == 0 else None
+    sampler = ClockSampler(dev.index) if rank == 0 and args.only is None else None
     if sampler:
         sampler.start()
     barrier(world)
@@ -280,6 +285,9 @@ def run_ours(args, rank, world, local):
     tokens_per_s = wl.A * K * world / (total_ms / 1e3)
     attn_avg_s = float(np.mean(attn_ms)) / 1e3
     achieved = attn_bytes / attn_avg_s / 1e9
+    if args.only == "decode":
+        return {"impl": "ours", "only": "decode", "value": round(tokens_per_s, 1), "unit": UNIT,
+                "attention_ms": round(attn_avg_s * 1e3, 5), "kv_gbs": round(achieved, 1)} if rank == 0 else None
 
     # ---- end to end: pinned host inputs -> device -> two calls -> host output
     h_q, h_k, h_v = inp.q.pin_memory(), inp.k.pin_memory(), inp.v.pin_memory()

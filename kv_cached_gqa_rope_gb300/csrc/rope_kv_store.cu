@@ -97,8 +97,15 @@ __global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constan
   }
 
   for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
+    // Cody-Waite reduction of the angle by 2*pi (2*pi split in two doubles,
+    // the products fused), so sincos only ever sees |r| <= pi.
+    constexpr double kTwoPiHi = 6.283185307179586232;    // nearest double to 2*pi
+    constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
+    const double phi = static_cast<double>(pos) * p.inv_freq[i];
+    const double k = rint(phi * 0.15915494309189535);    // 1 / (2*pi)
+    const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, phi));
     double s, c;
-    sincos(static_cast<double>(pos) * p.inv_freq[i], &s, &c);
+    sincos(r, &s, &c);
     CosSin v;
     v.ch = static_cast<float>(c);
     v.cl = static_cast<float>(c - static_cast<double>(v.ch));
