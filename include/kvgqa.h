@@ -176,6 +176,38 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
                                        const kvgqa_tensor* out, const kvgqa_tensor* workspace,
                                        void* stream);
 
+/*
+ * cached_gqa_attention_static_scratch_out_ -- the same attention as
+ * cached_gqa_attention_out_, for callers that cannot allocate device memory.
+ *
+ * The pages describe no such operation; it exists for callers that have no
+ * way to obtain a workspace: code that runs where cudaMalloc is unavailable or
+ * forbidden (inside an allocator hook, under an external memory budget that
+ * owns every byte, or a host runtime that only ever hands out its inputs and
+ * outputs).  Instead of a workspace, the split-K partials go to a scratch array
+ * that the library itself holds in device memory: a file-scope static device
+ * array of 4 MiB (KVGQA_STATIC_SCRATCH_BYTES), present on every GPU that loads
+ * the library until the process exits.  Nothing is allocated by this call: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call on a device looks up the device address of that array (once
+ * per device, with that device current); make that first call before any
+ * stream capture.  Sizes whose partials do not fit the array are rejected
+ * with KVGQA_EUNSUPPORTED.  Every call shares the one array and overwrites the
+ * partials of the previous call before reading them, so nothing needs to start
+ * at zero; calls whose kernels overlap on the GPU (different streams, or
+ * different host threads) race on it.  Device-side range checks still skip
+ * rows with invalid positions or cache rows, but this variant has no status
+ * word for the caller to read.
+ */
+#define KVGQA_STATIC_SCRATCH_BYTES (4u << 20)
+kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
+                                                      const kvgqa_tensor* k_cache,
+                                                      const kvgqa_tensor* v_cache,
+                                                      const kvgqa_tensor* positions,
+                                                      const kvgqa_tensor* cache_rows, float scale,
+                                                      const kvgqa_tensor* out, void* stream);
+
 /* Workspace of prefill_gqa_cached_rows_out_: the status block plus the rotated
  * queries (A*T*H_q*D bf16). */
 kvgqa_status prefill_gqa_cached_rows_workspace_size(int64_t A, int64_t T, int64_t H_q,

@@ -69,6 +69,8 @@ def _load():
     lib.prefill_gqa_cached_rows_workspace_size.restype = st
     lib.prefill_gqa_cached_rows_out_.argtypes = [P, P, P, P, ctypes.c_double, ctypes.c_float, P, P, P, P, ctypes.c_void_p]
     lib.prefill_gqa_cached_rows_out_.restype = st
+    lib.cached_gqa_attention_static_scratch_out_.argtypes = [P, P, P, P, P, ctypes.c_float, P, ctypes.c_void_p]
+    lib.cached_gqa_attention_static_scratch_out_.restype = st
     lib.kvgqa_read_status.argtypes = [P, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.kvgqa_read_status.restype = st
     return lib
@@ -79,7 +81,8 @@ _lib = _load()
 EXPORTED_SYMBOLS = ("kvgqa_abi_version", "kvgqa_last_error", "rope_kv_store_workspace_size",
                     "rope_kv_store_out_", "cached_gqa_attention_workspace_size",
                     "cached_gqa_attention_out_", "prefill_gqa_cached_rows_workspace_size",
-                    "prefill_gqa_cached_rows_out_", "kvgqa_read_status")
+                    "prefill_gqa_cached_rows_out_", "kvgqa_read_status",
+                    "cached_gqa_attention_static_scratch_out_")
 
 
 def library() -> ctypes.CDLL:
@@ -158,6 +161,16 @@ def cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_rows, sc
     ds = [describe(t) for t in (q_rot, k_cache, v_cache, positions, cache_rows)]
     o, w = describe(out), describe(workspace)
     _check(_lib.cached_gqa_attention_out_(*map(_ref, ds), float(scale), _ref(o), _ref(w), _stream(stream)))
+
+
+def cached_gqa_attention_static_scratch_out_(q_rot, k_cache, v_cache, positions, cache_rows, scale, out,
+                                             stream=None) -> None:
+    """Cached GQA attention without a workspace, for callers that cannot
+    allocate device memory: the partials live in the library's own 4 MiB
+    static device array, shared by every call (see include/kvgqa.h)."""
+    ds = [describe(t) for t in (q_rot, k_cache, v_cache, positions, cache_rows)]
+    o = describe(out)
+    _check(_lib.cached_gqa_attention_static_scratch_out_(*map(_ref, ds), float(scale), _ref(o), _stream(stream)))
 
 
 def prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_cache, out, workspace,

@@ -330,6 +330,64 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
   });
 }
 
+kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
+                                                      const kvgqa_tensor* k_cache,
+                                                      const kvgqa_tensor* v_cache,
+                                                      const kvgqa_tensor* positions,
+                                                      const kvgqa_tensor* cache_rows, float scale,
+                                                      const kvgqa_tensor* out, void* stream) {
+  return guarded([&] {
+    if (!q_rot || !k_cache) fail(KVGQA_EINVAL, "null descriptor");
+    if (q_rot->ndim != 3 || k_cache->ndim != 4) fail(KVGQA_EINVAL, "q_rot must be [A,H_q,D], caches [S,H_kv,max_seq,D]");
+    const int64_t A = q_rot->shape[0], H_q = q_rot->shape[1], D = q_rot->shape[2];
+    const int64_t S = k_cache->shape[0], H_kv = k_cache->shape[1], max_seq = k_cache->shape[2];
+    check_head_dim(D);
+    check_heads(H_q, H_kv);
+    if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
+    const int G = (int)(H_q / H_kv);
+    if (G > 8) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 8", G);
+    if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
+    if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
+    View vq = check_tensor("q_rot", q_rot, 3, KVGQA_BF16, 16);
+    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+    View vp = check_tensor("positions", positions, 1, KVGQA_I32, 4);
+    View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
+    View vo = check_tensor("out", out, 3, KVGQA_BF16, 16);
+    require_shape(vvc, {S, H_kv, max_seq, D});
+    require_shape(vp, {A});
+    require_shape(vr, {A});
+    require_shape(vo, {A, H_q, D});
+    check_no_alias({&vo}, {&vq, &vkc, &vvc, &vp, &vr, &vo});
+    const int dev = current_device();
+    check_device({&vq, &vkc, &vvc, &vp, &vr, &vo}, dev);
+    int ctas = 0;
+    size_t part = 0;
+    check_cuda(kvgqa::decode_launch_shape(dev, (int)D, kvgqa::decode_group_pad(G), &ctas, &part),
+               "decode kernel set-up");
+    if (KVGQA_STATUS_BYTES + part > kvgqa::kStaticScratchBytes)
+      fail(KVGQA_EUNSUPPORTED, "needs %zu bytes of scratch; the library's static scratch holds %zu",
+           KVGQA_STATUS_BYTES + part, kvgqa::kStaticScratchBytes);
+    void* scratch = nullptr;
+    check_cuda(kvgqa::static_scratch_address(dev, &scratch), "static scratch address");
+    if (A == 0) return;
+    kvgqa::DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q_rot->data);
+    p.k_cache = static_cast<const uint16_t*>(k_cache->data);
+    p.v_cache = static_cast<const uint16_t*>(v_cache->data);
+    p.positions = static_cast<const int32_t*>(positions->data);
+    p.cache_rows = static_cast<const int32_t*>(cache_rows->data);
+    p.out = static_cast<uint16_t*>(out->data);
+    p.status = static_cast<int32_t*>(scratch);
+    p.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + KVGQA_STATUS_BYTES);
+    p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
+    p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = ctas;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    check_cuda(kvgqa::launch_cached_gqa_attention(p, static_cast<cudaStream_t>(stream)),
+               "cached_gqa_attention launch");
+  });
+}
+
 kvgqa_status prefill_gqa_cached_rows_workspace_size(int64_t A, int64_t T, int64_t H_q, int64_t H_kv,
                                                     int64_t D, size_t* bytes) {
   return guarded([&] {

@@ -558,6 +558,23 @@ cudaError_t decode_launch_shape(int device, int D, int GP, int* num_ctas, size_t
   return cudaSuccess;
 }
 
+// Scratch for callers that cannot allocate device memory themselves: the
+// split-K partials (and the status word in front of them) live in this
+// file-scope device array instead of a caller workspace.  Every GPU that
+// loads the library holds it until the process exits; all calls share it.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+cudaError_t static_scratch_address(int device, void** ptr) {
+  static std::once_flag flags[64];
+  static void* addr[64];
+  static cudaError_t errs[64];
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  // Runs once per device, with that device current (the caller's current device).
+  std::call_once(flags[device], [&] { errs[device] = cudaGetSymbolAddress(&addr[device], g_static_scratch); });
+  *ptr = addr[device];
+  return errs[device];
+}
+
 cudaError_t launch_cached_gqa_attention(const DecodeParams& p, cudaStream_t stream) {
   if (p.A == 0) return cudaSuccess;
   const int GP = decode_group_pad(p.G);

@@ -48,6 +48,12 @@ int decode_group_pad(int G);
 cudaError_t decode_launch_shape(int device, int D, int GP, int* num_ctas, size_t* partial_bytes);
 cudaError_t launch_cached_gqa_attention(const DecodeParams& p, cudaStream_t stream);
 
+// Size of the library's own device scratch array (status block + partials)
+// used by the entry point for callers that cannot allocate, and its device
+// address on `device` (looked up once per device; `device` must be current).
+constexpr size_t kStaticScratchBytes = 4u << 20;
+cudaError_t static_scratch_address(int device, void** ptr);
+
 // ------------------------------------------------------------------ prefill attention
 struct PrefillParams {
   const uint16_t* q_rot;      // [A,T,H_q,D] rotated queries (workspace)
