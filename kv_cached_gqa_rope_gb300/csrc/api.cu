@@ -267,7 +267,7 @@ kvgqa_status cached_gqa_attention_workspace_size(int64_t A, int64_t H_q, int64_t
     check_head_dim(D);
     check_heads(H_q, H_kv);
     const int G = (int)(H_q / H_kv);
-    if (G > 8) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 8", G);
+    if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     int ctas = 0;
     size_t part = 0;
     check_cuda(kvgqa::decode_launch_shape(device, (int)D, kvgqa::decode_group_pad(G), &ctas, &part),
@@ -290,7 +290,7 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
     check_heads(H_q, H_kv);
     if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
     const int G = (int)(H_q / H_kv);
-    if (G > 8) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 8", G);
+    if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
     if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
     View vq = check_tensor("q_rot", q_rot, 3, KVGQA_BF16, 16);
@@ -345,7 +345,7 @@ kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
     check_heads(H_q, H_kv);
     if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
     const int G = (int)(H_q / H_kv);
-    if (G > 8) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 8", G);
+    if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
     if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
     View vq = check_tensor("q_rot", q_rot, 3, KVGQA_BF16, 16);

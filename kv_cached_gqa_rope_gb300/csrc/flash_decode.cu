@@ -1,52 +1,62 @@
-// K2: split-K flash-decode over the shared slot KV cache, and K3: the combine.
+// K2: split-K flash-decode over the shared slot KV cache on tcgen05 tensor
+// cores, and K3: the combine.
 //
 // microLLM-rocm ARCHITECTURE.md, section "Tensor ownership boundary": each
 // survivor token attends to its own row's cached prefix, with device
 // positions[A] and cache_rows[A].  Section "Attention layout boundary": with
-// GQA, one K/V head serves a group of query heads (the zero-stride idea: K/V
+// GQA one K/V head serves a group of query heads (the zero-stride idea: K/V
 // are never expanded).  operator-development.md, "Public interfaces": low
 // precision softmax keeps FP32 reductions and rounds only the caller output.
 //
 // Work split.  Segment (a, g) is the prefix of KV head g in row cache_rows[a]:
-// n_a = positions[a] + 1 keys, contiguous in memory ((n_a * D * 2) bytes).  All
-// segments, laid end to end, form one key range of K_tot keys; CTA b of the
-// persistent grid takes keys [b*W, (b+1)*W) with W = ceil(K_tot / grid), so
-// every SM streams the same number of bytes whatever the length mix.  A
-// segment that lies inside one CTA is finished there (BF16 out written); a
-// segment cut by a CTA boundary leaves FP32 partials (m, l, o) that K3 merges.
-// Each CTA writes at most two partials (its first and its last segment).
+// n_a = positions[a] + 1 keys, contiguous in memory.  All segments, laid end to
+// end, form one key range of K_tot keys; CTA b of the persistent grid (one CTA
+// per SM) takes keys [b*W, (b+1)*W) with W = ceil(K_tot / grid), so every SM
+// streams the same number of bytes whatever the length mix.  A segment that
+// lies inside one CTA is finished there (BF16 out written); a segment cut by a
+// CTA boundary leaves FP32 partials (m, l, o) that K3 merges.  Each CTA writes
+// at most two partials (its first and its last segment).
 //
-// Inside a CTA: one producer warp streams 64-key K and V tiles (and, at a
-// segment start, the G query rows) into a 4-stage shared-memory ring with
-// bulk TMA copies completed on mbarriers; eight consumer warps take 8 keys of
-// each tile.  In a consumer warp, D/8 lanes share one key: each lane owns a
-// 16-byte chunk of D and holds that chunk of all G (padded to GP) query heads in
-// registers.  Partial dot products are reduced with a transposing butterfly
-// (shuffles) that leaves each lane with the full score of one head, so the
-// FP32 online softmax needs no further exchange; probabilities go through a
-// small per-warp shared buffer to the P.V accumulation, which uses packed
-// FP32x2 FMAs.
+// Inside a CTA, per tile of up to 128 keys of one segment:
+//   warp 4     TMA producer: K and V tiles (128B swizzle, 32-row boxes, so a
+//              short tail reads at most 31 rows past the prefix) and the
+//              group's query rows (16 rows: the G heads, the rest padding) into
+//              a 3-stage ring;
+//   warp 5     one thread issues tcgen05.mma: S^T = K Q_g^T (M = 128 keys,
+//              N = 16 heads) into one of two TMEM buffers, then
+//              O^T += V^T P^T (M = D, N = 16; V is an MN-major operand) into a
+//              TMEM accumulator;
+//   warps 0-3  one thread per key: S^T row from TMEM, FP32 online softmax per
+//              head (warp shuffles + a 4-warp exchange for the tile maximum
+//              and sum), P^T as BF16 into 128B-swizzled shared memory; the O^T
+//              rescale (TMEM load/scale/store, one lane per d) happens only when
+//              a head's maximum grew by more than 2^8; at a segment end each
+//              lane d writes O^T[d][h] / l[h] (or the partial).
+// The tensor cores do the two contractions, so the CUDA cores only run the
+// softmax: the kernel is bound by the HBM stream of K and V.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cmath>
 #include <mutex>
 
 #include "kvgqa_internal.h"
-#include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace kvgqa {
 namespace {
 
-constexpr int NCW = 8;                  // consumer warps
-constexpr int NT = 64;                  // keys per tile
-constexpr int KPW = NT / NCW;           // keys of a tile per consumer warp
-constexpr int NS = 4;                   // pipeline stages
-constexpr int THREADS = (NCW + 1) * 32; // + one producer warp
+constexpr int BN = 128;                 // keys per tile (= TMEM lanes = softmax threads)
+constexpr int NQ = 16;                  // MMA N: query heads of a group, padded
+constexpr int BOX_ROWS = 32;            // rows per TMA box of a K or V tile
+constexpr int SUB = BN * 128;           // one [128 rows x 64 bf16] swizzled sub-tile
+constexpr int QSUB = NQ * 128;          // one [16 rows x 64 bf16] swizzled sub-tile
+constexpr int THREADS = 192;            // 4 softmax warps + producer + MMA
+constexpr int TMEM_COLS = 64;           // S^T x2 (16 cols each) + O^T (16 cols)
 constexpr int W_MIN = 256;              // fewest keys a CTA is given
 constexpr unsigned FULL = 0xffffffffu;
-
-constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
 // One split-K partial result: o[GP][D], then m[GP], then l[GP] (each of the
 // last two padded to at least 2 floats) so that every slot starts on a
@@ -55,27 +65,31 @@ __host__ __device__ constexpr int slot_floats(int GP, int D) { return GP * D + 2
 __host__ __device__ constexpr int slot_l_offset(int GP, int D) { return GP * D + (GP < 2 ? 2 : GP); }
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-template <int D, int GP>
+template <int D>
 struct Cfg {
-  static constexpr int L = D / 8;           // lanes sharing one key
-  static constexpr int KPS = 32 / L;        // keys per warp step
-  static constexpr int STEPS = KPW / KPS;   // warp steps per tile
-  static constexpr int LOGL = ilog2(L);
-  static constexpr int LOGG = ilog2(GP);
-  static constexpr int KV_BYTES = NT * D * 2;
-  static constexpr int Q_BYTES = GP * D * 2;
-  static constexpr int STAGE = 2 * KV_BYTES + Q_BYTES;
-  static constexpr int OFF_P = NS * STAGE;                     // [NCW][KPW][GP] f32
-  static constexpr int OFF_ALPHA = OFF_P + NCW * KPW * GP * 4;  // [NCW][GP]
-  static constexpr int OFF_CM = OFF_ALPHA + NCW * GP * 4;       // [NCW][GP]
-  static constexpr int OFF_CL = OFF_CM + NCW * GP * 4;          // [NCW][GP]
-  static constexpr int OFF_CO = OFF_CL + NCW * GP * 4;          // [NCW][GP][D]
-  static constexpr int OFF_PREFIX = OFF_CO + NCW * GP * D * 4;  // [kMaxActiveRows + 1] int
-  static constexpr int OFF_BAR = align_up(OFF_PREFIX + (kMaxActiveRows + 1) * 4, 16);
-  static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
-  static constexpr int SMEM = OFF_FLAG + 16;
-  static_assert(GP <= L, "group larger than the lanes of one key");
+  static constexpr int NSUB = D / 64;
+  static constexpr int NS = D == 128 ? 3 : 4;          // stages
+  static constexpr int K_OFF = 0;                      // inside a stage
+  static constexpr int V_OFF = NSUB * SUB;
+  static constexpr int Q_OFF = 2 * NSUB * SUB;
+  static constexpr int STAGE = 2 * NSUB * SUB + NSUB * QSUB;   // multiple of 1024
+  static constexpr int P_OFF = NS * STAGE;                     // P^T [16 x 128 keys], 2 sub-tiles
+  static constexpr int RED_OFF = P_OFF + 2 * QSUB;             // [2][4 warps][16] floats
+  static constexpr int PREFIX_OFF = RED_OFF + 2 * 4 * NQ * 4;  // [kMaxActiveRows + 1] ints
+  static constexpr int BAR_OFF = align_up(PREFIX_OFF + (kMaxActiveRows + 1) * 4, 16);
+  // kv_full[NS], kv_empty[NS], s_full[2], p_full, o_done, drain
+  static constexpr int NBAR = 2 * NS + 5;
+  static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int FLAG_OFF = SLOT_OFF + 8;
+  static constexpr int SMEM = FLAG_OFF + 16 + 1024;            // + alignment slack
+  static_assert(STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct DecodeMaps {
+  CUtensorMap kc;  // cache [S*H_kv][max_seq][D], box {64, 32, 1}
+  CUtensorMap vc;
+  CUtensorMap q;   // q_rot [A*H_q][D], box {64, 16}
 };
 
 // Per-row key counts and their running sum (times H_kv): prefix[a] is the
@@ -116,8 +130,8 @@ __device__ __forceinline__ int keys_per_cta(int k_tot, int num_ctas) {
   return w < W_MIN ? W_MIN : w;
 }
 
-// Walks the tiles of one CTA's key range [x0, x1): segment by segment, NT keys
-// at a time.  Producer and consumers run identical copies.
+// Walks the tiles of one CTA's key range [x0, x1): segment by segment, BN keys
+// at a time.  Every role runs its own identical copy.
 struct Cursor {
   const int* prefix;
   int H_kv, x0, x1;
@@ -127,7 +141,7 @@ struct Cursor {
 
   __device__ void init(const int* pf, int h_kv, int A, int lo, int hi) {
     prefix = pf; H_kv = h_kv; x0 = lo; x1 = hi; x = lo;
-    int l = 0, r = A - 1;  // last row with prefix[row] <= x0 and a nonempty range
+    int l = 0, r = A - 1;  // last row with prefix[row] <= x0
     while (l < r) {
       const int mid = (l + r + 1) >> 1;
       if (prefix[mid] <= lo) l = mid; else r = mid - 1;
@@ -142,7 +156,7 @@ struct Cursor {
   __device__ __forceinline__ bool more() const { return x < x1; }
   __device__ __forceinline__ int seg_end() const { return min(seg_lo + n, x1); }
   __device__ __forceinline__ int k0() const { return x - seg_lo; }
-  __device__ __forceinline__ int nt() const { return min(NT, seg_end() - x); }
+  __device__ __forceinline__ int nt() const { return min(BN, seg_end() - x); }
   __device__ __forceinline__ bool first() const { return x == seg_in; }
   __device__ __forceinline__ bool last() const { return x + nt() == seg_end(); }
   __device__ __forceinline__ bool whole() const { return seg_lo >= x0 && seg_lo + n <= x1; }
@@ -162,22 +176,41 @@ struct Cursor {
   }
 };
 
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&b);
+}
+
 template <int D, int GP>
 __global__ void __launch_bounds__(THREADS, 1)
-flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p) {
-  using C = Cfg<D, GP>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  int* prefix = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + NS;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
-
+flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap map_k,
+                           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_q) {
+  using C = Cfg<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  int* prefix = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = bars + C::NS;
+  uint64_t* s_full = bars + 2 * C::NS;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* drain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NCW);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_full, BN);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -186,261 +219,230 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p) {
   const int k_tot = prefix[p.A];
   const int W = keys_per_cta(k_tot, p.num_ctas);
   const int x0 = blockIdx.x * W;
-  if (x0 >= k_tot) return;
+  if (x0 >= k_tot) return;  // uniform: nothing allocated yet
   const int x1 = min(x0 + W, k_tot);
+
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = smem_u32(smem);
 
   Cursor cur;
   cur.init(prefix, p.H_kv, p.A, x0, x1);
 
-  if (warp == NCW) {
-    // ---------------------------------------------------------- producer
-    if (lane != 0) return;
-    const uint64_t pol_kv = l2_evict_first_policy();
-    const uint64_t pol_q = l2_evict_last_policy();
-    int it = 0;
-    bool ok = true;
-    for (; cur.more(); cur.advance(), ++it) {
-      const int s = it % NS;
-      if (it >= NS && !mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
+  if (warp == 4) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_evict_first_policy();
+      const uint64_t pol_q = l2_evict_last_policy();
+      int it = 0;
+      for (; cur.more(); cur.advance(), ++it) {
+        const int s = it % C::NS;
+        if (it >= C::NS && !mbar_wait_bounded(&kv_empty[s], ((it / C::NS) - 1) & 1, abort_flag, p.status)) break;
+        const int nb = (cur.nt() + BOX_ROWS - 1) / BOX_ROWS;
+        const uint32_t bytes = static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + QSUB);
+        unsigned char* st = smem + s * C::STAGE;
+        const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
+        mbar_arrive_expect_tx(&kv_full[s], bytes);
+        for (int sub = 0; sub < C::NSUB; ++sub) {
+          for (int b = 0; b < nb; ++b) {
+            tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
+                        kv_row, &kv_full[s], pol_kv);
+            tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
+                        kv_row, &kv_full[s], pol_kv);
+          }
+          tma_load_3d(st + C::Q_OFF + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, &kv_full[s],
+                      pol_q);
+        }
       }
+      if (*abort_flag) {
+        volatile int none = 0;
+        for (int t = it - C::NS < 0 ? 0 : it - C::NS; t < it; ++t)
+          mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, &none, nullptr);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(BN, NQ, 0, 0);
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(BN, NQ, 0, 1);
+      constexpr uint32_t V_LBO = D == 128 ? SUB : 0;  // D = 64: the second M half repeats the first
+      const uint32_t p_addr = sbase + C::P_OFF;
+      bool issued = false;
+      auto issue_s = [&](int t) {
+        const uint32_t st = sbase + (t % C::NS) * C::STAGE;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (ks / 4) * SUB + (ks % 4) * 32;
+          const uint32_t qoff = (ks / 4) * QSUB + (ks % 4) * 32;
+          umma_f16_ss(tmem + (t & 1) * NQ, smem_desc_sw128(st + C::K_OFF + koff, 16, 1024),
+                      smem_desc_sw128(st + C::Q_OFF + qoff, 16, 1024), IDESC_S, ks > 0);
+        }
+        umma_commit(&s_full[t & 1]);
+        issued = true;
+      };
+      int it = 0;
+      for (; cur.more(); cur.advance(), ++it) {
+        if (it == 0) {
+          if (!mbar_wait_bounded(&kv_full[0], 0, abort_flag, p.status)) break;
+          tc_fence_after();
+          issue_s(0);
+        }
+        if (cur.x + cur.nt() < cur.x1) {  // another tile follows: overlap its S with this softmax
+          const int t = it + 1;
+          if (!mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, abort_flag, p.status)) break;
+          tc_fence_after();
+          issue_s(t);
+        }
+        if (!mbar_wait_bounded(p_full, it & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t v_addr = sbase + (it % C::NS) * C::STAGE + C::V_OFF;
+        const uint32_t acc0 = cur.first() ? 0u : 1u;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          umma_f16_ss(tmem + 2 * NQ, smem_desc_sw128(v_addr + ks * 2048, V_LBO, 1024),
+                      smem_desc_sw128(p_addr + (ks / 4) * QSUB + (ks % 4) * 32, 16, 1024), IDESC_O,
+                      ks > 0 ? 1u : acc0);
+        }
+        umma_commit(o_done);
+        umma_commit(&kv_empty[it % C::NS]);
+      }
+      if (*abort_flag && issued) {
+        umma_commit(drain);
+        volatile int none = 0;
+        mbar_wait_bounded(drain, 0, &none, nullptr);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax (warps 0-3)
+    const int r = threadIdx.x;  // key row of the tile == TMEM lane == d of O^T
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float* red_max = reinterpret_cast<float*>(smem + C::RED_OFF);
+    float* red_sum = red_max + 4 * NQ;
+    unsigned char* pt = smem + C::P_OFF;
+    float m_ref[GP], l[GP];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) { m_ref[h] = -INFINITY; l[h] = 0.f; }
+    int it = 0;
+    for (; cur.more(); cur.advance(), ++it) {
       const int nt = cur.nt();
       const bool first = cur.first();
-      const uint32_t kv_bytes = static_cast<uint32_t>(nt) * D * 2;
-      const uint32_t q_bytes = first ? static_cast<uint32_t>(p.G) * D * 2 : 0u;
-      unsigned char* st = smem + s * C::STAGE;
-      const int row = p.cache_rows[cur.a];
-      const size_t cell = (static_cast<size_t>(row) * p.H_kv + cur.g) * p.max_seq + cur.k0();
-      mbar_arrive_expect_tx(&full[s], 2 * kv_bytes + q_bytes);
-      bulk_g2s(st, p.k_cache + cell * D, kv_bytes, &full[s], pol_kv);
-      bulk_g2s(st + C::KV_BYTES, p.v_cache + cell * D, kv_bytes, &full[s], pol_kv);
-      if (first)
-        bulk_g2s(st + 2 * C::KV_BYTES,
-                 p.q + (static_cast<size_t>(cur.a) * p.H_q + static_cast<size_t>(cur.g) * p.G) * D,
-                 q_bytes, &full[s], pol_q);
-    }
-    if (!ok) {
-      // Drain: wait (bounded) for copies this warp may still have in flight.
-      for (int t = it - NS < 0 ? 0 : it - NS; t < it; ++t) {
-        volatile int no_abort = 0;
-        mbar_wait_bounded(&full[t % NS], (t / NS) & 1, &no_abort, nullptr);
+      if (!__all_sync(FULL, mbar_wait_bounded(&s_full[it & 1], (it >> 1) & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+      uint32_t u[16];
+      tmem_ld16(tmem + lane_base + (it & 1) * NQ, u);
+      tmem_wait_ld();
+      const bool valid = r < nt;
+      float x[GP], mt[GP];
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        x[h] = (valid && h < p.G) ? __uint_as_float(u[h]) * p.scale_log2 : -INFINITY;
+        float m = x[h];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+        if (lane == 0) red_max[warp * NQ + h] = m;
       }
-    }
-    return;
-  }
+      named_bar_sync(1, BN);
+      bool grow_any = false;
+      float alpha[GP];
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        mt[h] = fmaxf(fmaxf(red_max[h], red_max[NQ + h]), fmaxf(red_max[2 * NQ + h], red_max[3 * NQ + h]));
+        const bool grow = mt[h] > m_ref[h] + 8.f || first;
+        alpha[h] = 1.f;
+        if (grow) {
+          const float mn = first ? mt[h] : fmaxf(m_ref[h], mt[h]);
+          alpha[h] = first ? 0.f : exp2f(m_ref[h] - mn);
+          m_ref[h] = mn;
+          grow_any |= !first;
+        }
+        l[h] = first ? 0.f : l[h] * alpha[h];
+      }
+      // The previous tile's P.V must be complete before P^T is rewritten or O^T rescaled.
+      if (it > 0 && !__all_sync(FULL, mbar_wait_bounded(o_done, (it - 1) & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+      if (grow_any) {  // uniform across the CTA: every thread saw the same maxima
+        uint32_t o[16];
+        tmem_ld16(tmem + lane_base + 2 * NQ, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < GP; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+        tmem_st16(tmem + lane_base + 2 * NQ, o);
+        tmem_wait_st();
+      }
+      // P^T[h][r] as BF16 (K-major B operand: 16 rows of 128 keys, two 64-key
+      // swizzled sub-tiles); padded heads and invalid keys are zero.
+      const int sub = r >> 6, chunk = (r & 63) >> 3, e = r & 7;
+#pragma unroll
+      for (int h = 0; h < NQ; ++h) {
+        uint16_t b = 0;
+        if (h < GP) {
+          const float pv = x[h] == -INFINITY ? 0.f : exp2f(x[h] - m_ref[h]);
+          b = bf16_bits(pv);
+          float ps = __uint_as_float(static_cast<uint32_t>(b) << 16);
+#pragma unroll
+          for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(FULL, ps, off);
+          if (lane == 0) red_sum[warp * NQ + h] = ps;
+        }
+        *reinterpret_cast<uint16_t*>(pt + sub * QSUB + h * 128 + ((chunk ^ (h & 7)) << 4) + e * 2) = b;
+      }
+      if (!valid) {  // rows past the tile's keys: zero V so P = 0 meets no stale NaN
+        unsigned char* vrow = smem + (it % C::NS) * C::STAGE + C::V_OFF + r * 128;
+#pragma unroll
+        for (int sb = 0; sb < C::NSUB; ++sb)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + sb * SUB + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, BN);
+#pragma unroll
+      for (int h = 0; h < GP; ++h)
+        l[h] += (red_sum[h] + red_sum[NQ + h]) + (red_sum[2 * NQ + h] + red_sum[3 * NQ + h]);
+      tc_fence_before();
+      mbar_arrive(p_full);
 
-  // ------------------------------------------------------------ consumers
-  constexpr int L = C::L, KPS = C::KPS, STEPS = C::STEPS, LOGL = C::LOGL, LOGG = C::LOGG;
-  const int j = lane & (L - 1);                 // 16-byte chunk of D owned by this lane
-  const int ks = lane >> LOGL;                  // key slot inside a warp step
-  const int hsel = j >> (LOGL - LOGG);          // head whose score this lane ends with
-  const bool head_rep = (j & ((L / GP) - 1)) == 0;  // one lane per (key slot, head)
-  float* Pw = reinterpret_cast<float*>(smem + C::OFF_P) + warp * KPW * GP;
-  float* alpha_w = reinterpret_cast<float*>(smem + C::OFF_ALPHA) + warp * GP;
-  float* CM = reinterpret_cast<float*>(smem + C::OFF_CM);
-  float* CL = reinterpret_cast<float*>(smem + C::OFF_CL);
-  float* CO = reinterpret_cast<float*>(smem + C::OFF_CO);
-  const uint32_t smem_base = smem_u32(smem);
-
-  float2 qf[GP][4];
-  float2 o[GP][4];
-  float m_run = -INFINITY, l_run = 0.f;
+      if (cur.last()) {
+        // ---------------------------------------------------- segment end
+        if (!__all_sync(FULL, mbar_wait_bounded(o_done, it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        uint32_t o[16];
+        tmem_ld16(tmem + lane_base + 2 * NQ, o);
+        tmem_wait_ld();
+        const int d = r;
+        if (d < D) {
+          if (cur.whole()) {
+            uint16_t* dst = p.out + (static_cast<size_t>(cur.a) * p.H_q + cur.g * p.G) * D + d;
 #pragma unroll
-  for (int i = 0; i < GP; ++i)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) o[i][c] = make_float2(0.f, 0.f);
-
-  int it = 0;
-  for (; cur.more(); cur.advance(), ++it) {
-    const int s = it % NS;
-    if (!mbar_wait_bounded(&full[s], (it / NS) & 1, abort_flag, p.status)) break;
-    const uint32_t st = smem_base + s * C::STAGE;
-    if (cur.first()) {
-#pragma unroll
-      for (int i = 0; i < GP; ++i) {
-        const int h = i ^ hsel;  // heads permuted so the butterfly needs no selects
-        if (h < p.G) {
-          const uint4 w = lds128(st + 2 * C::KV_BYTES + h * D * 2 + j * 16);
-          qf[i][0] = bf16x2_to_f2(w.x); qf[i][1] = bf16x2_to_f2(w.y);
-          qf[i][2] = bf16x2_to_f2(w.z); qf[i][3] = bf16x2_to_f2(w.w);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) qf[i][c] = make_float2(0.f, 0.f);
-        }
-      }
-    }
-    const int nv = min(max(cur.nt() - warp * KPW, 0), KPW);  // valid keys of this warp
-    if (nv > 0) {
-      const uint32_t kbase = st + (warp * KPW) * D * 2 + j * 16;
-      const uint32_t vbase = kbase + C::KV_BYTES;
-      float sc[STEPS];
-#pragma unroll
-      for (int t = 0; t < STEPS; ++t) {
-        const int key = t * KPS + ks;
-        const uint4 w = lds128(kbase + key * D * 2);
-        const float2 k0 = bf16x2_to_f2(w.x), k1 = bf16x2_to_f2(w.y);
-        const float2 k2 = bf16x2_to_f2(w.z), k3 = bf16x2_to_f2(w.w);
-        float part[GP];
-#pragma unroll
-        for (int i = 0; i < GP; ++i) {
-          float2 acc = fmul2(qf[i][0], k0);
-          acc = ffma2(qf[i][1], k1, acc);
-          acc = ffma2(qf[i][2], k2, acc);
-          acc = ffma2(qf[i][3], k3, acc);
-          part[i] = acc.x + acc.y;
-        }
-        // Transposing butterfly: at level lv, exchange the upper half of the
-        // live heads with the partner lane lane ^ 2^(LOGL-1-lv).
-#pragma unroll
-        for (int lv = 0; lv < LOGG; ++lv) {
-          const int half = GP >> (lv + 1);
-#pragma unroll
-          for (int i = 0; i < half; ++i)
-            part[i] += __shfl_xor_sync(FULL, part[i + half], 1 << (LOGL - 1 - lv));
-        }
-#pragma unroll
-        for (int lv = LOGG; lv < LOGL; ++lv)
-          part[0] += __shfl_xor_sync(FULL, part[0], 1 << (LOGL - 1 - lv));
-        sc[t] = key < nv ? part[0] * p.scale_log2 : -INFINITY;
-      }
-      // Online softmax (base 2; scores already carry the log2(e) factor).
-      float mb = sc[0];
-#pragma unroll
-      for (int t = 1; t < STEPS; ++t) mb = fmaxf(mb, sc[t]);
-#pragma unroll
-      for (int off = L; off < 32; off <<= 1) mb = fmaxf(mb, __shfl_xor_sync(FULL, mb, off));
-      const float m_new = fmaxf(m_run, mb);
-      const float alpha = exp2f(m_run - m_new);
-      float psum = 0.f;
-#pragma unroll
-      for (int t = 0; t < STEPS; ++t) {
-        const float pt = exp2f(sc[t] - m_new);
-        psum += pt;
-        if (head_rep) Pw[(t * KPS + ks) * GP + hsel] = pt;
-      }
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      if (head_rep && ks == 0) alpha_w[hsel] = alpha;
-      __syncwarp();
-      if (__any_sync(FULL, alpha != 1.f)) {
-#pragma unroll
-        for (int i = 0; i < GP; ++i) {
-          const float al = alpha_w[i];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) o[i][c] = fmul2(o[i][c], make_float2(al, al));
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < STEPS; ++t) {
-        const int key = t * KPS + ks;
-        if (key < nv) {
-          const uint4 w = lds128(vbase + key * D * 2);
-          const float2 v0 = bf16x2_to_f2(w.x), v1 = bf16x2_to_f2(w.y);
-          const float2 v2 = bf16x2_to_f2(w.z), v3 = bf16x2_to_f2(w.w);
-          float pv[GP];
-          const uint32_t pa = smem_u32(Pw + key * GP);
-          if constexpr (GP >= 4) {
-#pragma unroll
-            for (int i = 0; i < GP; i += 4) {
-              const float4 q4 = lds128f(pa + i * 4);
-              pv[i] = q4.x; pv[i + 1] = q4.y; pv[i + 2] = q4.z; pv[i + 3] = q4.w;
-            }
+            for (int h = 0; h < GP; ++h)
+              if (h < p.G) dst[h * D] = bf16_bits(__uint_as_float(o[h]) / l[h]);
           } else {
+            float* slotp = p.partials + static_cast<size_t>(blockIdx.x * 2 + cur.slot()) * slot_floats(GP, D);
 #pragma unroll
-            for (int i = 0; i < GP; ++i) pv[i] = Pw[key * GP + i];
-          }
+            for (int h = 0; h < GP; ++h) slotp[h * D + d] = __uint_as_float(o[h]);
+            if (d < GP) {
 #pragma unroll
-          for (int i = 0; i < GP; ++i) {
-            const float2 pp = make_float2(pv[i], pv[i]);
-            o[i][0] = ffma2(pp, v0, o[i][0]);
-            o[i][1] = ffma2(pp, v1, o[i][1]);
-            o[i][2] = ffma2(pp, v2, o[i][2]);
-            o[i][3] = ffma2(pp, v3, o[i][3]);
-          }
-        }
-      }
-      __syncwarp();
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-
-    if (cur.last()) {
-      // ---------------------------------------------------- segment end
-#pragma unroll
-      for (int off = L; off < 32; off <<= 1) {
-        l_run += __shfl_xor_sync(FULL, l_run, off);
-#pragma unroll
-        for (int i = 0; i < GP; ++i)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            o[i][c].x += __shfl_xor_sync(FULL, o[i][c].x, off);
-            o[i][c].y += __shfl_xor_sync(FULL, o[i][c].y, off);
-          }
-      }
-      if (ks == 0) {
-#pragma unroll
-        for (int i = 0; i < GP; ++i) {
-          float4* dst = reinterpret_cast<float4*>(CO + (warp * GP + i) * D + j * 8);
-          dst[0] = make_float4(o[i][0].x, o[i][0].y, o[i][1].x, o[i][1].y);
-          dst[1] = make_float4(o[i][2].x, o[i][2].y, o[i][3].x, o[i][3].y);
-        }
-        if (head_rep) {
-          CM[warp * GP + hsel] = m_run;
-          CL[warp * GP + hsel] = l_run;
-        }
-      }
-      named_bar_sync(1, NCW * 32);
-      const bool whole = cur.whole();
-      float* slotp = p.partials + static_cast<size_t>(blockIdx.x * 2 + cur.slot()) * slot_floats(GP, D);
-      for (int item = threadIdx.x; item < p.G * (D / 8); item += NCW * 32) {
-        const int h = item / (D / 8), c8 = item - h * (D / 8);
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, CM[w * GP + h]);
-        float lsum = 0.f, acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-          const float mw = CM[w * GP + h];
-          const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
-          lsum += CL[w * GP + h] * sc;
-          const float4* src = reinterpret_cast<const float4*>(CO + (w * GP + h) * D + c8 * 8);
-          const float4 u0 = src[0], u1 = src[1];
-          acc[0] += u0.x * sc; acc[1] += u0.y * sc; acc[2] += u0.z * sc; acc[3] += u0.w * sc;
-          acc[4] += u1.x * sc; acc[5] += u1.y * sc; acc[6] += u1.z * sc; acc[7] += u1.w * sc;
-        }
-        if (whole) {
-          const float inv = 1.f / lsum;
-          uint4 pk;
-          __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-          __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[4] * inv, acc[5] * inv);
-          __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[6] * inv, acc[7] * inv);
-          pk.x = *reinterpret_cast<uint32_t*>(&b0); pk.y = *reinterpret_cast<uint32_t*>(&b1);
-          pk.z = *reinterpret_cast<uint32_t*>(&b2); pk.w = *reinterpret_cast<uint32_t*>(&b3);
-          uint16_t* dst = p.out + (static_cast<size_t>(cur.a) * p.H_q + cur.g * p.G + h) * D + c8 * 8;
-          *reinterpret_cast<uint4*>(dst) = pk;
-        } else {
-          float4* dst = reinterpret_cast<float4*>(slotp + h * D + c8 * 8);
-          dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-          dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-          if (c8 == 0) {
-            slotp[GP * D + h] = M;
-            slotp[slot_l_offset(GP, D) + h] = lsum;
+              for (int h = 0; h < GP; ++h)
+                if (h == d) {
+                  slotp[GP * D + h] = m_ref[h];
+                  slotp[slot_l_offset(GP, D) + h] = l[h];
+                }
+            }
           }
         }
       }
-      named_bar_sync(1, NCW * 32);
-      m_run = -INFINITY;
-      l_run = 0.f;
-#pragma unroll
-      for (int i = 0; i < GP; ++i)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) o[i][c] = make_float2(0.f, 0.f);
     }
   }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // K3: for every segment cut by a CTA boundary, merge the partials of the CTAs
@@ -489,31 +491,53 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   }
 }
 
+cudaError_t make_decode_maps(const DecodeParams& p, DecodeMaps* m) {
+  auto enc = tma_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t D = p.D;
+  cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(p.max_seq), static_cast<cuuint64_t>(p.S) * p.H_kv};
+  cuuint64_t strides[2] = {D * 2, D * 2 * static_cast<cuuint64_t>(p.max_seq)};
+  cuuint32_t box[3] = {64, BOX_ROWS, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  for (int t = 0; t < 2; ++t) {
+    if (enc(t == 0 ? &m->kc : &m->vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<uint16_t*>(t == 0 ? p.k_cache : p.v_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  // Queries as rows of D; a group reads 16 rows (its G heads, then padding
+  // that is never used; rows past the tensor read as zeros).
+  cuuint64_t qdims[3] = {D, static_cast<cuuint64_t>(p.A) * p.H_q, 1};
+  cuuint64_t qstrides[2] = {D * 2, D * 2 * static_cast<cuuint64_t>(p.A) * p.H_q};
+  cuuint32_t qbox[3] = {64, NQ, 1};
+  if (enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.q), qdims, qstrides, qbox, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 template <int D, int GP>
 struct Kernels {
-  static void* splitk() { return reinterpret_cast<void*>(&flash_decode_splitk_kernel<D, GP>); }
   static cudaError_t prepare(int device, int* num_ctas) {
-    // Opt in to the large dynamic shared memory once per device.
     static std::once_flag flags[64];
     static cudaError_t errs[64];
     static int ctas[64];
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::call_once(flags[device], [&]() {
       errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, GP>::SMEM);
-      int sms = 0, per_sm = 0;
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+      int sms = 0;
       if (errs[device] == cudaSuccess)
         errs[device] = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-      if (errs[device] == cudaSuccess)
-        errs[device] = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, flash_decode_splitk_kernel<D, GP>, THREADS, Cfg<D, GP>::SMEM);
-      ctas[device] = sms * (per_sm > 0 ? per_sm : 1);
+      ctas[device] = sms;  // one CTA per SM (the shared-memory ring fills an SM)
     });
     *num_ctas = ctas[device];
     return errs[device];
   }
-  static cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
-    flash_decode_splitk_kernel<D, GP><<<p.num_ctas, THREADS, Cfg<D, GP>::SMEM, stream>>>(p);
+  static cudaError_t launch(const DecodeParams& p, const DecodeMaps& m, cudaStream_t stream) {
+    flash_decode_splitk_kernel<D, GP><<<p.num_ctas, THREADS, Cfg<D>::SMEM, stream>>>(p, m.kc, m.vc, m.q);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     decode_combine_kernel<D, GP><<<p.A * p.H_kv, 128, 0, stream>>>(p);
@@ -529,6 +553,7 @@ cudaError_t dispatch(int D, int GP, F&& f) {
       case 2: return f(Kernels<128, 2>{});
       case 4: return f(Kernels<128, 4>{});
       case 8: return f(Kernels<128, 8>{});
+      case 16: return f(Kernels<128, 16>{});
     }
   } else if (D == 64) {
     switch (GP) {
@@ -536,6 +561,7 @@ cudaError_t dispatch(int D, int GP, F&& f) {
       case 2: return f(Kernels<64, 2>{});
       case 4: return f(Kernels<64, 4>{});
       case 8: return f(Kernels<64, 8>{});
+      case 16: return f(Kernels<64, 16>{});
     }
   }
   return cudaErrorInvalidValue;
@@ -577,8 +603,11 @@ cudaError_t static_scratch_address(int device, void** ptr) {
 
 cudaError_t launch_cached_gqa_attention(const DecodeParams& p, cudaStream_t stream) {
   if (p.A == 0) return cudaSuccess;
+  DecodeMaps m;
+  const cudaError_t e = make_decode_maps(p, &m);
+  if (e != cudaSuccess) return e;
   const int GP = decode_group_pad(p.G);
-  return dispatch(p.D, GP, [&](auto k) { return decltype(k)::launch(p, stream); });
+  return dispatch(p.D, GP, [&](auto k) { return decltype(k)::launch(p, m, stream); });
 }
 
 }  // namespace kvgqa

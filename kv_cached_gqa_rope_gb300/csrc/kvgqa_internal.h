@@ -3,9 +3,14 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 namespace kvgqa {
+
+// cuTensorMapEncodeTiled from the driver (looked up once); nullptr if absent.
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder();
 
 constexpr int kMaxHeadDim = 128;
 constexpr int kMaxActiveRows = 2048;  // decode attention keeps a prefix table of A+1 ints in smem

@@ -316,22 +316,8 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 cudaError_t make_maps(const PrefillParams& p, PrefillMaps* m) {
-  auto enc = encode_fn();
+  auto enc = tma_encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t D = p.D;
   {
@@ -382,6 +368,20 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t 
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
 
 cudaError_t launch_prefill_attention(const PrefillParams& p, cudaStream_t stream) {
   if (p.A == 0 || p.T == 0) return cudaSuccess;

@@ -170,7 +170,7 @@ def test_attention_contract():
     a = attention_args()
     a["scale"] = float("nan")
     assert code_of(kv.cached_gqa_attention_out_, **a) == "EINVAL"
-    a = attention_args(H_q=32, H_kv=2)          # G = 16 has no decode kernel
+    a = attention_args(H_q=64, H_kv=2)          # G = 32 has no decode kernel
     assert code_of(kv.cached_gqa_attention_out_, **a) == "EUNSUPPORTED"
     a = attention_args()
     a["v_cache"] = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16)
