@@ -9,13 +9,16 @@
 // precision softmax keeps FP32 reductions and rounds only the caller output.
 //
 // Work split.  Segment (a, g) is the prefix of KV head g in row cache_rows[a]:
-// n_a = positions[a] + 1 keys, contiguous in memory.  All segments, laid end to
-// end, form one key range of K_tot keys; CTA b of the persistent grid (one CTA
-// per SM) takes keys [b*W, (b+1)*W) with W = ceil(K_tot / grid), so every SM
-// streams the same number of bytes whatever the length mix.  A segment that
-// lies inside one CTA is finished there (BF16 out written); a segment cut by a
-// CTA boundary leaves FP32 partials (m, l, o) that K3 merges.  Each CTA writes
-// at most two partials (its first and its last segment).
+// n_a = positions[a] + 1 keys, contiguous in memory.  A tile costs about the
+// same whether it holds 128 keys or a short tail (its softmax and P.V round
+// trip dominate), so work is balanced in a virtual key space where segment
+// (a, g) occupies ceil(n_a / 128) * 128 + SEG_V keys: its n_a real keys first,
+// then padding that stands for the cost of its tail tile and its end.  CTA b
+// of the persistent grid (one CTA per SM) takes the virtual range
+// [b*W, (b+1)*W), W = ceil(V_tot / grid), and processes the real keys in it.
+// A segment whose real keys lie inside one CTA is finished there (BF16 out
+// written); a segment cut by a CTA boundary leaves FP32 partials (m, l, o)
+// that K3 merges: the CTA where it starts writes slot 1, each later CTA slot 0.
 //
 // Inside a CTA, per tile of up to 128 keys of one segment:
 //   warp 4     TMA producer: K and V tiles (128B swizzle, 32-row boxes, so a
@@ -55,7 +58,8 @@ constexpr int SUB = BN * 128;           // one [128 rows x 64 bf16] swizzled sub
 constexpr int QSUB = NQ * 128;          // one [16 rows x 64 bf16] swizzled sub-tile
 constexpr int THREADS = 192;            // 4 softmax warps + producer + MMA
 constexpr int TMEM_COLS = 64;           // S^T x2 (16 cols each) + O^T (16 cols)
-constexpr int W_MIN = 256;              // fewest keys a CTA is given
+constexpr int W_MIN = 256;              // fewest (virtual) keys a CTA is given
+constexpr int SEG_V = 32;               // virtual keys charged for a segment end
 constexpr unsigned FULL = 0xffffffffu;
 
 // One split-K partial result: o[GP][D], then m[GP], then l[GP] (each of the
@@ -73,12 +77,12 @@ struct Cfg {
   static constexpr int V_OFF = NSUB * SUB;
   static constexpr int Q_OFF = 2 * NSUB * SUB;
   static constexpr int STAGE = 2 * NSUB * SUB + NSUB * QSUB;   // multiple of 1024
-  static constexpr int P_OFF = NS * STAGE;                     // P^T [16 x 128 keys], 2 sub-tiles
-  static constexpr int RED_OFF = P_OFF + 2 * QSUB;             // [2][4 warps][16] floats
+  static constexpr int P_OFF = NS * STAGE;                     // P^T x2 buffers, [16 x 128 keys] each
+  static constexpr int RED_OFF = P_OFF + 2 * 2 * QSUB;         // [2][4 warps][16] floats
   static constexpr int PREFIX_OFF = RED_OFF + 2 * 4 * NQ * 4;  // [kMaxActiveRows + 1] ints
   static constexpr int BAR_OFF = align_up(PREFIX_OFF + (kMaxActiveRows + 1) * 4, 16);
-  // kv_full[NS], kv_empty[NS], s_full[2], p_full, o_done, drain
-  static constexpr int NBAR = 2 * NS + 5;
+  // kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NBAR = 2 * NS + 7;
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 8;
   static constexpr int SMEM = FLAG_OFF + 16 + 1024;            // + alignment slack
@@ -92,8 +96,11 @@ struct DecodeMaps {
   CUtensorMap q;   // q_rot [A*H_q][D], box {64, 16}
 };
 
-// Per-row key counts and their running sum (times H_kv): prefix[a] is the
-// flattened start of row a's first segment.  Invalid metadata -> 0 keys.
+// Virtual length of a segment of n real keys (0 for an invalid row).
+__device__ __forceinline__ int seg_vlen(int n) { return n == 0 ? 0 : (n + BN - 1) / BN * BN + SEG_V; }
+
+// Running sum over rows of H_kv * seg_vlen(n_a): prefix[a] is the virtual
+// start of row a's first segment.  Invalid metadata -> an empty row.
 __device__ void build_prefix(const DecodeParams& p, int* prefix, bool flag) {
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
@@ -106,7 +113,7 @@ __device__ void build_prefix(const DecodeParams& p, int* prefix, bool flag) {
         const int row = p.cache_rows[a];
         const bool pos_ok = pos >= 0 && pos < p.max_seq;
         const bool row_ok = row >= 0 && row < p.S;
-        if (pos_ok && row_ok) n = (pos + 1) * p.H_kv;
+        if (pos_ok && row_ok) n = seg_vlen(pos + 1) * p.H_kv;
         bad |= (pos_ok ? 0 : KVGQA_FLAG_POSITION_RANGE) | (row_ok ? 0 : KVGQA_FLAG_ROW_RANGE);
       }
       int incl = n;
@@ -130,49 +137,72 @@ __device__ __forceinline__ int keys_per_cta(int k_tot, int num_ctas) {
   return w < W_MIN ? W_MIN : w;
 }
 
-// Walks the tiles of one CTA's key range [x0, x1): segment by segment, BN keys
-// at a time.  Every role runs its own identical copy.
+// Walks the tiles of one CTA's virtual range [v0, v1): segment by segment, the
+// real keys of each in tiles of at most BN.  Every role runs its own copy.
 struct Cursor {
   const int* prefix;
-  int H_kv, x0, x1;
-  int x, a, g, n, seg_lo, seg_in;  // seg_in: where this CTA entered the segment
+  const int32_t* positions;
+  int H_kv, A, v0, v1;
+  int a, g, n, vlen, vlo;  // current segment: row, head, real keys, virtual length and start
+  int x, x_end;            // next real key of the segment and the end of this CTA's part
+  int k_first;             // first real key of this CTA's part of the segment
 
-  __device__ __forceinline__ int row_keys(int r) const { return (prefix[r + 1] - prefix[r]) / H_kv; }
+  __device__ __forceinline__ int row_vlen(int r) const { return (prefix[r + 1] - prefix[r]) / H_kv; }
 
-  __device__ void init(const int* pf, int h_kv, int A, int lo, int hi) {
-    prefix = pf; H_kv = h_kv; x0 = lo; x1 = hi; x = lo;
-    int l = 0, r = A - 1;  // last row with prefix[row] <= x0
+  // Enter segment (a, g): clip its real keys to [v0, v1); false if none.
+  __device__ __forceinline__ bool enter() {
+    n = positions[a] + 1;
+    vlen = row_vlen(a);
+    vlo = prefix[a] + g * vlen;
+    const int lo = max(v0, vlo), hi = min(v1, vlo + n);
+    x = lo - vlo;
+    x_end = hi - vlo;
+    k_first = x;
+    return lo < hi;
+  }
+  // Step to the next segment that starts before v1; false when there is none.
+  __device__ __forceinline__ bool next_segment() {
+    for (;;) {
+      if (++g == H_kv) {
+        g = 0;
+        do { ++a; } while (a < A && row_vlen(a) == 0);
+        if (a >= A) return false;
+      }
+      if (prefix[a] + g * row_vlen(a) >= v1) return false;
+      if (enter()) return true;
+    }
+  }
+  __device__ void init(const int* pf, const int32_t* pos, int h_kv, int rows, int lo, int hi) {
+    prefix = pf; positions = pos; H_kv = h_kv; A = rows; v0 = lo; v1 = hi;
+    int l = 0, r = A - 1;  // last row with prefix[row] <= v0
     while (l < r) {
       const int mid = (l + r + 1) >> 1;
       if (prefix[mid] <= lo) l = mid; else r = mid - 1;
     }
     a = l;
-    while (row_keys(a) == 0) ++a;
-    n = row_keys(a);
-    g = (lo - prefix[a]) / n;
-    seg_lo = prefix[a] + g * n;
-    seg_in = lo;
-  }
-  __device__ __forceinline__ bool more() const { return x < x1; }
-  __device__ __forceinline__ int seg_end() const { return min(seg_lo + n, x1); }
-  __device__ __forceinline__ int k0() const { return x - seg_lo; }
-  __device__ __forceinline__ int nt() const { return min(BN, seg_end() - x); }
-  __device__ __forceinline__ bool first() const { return x == seg_in; }
-  __device__ __forceinline__ bool last() const { return x + nt() == seg_end(); }
-  __device__ __forceinline__ bool whole() const { return seg_lo >= x0 && seg_lo + n <= x1; }
-  __device__ __forceinline__ int slot() const { return seg_in == x0 ? 0 : 1; }
-  __device__ void advance() {
-    const bool was_last = last();
-    x += nt();
-    if (was_last && x < x1) {
-      if (++g == H_kv) {
-        g = 0;
-        do { ++a; } while (row_keys(a) == 0);
-        n = row_keys(a);
-      }
-      seg_lo = prefix[a] + g * n;
-      seg_in = x;
+    while (row_vlen(a) == 0) ++a;
+    g = (lo - prefix[a]) / row_vlen(a);
+    if (!enter()) {
+      if (!next_segment()) x = x_end = 0, done_ = true;
     }
+  }
+  bool done_ = false;
+  __device__ __forceinline__ bool more() const { return !done_; }
+  __device__ __forceinline__ int k0() const { return x; }
+  __device__ __forceinline__ int nt() const { return min(BN, x_end - x); }
+  __device__ __forceinline__ bool first() const { return x == k_first; }
+  __device__ __forceinline__ bool last() const { return x + nt() == x_end; }
+  __device__ __forceinline__ bool whole() const { return vlo >= v0 && vlo + n <= v1; }
+  __device__ __forceinline__ int slot() const { return vlo < v0 ? 0 : 1; }
+  // Another tile follows in this CTA (used to run S of the next tile early).
+  __device__ __forceinline__ bool has_next() const {
+    if (!last()) return true;
+    Cursor c = *this;
+    return c.next_segment();
+  }
+  __device__ void advance() {
+    if (!last()) { x += nt(); return; }
+    if (!next_segment()) done_ = true;
   }
 };
 
@@ -195,8 +225,8 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   uint64_t* kv_empty = bars + C::NS;
   uint64_t* s_full = bars + 2 * C::NS;
   uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* drain = o_done + 1;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -206,21 +236,24 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, BN);
-    mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], BN);
+      mbar_init(&o_done[b], 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   build_prefix(p, prefix, blockIdx.x == 0);  // ends with __syncthreads
 
-  const int k_tot = prefix[p.A];
-  const int W = keys_per_cta(k_tot, p.num_ctas);
-  const int x0 = blockIdx.x * W;
-  if (x0 >= k_tot) return;  // uniform: nothing allocated yet
-  const int x1 = min(x0 + W, k_tot);
+  const int v_tot = prefix[p.A];
+  const int W = keys_per_cta(v_tot, p.num_ctas);
+  const int v0 = blockIdx.x * W;
+  const int v1 = min(v0 + W, v_tot);
+  Cursor cur;
+  if (v0 < v_tot) cur.init(prefix, p.positions, p.H_kv, p.A, v0, v1);
+  if (v0 >= v_tot || !cur.more()) return;  // uniform: nothing allocated yet
 
   if (warp == 5) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -231,9 +264,6 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(smem);
-
-  Cursor cur;
-  cur.init(prefix, p.H_kv, p.A, x0, x1);
 
   if (warp == 4) {
     // ---------------------------------------------------------- TMA producer
@@ -293,23 +323,24 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
           tc_fence_after();
           issue_s(0);
         }
-        if (cur.x + cur.nt() < cur.x1) {  // another tile follows: overlap its S with this softmax
+        if (cur.has_next()) {  // another tile follows: overlap its S with this softmax
           const int t = it + 1;
           if (!mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, abort_flag, p.status)) break;
           tc_fence_after();
           issue_s(t);
         }
-        if (!mbar_wait_bounded(p_full, it & 1, abort_flag, p.status)) break;
+        if (!mbar_wait_bounded(&p_full[it & 1], (it >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t v_addr = sbase + (it % C::NS) * C::STAGE + C::V_OFF;
+        const uint32_t pb_addr = p_addr + (it & 1) * 2 * QSUB;
         const uint32_t acc0 = cur.first() ? 0u : 1u;
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           umma_f16_ss(tmem + 2 * NQ, smem_desc_sw128(v_addr + ks * 2048, V_LBO, 1024),
-                      smem_desc_sw128(p_addr + (ks / 4) * QSUB + (ks % 4) * 32, 16, 1024), IDESC_O,
+                      smem_desc_sw128(pb_addr + (ks / 4) * QSUB + (ks % 4) * 32, 16, 1024), IDESC_O,
                       ks > 0 ? 1u : acc0);
         }
-        umma_commit(o_done);
+        umma_commit(&o_done[it & 1]);
         umma_commit(&kv_empty[it % C::NS]);
       }
       if (*abort_flag && issued) {
@@ -324,7 +355,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float* red_max = reinterpret_cast<float*>(smem + C::RED_OFF);
     float* red_sum = red_max + 4 * NQ;
-    unsigned char* pt = smem + C::P_OFF;
+    unsigned char* pt0 = smem + C::P_OFF;
     float m_ref[GP], l[GP];
 #pragma unroll
     for (int h = 0; h < GP; ++h) { m_ref[h] = -INFINITY; l[h] = 0.f; }
@@ -363,8 +394,12 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         }
         l[h] = first ? 0.f : l[h] * alpha[h];
       }
-      // The previous tile's P.V must be complete before P^T is rewritten or O^T rescaled.
-      if (it > 0 && !__all_sync(FULL, mbar_wait_bounded(o_done, (it - 1) & 1, abort_flag, p.status))) break;
+      // P^T buffer it&1 was last read by the P.V of tile it-2; an O^T rescale
+      // needs the P.V of tile it-1 to be complete.
+      if (it > 1 && !__all_sync(FULL, mbar_wait_bounded(&o_done[it & 1], ((it - 2) >> 1) & 1, abort_flag, p.status))) break;
+      if (grow_any && it > 0 &&
+          !__all_sync(FULL, mbar_wait_bounded(&o_done[(it - 1) & 1], ((it - 1) >> 1) & 1, abort_flag, p.status)))
+        break;
       tc_fence_after();
       if (grow_any) {  // uniform across the CTA: every thread saw the same maxima
         uint32_t o[16];
@@ -378,6 +413,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       // P^T[h][r] as BF16 (K-major B operand: 16 rows of 128 keys, two 64-key
       // swizzled sub-tiles); padded heads and invalid keys are zero.
       const int sub = r >> 6, chunk = (r & 63) >> 3, e = r & 7;
+      unsigned char* pt = pt0 + (it & 1) * 2 * QSUB;
 #pragma unroll
       for (int h = 0; h < NQ; ++h) {
         uint16_t b = 0;
@@ -404,11 +440,11 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       for (int h = 0; h < GP; ++h)
         l[h] += (red_sum[h] + red_sum[NQ + h]) + (red_sum[2 * NQ + h] + red_sum[3 * NQ + h]);
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[it & 1]);
 
       if (cur.last()) {
         // ---------------------------------------------------- segment end
-        if (!__all_sync(FULL, mbar_wait_bounded(o_done, it & 1, abort_flag, p.status))) break;
+        if (!__all_sync(FULL, mbar_wait_bounded(&o_done[it & 1], (it >> 1) & 1, abort_flag, p.status))) break;
         tc_fence_after();
         uint32_t o[16];
         tmem_ld16(tmem + lane_base + 2 * NQ, o);
@@ -452,13 +488,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   __shared__ int prefix[kMaxActiveRows + 1];
   build_prefix(p, prefix, false);
   const int a = blockIdx.x / p.H_kv, g = blockIdx.x - a * p.H_kv;
-  const int n = (prefix[a + 1] - prefix[a]) / p.H_kv;
-  if (n == 0) return;
+  const int vlen = (prefix[a + 1] - prefix[a]) / p.H_kv;
+  if (vlen == 0) return;
+  const int n = p.positions[a] + 1;
   const int W = keys_per_cta(prefix[p.A], p.num_ctas);
-  const int seg_lo = prefix[a] + g * n;
-  const int b0 = seg_lo / W, b1 = (seg_lo + n - 1) / W;
+  const int vlo = prefix[a] + g * vlen;
+  const int b0 = vlo / W, b1 = (vlo + n - 1) / W;
   if (b0 == b1) return;  // finished by the split-K kernel
-  const int slot0 = (b0 * W == seg_lo) ? 0 : 1;
+  const int slot0 = 1;   // the CTA where the segment starts wrote slot 1
   constexpr size_t SLOT = slot_floats(GP, D);
   for (int item = threadIdx.x; item < p.G * (D / 8); item += blockDim.x) {
     const int h = item / (D / 8), c8 = item - h * (D / 8);

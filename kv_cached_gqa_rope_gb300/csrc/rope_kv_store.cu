@@ -23,9 +23,14 @@
 namespace kvgqa {
 namespace {
 
-struct CosSin {
+struct __align__(16) CosSin {
   float ch, cl, sh, sl;  // cos = ch + cl, sin = sh + sl
 };
+
+// The cos/sin table is read eight consecutive entries at a time by lanes that
+// differ in which group of eight they read; one 16-byte pad after every eight
+// entries puts those lanes on different shared-memory banks.
+__device__ __forceinline__ int cs_slot(int i) { return i + (i >> 3); }
 
 // x1 * C - x2 * S with C, S given as hi+lo pairs.  Products are split exactly
 // with FMA; intrinsics keep the compiler from contracting them differently.
@@ -56,6 +61,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Rotate the 8 pairs (a[i], b[i]) held in two 16-byte chunks.
 __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const CosSin* cs,
                                         uint4& ya, uint4& yb) {
+  // cs points at the padded slot of pair 8c; the eight pairs follow contiguously
   const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
   const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
   uint32_t oa[4], ob[4];
@@ -77,7 +83,7 @@ __global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constan
   constexpr int HALF = D / 2;
   constexpr int RU = D / 16;  // rotation units per head: 8 pairs each
   constexpr int VU = D / 8;   // copy units per head: 8 elements (16 bytes) each
-  __shared__ CosSin cs[HALF];
+  __shared__ CosSin cs[HALF + HALF / 8];
 
   int pos, ntok;
   if (prefill) {
@@ -111,47 +117,47 @@ __global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constan
     v.cl = static_cast<float>(c - static_cast<double>(v.ch));
     v.sh = static_cast<float>(s);
     v.sl = static_cast<float>(s - static_cast<double>(v.sh));
-    cs[i] = v;
+    cs[cs_slot(i)] = v;
   }
   __syncthreads();
 
   const int units = (p.H_q + p.H_kv) * RU + p.H_kv * VU;
-  for (int u = threadIdx.x; u < ntok * units; u += blockDim.x) {
-    const int ti = u / units;
-    const int r = u - ti * units;
+  for (int ti = 0; ti < ntok; ++ti) {
     const int a = prefill ? ti : blockIdx.x;
     const int row = p.cache_rows[a];
     if (prefill && (row < 0 || row >= p.S)) {
-      if (r == 0) atomicOr(p.status, KVGQA_FLAG_ROW_RANGE);
+      if (threadIdx.x == 0) atomicOr(p.status, KVGQA_FLAG_ROW_RANGE);
       continue;
     }
     const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : static_cast<size_t>(a);
     const size_t q_base = tok * p.H_q * D;
     const size_t kv_base = tok * p.H_kv * D;
-    if (r < (p.H_q + p.H_kv) * RU) {
-      const int h = r / RU, c = r - (r / RU) * RU;
-      const uint16_t* src;
-      uint16_t* dst;
-      if (h < p.H_q) {
-        src = p.q + q_base + static_cast<size_t>(h) * D;
-        dst = p.q_out + q_base + static_cast<size_t>(h) * D;
+    for (int r = threadIdx.x; r < units; r += blockDim.x) {
+      if (r < (p.H_q + p.H_kv) * RU) {
+        const int h = r / RU, c = r % RU;
+        const uint16_t* src;
+        uint16_t* dst;
+        if (h < p.H_q) {
+          src = p.q + q_base + static_cast<size_t>(h) * D;
+          dst = p.q_out + q_base + static_cast<size_t>(h) * D;
+        } else {
+          const int g = h - p.H_q;
+          src = p.k + kv_base + static_cast<size_t>(g) * D;
+          dst = p.k_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D;
+        }
+        const uint4 a8 = *reinterpret_cast<const uint4*>(src + c * 8);
+        const uint4 b8 = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
+        uint4 ya, yb;
+        rotate8(a8, b8, cs + cs_slot(c * 8), ya, yb);
+        *reinterpret_cast<uint4*>(dst + c * 8) = ya;
+        *reinterpret_cast<uint4*>(dst + HALF + c * 8) = yb;
       } else {
-        const int g = h - p.H_q;
-        src = p.k + kv_base + static_cast<size_t>(g) * D;
-        dst = p.k_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D;
+        const int rr = r - (p.H_q + p.H_kv) * RU;
+        const int g = rr / VU, c = rr % VU;
+        const uint16_t* src = p.v + kv_base + static_cast<size_t>(g) * D + c * 8;
+        uint16_t* dst = p.v_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D + c * 8;
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
       }
-      const uint4 a8 = *reinterpret_cast<const uint4*>(src + c * 8);
-      const uint4 b8 = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
-      uint4 ya, yb;
-      rotate8(a8, b8, cs + c * 8, ya, yb);
-      *reinterpret_cast<uint4*>(dst + c * 8) = ya;
-      *reinterpret_cast<uint4*>(dst + HALF + c * 8) = yb;
-    } else {
-      const int rr = r - (p.H_q + p.H_kv) * RU;
-      const int g = rr / VU, c = rr - (rr / VU) * VU;
-      const uint16_t* src = p.v + kv_base + static_cast<size_t>(g) * D + c * 8;
-      uint16_t* dst = p.v_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D + c * 8;
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
     }
   }
 }
