@@ -167,7 +167,7 @@ kvgqa_status cached_gqa_attention_workspace_size(int64_t A, int64_t H_q, int64_t
  *   out [A,H_q,D] bf16 (written; rows with invalid metadata are left unwritten)
  *   workspace  >= cached_gqa_attention_workspace_size(...) bytes, 256-byte aligned
  * Limits: D in {64,128}; G = H_q / H_kv <= 16;
- * A <= 2048; A * H_kv * max_seq < 2^31.  A = 0 is a no-op.
+ * A <= 1024; A * H_kv * max_seq < 2^31.  A = 0 is a no-op.
  */
 kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_tensor* k_cache,
                                        const kvgqa_tensor* v_cache,

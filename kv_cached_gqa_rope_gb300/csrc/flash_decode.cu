@@ -59,7 +59,7 @@ constexpr int QSUB = NQ * 128;          // one [16 rows x 64 bf16] swizzled sub-
 constexpr int THREADS = 192;            // 4 softmax warps + producer + MMA
 constexpr int TMEM_COLS = 64;           // S^T x2 (16 cols each) + O^T (16 cols)
 constexpr int W_MIN = 256;              // fewest (virtual) keys a CTA is given
-constexpr int SEG_V = 32;               // virtual keys charged for a segment end
+constexpr int SEG_V = 128;              // virtual keys charged for a segment end
 constexpr unsigned FULL = 0xffffffffu;
 
 // One split-K partial result: o[GP][D], then m[GP], then l[GP] (each of the
@@ -80,7 +80,8 @@ struct Cfg {
   static constexpr int P_OFF = NS * STAGE;                     // P^T x2 buffers, [16 x 128 keys] each
   static constexpr int RED_OFF = P_OFF + 2 * 2 * QSUB;         // [2][4 warps][16] floats
   static constexpr int PREFIX_OFF = RED_OFF + 2 * 4 * NQ * 4;  // [kMaxActiveRows + 1] ints
-  static constexpr int BAR_OFF = align_up(PREFIX_OFF + (kMaxActiveRows + 1) * 4, 16);
+  static constexpr int NKEYS_OFF = PREFIX_OFF + (kMaxActiveRows + 1) * 4;  // [kMaxActiveRows] ints
+  static constexpr int BAR_OFF = align_up(NKEYS_OFF + kMaxActiveRows * 4, 16);
   // kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
   static constexpr int NBAR = 2 * NS + 7;
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
@@ -101,7 +102,7 @@ __device__ __forceinline__ int seg_vlen(int n) { return n == 0 ? 0 : (n + BN - 1
 
 // Running sum over rows of H_kv * seg_vlen(n_a): prefix[a] is the virtual
 // start of row a's first segment.  Invalid metadata -> an empty row.
-__device__ void build_prefix(const DecodeParams& p, int* prefix, bool flag) {
+__device__ void build_prefix(const DecodeParams& p, int* prefix, int* nkeys, bool flag) {
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
     int carry = 0, bad = 0;
@@ -114,6 +115,7 @@ __device__ void build_prefix(const DecodeParams& p, int* prefix, bool flag) {
         const bool pos_ok = pos >= 0 && pos < p.max_seq;
         const bool row_ok = row >= 0 && row < p.S;
         if (pos_ok && row_ok) n = seg_vlen(pos + 1) * p.H_kv;
+        nkeys[a] = pos_ok && row_ok ? pos + 1 : 0;
         bad |= (pos_ok ? 0 : KVGQA_FLAG_POSITION_RANGE) | (row_ok ? 0 : KVGQA_FLAG_ROW_RANGE);
       }
       int incl = n;
@@ -141,7 +143,7 @@ __device__ __forceinline__ int keys_per_cta(int k_tot, int num_ctas) {
 // real keys of each in tiles of at most BN.  Every role runs its own copy.
 struct Cursor {
   const int* prefix;
-  const int32_t* positions;
+  const int* nkeys;
   int H_kv, A, v0, v1;
   int a, g, n, vlen, vlo;  // current segment: row, head, real keys, virtual length and start
   int x, x_end;            // next real key of the segment and the end of this CTA's part
@@ -151,7 +153,7 @@ struct Cursor {
 
   // Enter segment (a, g): clip its real keys to [v0, v1); false if none.
   __device__ __forceinline__ bool enter() {
-    n = positions[a] + 1;
+    n = nkeys[a];
     vlen = row_vlen(a);
     vlo = prefix[a] + g * vlen;
     const int lo = max(v0, vlo), hi = min(v1, vlo + n);
@@ -172,8 +174,8 @@ struct Cursor {
       if (enter()) return true;
     }
   }
-  __device__ void init(const int* pf, const int32_t* pos, int h_kv, int rows, int lo, int hi) {
-    prefix = pf; positions = pos; H_kv = h_kv; A = rows; v0 = lo; v1 = hi;
+  __device__ void init(const int* pf, const int* nk, int h_kv, int rows, int lo, int hi) {
+    prefix = pf; nkeys = nk; H_kv = h_kv; A = rows; v0 = lo; v1 = hi;
     int l = 0, r = A - 1;  // last row with prefix[row] <= v0
     while (l < r) {
       const int mid = (l + r + 1) >> 1;
@@ -220,6 +222,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   int* prefix = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
+  int* nkeys = reinterpret_cast<int*>(smem + C::NKEYS_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + C::NS;
@@ -245,14 +248,16 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     *abort_flag = 0;
     fence_mbar_init();
   }
-  build_prefix(p, prefix, blockIdx.x == 0);  // ends with __syncthreads
+  pdl_wait();     // everything below may read what the previous kernel wrote
+  pdl_trigger();  // let the combine kernel launch and run its own set-up
+  build_prefix(p, prefix, nkeys, blockIdx.x == 0);  // ends with __syncthreads
 
   const int v_tot = prefix[p.A];
   const int W = keys_per_cta(v_tot, p.num_ctas);
   const int v0 = blockIdx.x * W;
   const int v1 = min(v0 + W, v_tot);
   Cursor cur;
-  if (v0 < v_tot) cur.init(prefix, p.positions, p.H_kv, p.A, v0, v1);
+  if (v0 < v_tot) cur.init(prefix, nkeys, p.H_kv, p.A, v0, v1);
   if (v0 >= v_tot || !cur.more()) return;  // uniform: nothing allocated yet
 
   if (warp == 5) {
@@ -486,11 +491,15 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
 template <int D, int GP>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ int prefix[kMaxActiveRows + 1];
-  build_prefix(p, prefix, false);
+  __shared__ int nkeys[kMaxActiveRows];
+  // The split-K kernel passed its own wait before letting this grid start, so
+  // positions and cache rows are final; the partials are not until pdl_wait().
+  build_prefix(p, prefix, nkeys, false);
   const int a = blockIdx.x / p.H_kv, g = blockIdx.x - a * p.H_kv;
   const int vlen = (prefix[a + 1] - prefix[a]) / p.H_kv;
+  pdl_wait();
   if (vlen == 0) return;
-  const int n = p.positions[a] + 1;
+  const int n = nkeys[a];
   const int W = keys_per_cta(prefix[p.A], p.num_ctas);
   const int vlo = prefix[a] + g * vlen;
   const int b0 = vlo / W, b1 = (vlo + n - 1) / W;
@@ -574,11 +583,22 @@ struct Kernels {
     return errs[device];
   }
   static cudaError_t launch(const DecodeParams& p, const DecodeMaps& m, cudaStream_t stream) {
-    flash_decode_splitk_kernel<D, GP><<<p.num_ctas, THREADS, Cfg<D>::SMEM, stream>>>(p, m.kc, m.vc, m.q);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_ctas);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP>, p, m.kc, m.vc, m.q);
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<D, GP><<<p.A * p.H_kv, 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(p.A * p.H_kv);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, GP>, p);
   }
 };
 

@@ -13,7 +13,7 @@ namespace kvgqa {
 PFN_cuTensorMapEncodeTiled_v12000 tma_encoder();
 
 constexpr int kMaxHeadDim = 128;
-constexpr int kMaxActiveRows = 2048;  // decode attention keeps a prefix table of A+1 ints in smem
+constexpr int kMaxActiveRows = 1024;  // decode attention keeps per-row tables of A+1 ints in smem
 
 // ------------------------------------------------------------------ RoPE + store
 struct RopeStoreParams {

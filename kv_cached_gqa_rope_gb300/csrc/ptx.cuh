@@ -98,6 +98,15 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   return p;
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor in the
+// stream still runs; it must pass pdl_wait() before touching memory the
+// predecessor may write (its inputs included), and it lets its own successor
+// start early with pdl_trigger() (only after its own pdl_wait()).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ named barrier
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

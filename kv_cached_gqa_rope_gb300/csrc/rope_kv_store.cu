@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constan
   constexpr int VU = D / 8;   // copy units per head: 8 elements (16 bytes) each
   __shared__ CosSin cs[HALF + HALF / 8];
 
+  pdl_wait();     // inputs and outputs may belong to the previous kernel
+  pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
   int pos, ntok;
   if (prefill) {
     pos = blockIdx.x;  // position t, shared by all A prompts
@@ -167,13 +169,19 @@ __global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constan
 cudaError_t launch_rope_kv_store(const RopeStoreParams& p, bool prefill, cudaStream_t stream) {
   const unsigned grid = prefill ? static_cast<unsigned>(p.T) : static_cast<unsigned>(p.A);
   if (grid == 0) return cudaSuccess;
-  if (p.D == 128)
-    rope_kv_store_kernel<128><<<grid, 256, 0, stream>>>(p, prefill ? 1 : 0);
-  else if (p.D == 64)
-    rope_kv_store_kernel<64><<<grid, 256, 0, stream>>>(p, prefill ? 1 : 0);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int mode = prefill ? 1 : 0;
+  if (p.D == 128) return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<128>, p, mode);
+  if (p.D == 64) return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<64>, p, mode);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvgqa

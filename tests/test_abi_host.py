@@ -175,7 +175,7 @@ def test_attention_contract():
     a = attention_args()
     a["v_cache"] = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16)
     assert code_of(kv.cached_gqa_attention_out_, **a) == "EINVAL"
-    a = attention_args(A=3000)
+    a = attention_args(A=1100)
     assert code_of(kv.cached_gqa_attention_out_, **a) == "EUNSUPPORTED"
 
 
