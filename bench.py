@@ -255,8 +255,8 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("device status flags set during warm-up")
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # (1) the step as a user runs it: both calls back to back, events around the pair
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(dev.index) if rank == 0 and args.only is None else None
     if sampler:
         sampler.start()
@@ -265,18 +265,27 @@ def run_ours(args, rank, world, local):
     hold_gpu(K * (host_us["store"] + host_us["attention"] + 40.0))
     for i in range(K):
         flush.zero_()
-        e0, e1, e2 = ev[i]
-        e0.record(stream)
+        ev[i][0].record(stream)
         store()
-        e1.record(stream)
         attend()
-        e2.record(stream)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    step_ms = [a.elapsed_time(c) for a, b, c in ev]
-    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
-    store_ms = [a.elapsed_time(b) for a, b, c in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(float(sum(step_ms)), world)
+    # (2) the attention call alone (roofline of K2 + K3): the store runs before the
+    # first event so the events bracket exactly one cached_gqa_attention_out_ call
+    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    hold_gpu(K * (host_us["store"] + host_us["attention"] + 40.0))
+    for i in range(K):
+        flush.zero_()
+        store()
+        eva[i][0].record(stream)
+        attend()
+        eva[i][1].record(stream)
+    torch.cuda.synchronize()
+    attn_ms = [a.elapsed_time(b) for a, b in eva]
     flags = kv.kvgqa_read_status(ws1) | kv.kvgqa_read_status(ws2)
     if flags:
         raise RuntimeError(f"device status flags {flags} after the timed region")
@@ -339,7 +348,7 @@ def run_ours(args, rank, world, local):
                    "H_q": wl.H_q, "H_kv": wl.H_kv, "head_dim": wl.D, "theta": wl.theta,
                    "positions": "uniform [1,4096), seed 20261203", "l2": "flushed between timed steps (256 MB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "decode": {"attention_ms": round(attn_avg_s * 1e3, 5), "store_ms": round(float(np.mean(store_ms)), 5),
+        "decode": {"attention_ms": round(attn_avg_s * 1e3, 5),
                    "kv_bytes_per_step": attn_bytes, "step_bytes": step_bytes,
                    "kv_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm_peak, 4),
                    "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1)},

@@ -9,7 +9,8 @@
 // The rotated K and V have already been stored into the target cache rows
 // (K1), so this kernel reads them straight from the cache.
 //
-// One CTA computes a 128-query tile of one (prompt a, query head h):
+// A persistent grid (one CTA per SM) walks (128-query tile, prompt a, query
+// head h) items, longest first, dealt round-robin; per item:
 //   warp 4      TMA producer: the Q tile once, then 128-key K and V tiles of
 //               the row's cached prefix into a 2-stage ring (128B swizzle);
 //   warp 5      one thread issues tcgen05.mma: S = Q K^T into one of two TMEM
@@ -52,10 +53,10 @@ struct PCfg {
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = NSUB * SUB;
   static constexpr int STAGE = 2 * NSUB * SUB;      // K then V
-  static constexpr int P_OFF = KV_OFF + NS * STAGE;
-  static constexpr int BAR_OFF = P_OFF + 2 * SUB;
-  // barriers: q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full, o_done, drain
-  static constexpr int NBAR = 1 + 2 * NS + 2 + 3;
+  static constexpr int P_OFF = KV_OFF + NS * STAGE; // two P buffers of [128 x 128] BF16
+  static constexpr int BAR_OFF = P_OFF + 2 * 2 * SUB;
+  // q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NBAR = 2 + 2 * NS + 7;
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 8;
   static constexpr int SMEM = FLAG_OFF + 16 + 1024;  // + alignment slack
@@ -73,6 +74,58 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// 2^x on the special-function unit (flushes results below 2^-126 to zero,
+// which no BF16 probability needs).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The work of the persistent grid: items (query tile qt, prompt a, head h),
+// longest first (tile qt visits qt + 1 key tiles), dealt round-robin to the
+// CTAs; every role of a CTA walks the same sequence, tile by tile.
+struct TileWalk {
+  int i, stride, n_items, nqt, heads, H_q, H_kv, G, S;
+  const int32_t* rows;
+  int qt, a, h, kv_row;  // current item
+  int j;                 // key tile within the item
+  bool ok;               // false past the last item
+
+  __device__ bool load_item() {
+    while (i < n_items) {
+      qt = nqt - 1 - i / heads;
+      const int rem = i % heads;
+      a = rem / H_q;
+      h = rem % H_q;
+      const int r = rows[a];
+      if (r >= 0 && r < S) {
+        kv_row = r * H_kv + h / G;
+        j = 0;
+        return true;
+      }
+      i += stride;  // prompts with an invalid row are skipped (and flagged by the producer)
+    }
+    return false;
+  }
+  __device__ void init(const PrefillParams& p, int first, int step) {
+    nqt = (p.T + BM - 1) / BM;
+    heads = p.A * p.H_q;
+    n_items = nqt * heads;
+    H_q = p.H_q; H_kv = p.H_kv; G = p.G; S = p.S; rows = p.cache_rows;
+    i = first;
+    stride = step;
+    ok = load_item();
+  }
+  __device__ __forceinline__ bool first_tile() const { return j == 0; }
+  __device__ __forceinline__ bool last_tile() const { return j == qt; }
+  __device__ void advance() {
+    if (j < qt) { ++j; return; }
+    i += stride;
+    ok = load_item();
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap map_q,
@@ -83,38 +136,41 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
                                                          ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = bars + 1 + C::NS;
-  uint64_t* s_full = bars + 1 + 2 * C::NS;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;
+  uint64_t* kv_empty = kv_full + C::NS;
+  uint64_t* s_full = kv_empty + C::NS;
   uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* drain = o_done + 1;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nqt = (p.T + BM - 1) / BM;
-  const int heads = p.A * p.H_q;
-  const int qt = nqt - 1 - static_cast<int>(blockIdx.x) / heads;  // longest tiles first
-  const int rem = static_cast<int>(blockIdx.x) % heads;
-  const int a = rem / p.H_q, h = rem % p.H_q, g = h / p.G;
-  const int row = p.cache_rows[a];
-  if (row < 0 || row >= p.S) {
-    if (threadIdx.x == 0 && qt == nqt - 1 && h == 0) atomicOr(p.status, KVGQA_FLAG_ROW_RANGE);
+
+  TileWalk walk;
+  walk.init(p, blockIdx.x, gridDim.x);
+  if (!walk.ok) {  // uniform: this CTA has no valid item
+    if (threadIdx.x == 0) {
+      for (int i = blockIdx.x; i < walk.n_items; i += gridDim.x) {
+        const int r = p.cache_rows[(i % walk.heads) / p.H_q];
+        if (r < 0 || r >= p.S) { atomicOr(p.status, KVGQA_FLAG_ROW_RANGE); break; }
+      }
+    }
     return;
   }
-  const int nkt = qt + 1;  // key tiles 0..qt (the last one on the diagonal)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, BM);
-    mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], BM);
+      mbar_init(&o_done[b], 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -134,26 +190,39 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     if (lane == 0) {
       const uint64_t pol_q = l2_evict_first_policy();
       const uint64_t pol_kv = l2_evict_last_policy();  // K/V tiles are re-read by the group's heads
-      mbar_arrive_expect_tx(q_full, BM * D * 2);
-      for (int sub = 0; sub < C::NSUB; ++sub)
-        tma_load_4d(smem + C::Q_OFF + sub * SUB, &map_q, sub * 64, h, qt * BM, a, q_full, pol_q);
-      const int kv_row = row * p.H_kv + g;
-      int j = 0;
-      for (; j < nkt; ++j) {
-        const int s = j % C::NS;
-        if (j >= C::NS && !mbar_wait_bounded(&kv_empty[s], ((j / C::NS) - 1) & 1, abort_flag, p.status)) break;
+      // prompts whose cache row is invalid are skipped by every role; flag them here
+      for (int i = blockIdx.x; i < walk.n_items; i += gridDim.x) {
+        const int r = p.cache_rows[(i % walk.heads) / p.H_q];
+        if (r < 0 || r >= p.S) { atomicOr(p.status, KVGQA_FLAG_ROW_RANGE); break; }
+      }
+      int it = 0, qi = 0;
+      bool ok = true;
+      for (; walk.ok && ok; walk.advance()) {
+        if (walk.first_tile()) {
+          if (qi >= 1 && !mbar_wait_bounded(q_empty, (qi - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(q_full, BM * D * 2);
+          for (int sub = 0; sub < C::NSUB; ++sub)
+            tma_load_4d(smem + C::Q_OFF + sub * SUB, &map_q, sub * 64, walk.h, walk.qt * BM, walk.a, q_full, pol_q);
+          ++qi;
+        }
+        const int s = it % C::NS;
+        if (it >= C::NS && !mbar_wait_bounded(&kv_empty[s], ((it / C::NS) - 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
         unsigned char* st = smem + C::KV_OFF + s * C::STAGE;
         mbar_arrive_expect_tx(&kv_full[s], 2 * BN * D * 2);
         for (int sub = 0; sub < C::NSUB; ++sub) {
-          tma_load_3d(st + sub * SUB, &map_k, sub * 64, j * BN, kv_row, &kv_full[s], pol_kv);
-          tma_load_3d(st + (C::NSUB + sub) * SUB, &map_v, sub * 64, j * BN, kv_row, &kv_full[s], pol_kv);
+          tma_load_3d(st + sub * SUB, &map_k, sub * 64, walk.j * BN, walk.kv_row, &kv_full[s], pol_kv);
+          tma_load_3d(st + (C::NSUB + sub) * SUB, &map_v, sub * 64, walk.j * BN, walk.kv_row, &kv_full[s], pol_kv);
         }
+        ++it;
       }
       if (*abort_flag) {
         // drain: wait (bounded) for the copies that may still be landing
         volatile int none = 0;
-        mbar_wait_bounded(q_full, 0, &none, nullptr);
-        for (int t = j - C::NS < 0 ? 0 : j - C::NS; t < j; ++t)
+        if (qi >= 1) mbar_wait_bounded(q_full, (qi - 1) & 1, &none, nullptr);
+        for (int t = it - C::NS < 0 ? 0 : it - C::NS; t < it; ++t)
           mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, &none, nullptr);
       }
     }
@@ -164,41 +233,46 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);
       const uint32_t q_addr = sbase + C::Q_OFF, p_addr = sbase + C::P_OFF;
       bool issued = false;
-      auto issue_qk = [&](int j) {
-        const uint32_t k_addr = sbase + C::KV_OFF + (j % C::NS) * C::STAGE;
-        const uint32_t d_tmem = tmem + (j & 1) * BN;
+      int qi_next = 0;  // Q loads consumed so far by the look-ahead walk
+      TileWalk ahead = walk;
+      // S = Q K^T of look-ahead tile t; the last key tile of an item frees Q
+      auto issue_qk = [&](int t) -> bool {
+        if (ahead.first_tile()) {
+          if (!mbar_wait_bounded(q_full, qi_next & 1, abort_flag, p.status)) return false;
+          ++qi_next;
+        }
+        if (!mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = sbase + C::KV_OFF + (t % C::NS) * C::STAGE;
+        const uint32_t d_tmem = tmem + (t & 1) * BN;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks / 4) * SUB + (ks % 4) * 32;
           umma_f16_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024),
                       IDESC_QK, ks > 0);
         }
-        umma_commit(&s_full[j & 1]);
+        umma_commit(&s_full[t & 1]);
+        if (ahead.last_tile()) umma_commit(q_empty);
         issued = true;
+        ahead.advance();
+        return true;
       };
-      bool ok = mbar_wait_bounded(q_full, 0, abort_flag, p.status) &&
-                mbar_wait_bounded(&kv_full[0], 0, abort_flag, p.status);
-      if (ok) {
+      bool ok = issue_qk(0);
+      for (int t = 0; ok && walk.ok; ++t, walk.advance()) {
+        if (ahead.ok && !issue_qk(t + 1)) break;
+        if (!mbar_wait_bounded(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        issue_qk(0);
-      }
-      for (int j = 0; ok && j < nkt; ++j) {
-        if (j + 1 < nkt) {
-          if (!mbar_wait_bounded(&kv_full[(j + 1) % C::NS], ((j + 1) / C::NS) & 1, abort_flag, p.status)) break;
-          tc_fence_after();
-          issue_qk(j + 1);
-        }
-        if (!mbar_wait_bounded(p_full, j & 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t v_addr = sbase + C::KV_OFF + (j % C::NS) * C::STAGE + C::NSUB * SUB;
+        const uint32_t v_addr = sbase + C::KV_OFF + (t % C::NS) * C::STAGE + C::NSUB * SUB;
+        const uint32_t pb = p_addr + (t & 1) * 2 * SUB;
+        const uint32_t acc0 = walk.first_tile() ? 0u : 1u;
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint32_t poff = (ks / 4) * SUB + (ks % 4) * 32;
-          umma_f16_ss(tmem + 2 * BN, smem_desc_sw128(p_addr + poff, 16, 1024),
-                      smem_desc_sw128(v_addr + ks * 2048, SUB, 1024), IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
+          umma_f16_ss(tmem + 2 * BN, smem_desc_sw128(pb + poff, 16, 1024),
+                      smem_desc_sw128(v_addr + ks * 2048, SUB, 1024), IDESC_PV, ks > 0 ? 1u : acc0);
         }
-        umma_commit(o_done);
-        umma_commit(&kv_empty[j % C::NS]);
+        umma_commit(&o_done[t & 1]);
+        umma_commit(&kv_empty[t % C::NS]);
       }
       if (*abort_flag && issued) {
         // let every MMA issued so far finish before TMEM is released
@@ -211,98 +285,110 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     // ------------------------------------------------------------ softmax (warps 0-3)
     const int r = threadIdx.x;  // query row in the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    unsigned char* prow0 = smem + C::P_OFF + r * 128;
-    for (int j = 0; j < nkt; ++j) {
-      // wait outcomes are made warp-uniform: tcgen05.ld/st need the whole warp
-      if (!__all_sync(FULLMASK, mbar_wait_bounded(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.status))) {
-        ok = false;
-        break;
-      }
+    for (int t = 0; walk.ok; ++t, walk.advance()) {
+      const bool first = walk.first_tile(), diag = walk.last_tile();
+      if (!__all_sync(FULLMASK, mbar_wait_bounded(&s_full[t & 1], (t >> 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      float x[BN];
+      float sv[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int q = 0; q < BN / 32; ++q) {
         uint32_t u[32];
-        tmem_ld32(tmem + lane_base + (j & 1) * BN + c * 32, u);
+        tmem_ld32(tmem + lane_base + (t & 1) * BN + q * 32, u);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[i]) * p.scale_log2;
+        for (int i = 0; i < 32; ++i) sv[q * 32 + i] = __uint_as_float(u[i]);
       }
-      if (j == qt) {
+      // Scaled scores are s * c; with c > 0 the row maximum is c * max(s).
+      // Masked entries (keys after the query on the diagonal tile) become NaN-free zeros below.
+      float mx[8];
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c > r) x[c] = -INFINITY;
-      }
-      float mt = x[0];
+      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mt = fmaxf(mt, x[c]);
-      // PV of the previous tile must be done before O is rescaled or P rewritten.
-      if (j > 0 && !__all_sync(FULLMASK, mbar_wait_bounded(o_done, (j - 1) & 1, abort_flag, p.status))) {
-        ok = false;
-        break;
+      for (int i = 0; i < BN; ++i) {
+        const bool keep = !diag || i <= r;
+        const float v = c > 0.f ? sv[i] : -sv[i];
+        mx[i & 7] = keep ? fmaxf(mx[i & 7], v) : mx[i & 7];
       }
-      tc_fence_after();
-      const bool grow = mt > m_ref + 8.f;  // always true for the first tile
+      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mt = c > 0.f ? mraw * c : -mraw * c;  // tile maximum of the scaled scores
+      const bool grow = first || mt > m_ref + 8.f;       // keep the old base unless it grew by 2^8
       float alpha = 1.f;
       if (grow) {
-        alpha = exp2f(m_ref - mt);          // 0 for the first tile
+        alpha = first ? 0.f : ex2(m_ref - mt);
         m_ref = mt;
         l *= alpha;
       }
-      if (j > 0 && __any_sync(FULLMASK, grow)) {
+      // P buffer t&1 was last read by the P.V of tile t-2; an O rescale needs
+      // the P.V of tile t-1 complete.
+      if (t >= 2 && !__all_sync(FULLMASK, mbar_wait_bounded(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag, p.status)))
+        break;
+      const bool rescale = __any_sync(FULLMASK, grow && !first);
+      if (rescale && !__all_sync(FULLMASK, mbar_wait_bounded(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag,
+                                                          p.status)))
+        break;
+      tc_fence_after();
+      if (rescale) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int q = 0; q < D / 32; ++q) {
           uint32_t u[32];
-          tmem_ld32(tmem + lane_base + 2 * BN + c * 32, u);
+          tmem_ld32(tmem + lane_base + 2 * BN + q * 32, u);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(tmem + lane_base + 2 * BN + c * 32, u);
+          tmem_st32(tmem + lane_base + 2 * BN + q * 32, u);
         }
         tmem_wait_st();
       }
-      float lsum = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      unsigned char* prow = smem + C::P_OFF + (t & 1) * 2 * SUB + r * 128;
 #pragma unroll
       for (int ch = 0; ch < BN / 8; ++ch) {  // 16 chunks of 8 keys
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(x[ch * 8 + 2 * e] - m_ref);
-          const float p1 = exp2f(x[ch * 8 + 2 * e + 1] - m_ref);
+          const int i0 = ch * 8 + 2 * e, i1 = i0 + 1;
+          float p0 = ex2(fmaf(sv[i0], c, -m_ref));
+          float p1 = ex2(fmaf(sv[i1], c, -m_ref));
+          if (diag) {
+            p0 = i0 <= r ? p0 : 0.f;
+            p1 = i1 <= r ? p1 : 0.f;
+          }
+          ls[e] += p0 + p1;
           w[e] = pack2(p0, p1);
-          // accumulate the rounded weights: O / l is then a convex combination of V
-          lsum += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xffff0000u);
         }
         const int sub = ch / 8, cc = ch % 8;
-        uint4* dst = reinterpret_cast<uint4*>(prow0 + sub * SUB + ((cc ^ (r & 7)) << 4));
-        *dst = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + sub * SUB + ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      l += lsum;
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    if (ok && __all_sync(FULLMASK, mbar_wait_bounded(o_done, (nkt - 1) & 1, abort_flag, p.status))) {
-      tc_fence_after();
-      const int t = qt * BM + r;
-      const float inv = 1.f / l;
-      uint16_t* dst = p.out + ((static_cast<size_t>(a) * p.T + t) * p.H_q + h) * D;
+      mbar_arrive(&p_full[t & 1]);
+
+      if (diag) {
+        // ---------------------------------------------------- item epilogue
+        if (!__all_sync(FULLMASK, mbar_wait_bounded(&o_done[t & 1], (t >> 1) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        const int tq = walk.qt * BM + r;
+        const float inv = 1.f / l;
+        uint16_t* dst = p.out + ((static_cast<size_t>(walk.a) * p.T + tq) * p.H_q + walk.h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + 2 * BN + c * 32, u);
-        tmem_wait_ld();
-        if (t < p.T) {
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + 2 * BN + q * 32, u);
+          tmem_wait_ld();
+          if (tq < p.T) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 o;
-            o.x = pack2(__uint_as_float(u[q4 * 8 + 0]) * inv, __uint_as_float(u[q4 * 8 + 1]) * inv);
-            o.y = pack2(__uint_as_float(u[q4 * 8 + 2]) * inv, __uint_as_float(u[q4 * 8 + 3]) * inv);
-            o.z = pack2(__uint_as_float(u[q4 * 8 + 4]) * inv, __uint_as_float(u[q4 * 8 + 5]) * inv);
-            o.w = pack2(__uint_as_float(u[q4 * 8 + 6]) * inv, __uint_as_float(u[q4 * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = o;
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 o;
+              o.x = pack2(__uint_as_float(u[q4 * 8 + 0]) * inv, __uint_as_float(u[q4 * 8 + 1]) * inv);
+              o.y = pack2(__uint_as_float(u[q4 * 8 + 2]) * inv, __uint_as_float(u[q4 * 8 + 3]) * inv);
+              o.z = pack2(__uint_as_float(u[q4 * 8 + 4]) * inv, __uint_as_float(u[q4 * 8 + 5]) * inv);
+              o.w = pack2(__uint_as_float(u[q4 * 8 + 6]) * inv, __uint_as_float(u[q4 * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + q * 32 + q4 * 8) = o;
+            }
           }
         }
       }
@@ -361,8 +447,14 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t 
                                      PCfg<D>::SMEM);
   });
   if (errs[dev] != cudaSuccess) return errs[dev];
-  const int nqt = (p.T + BM - 1) / BM;
-  const unsigned grid = static_cast<unsigned>(nqt) * p.A * p.H_q;
+  static int sms[64];
+  static std::once_flag sm_flags[64];
+  std::call_once(sm_flags[dev], [&] {
+    if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms[dev] = 0;
+  });
+  if (sms[dev] <= 0) return cudaErrorInvalidDevice;
+  const long long items = static_cast<long long>((p.T + BM - 1) / BM) * p.A * p.H_q;
+  const unsigned grid = static_cast<unsigned>(items < sms[dev] ? items : sms[dev]);  // one CTA per SM
   prefill_attention_kernel<D><<<grid, THREADS, PCfg<D>::SMEM, stream>>>(p, m.q, m.k, m.v);
   return cudaGetLastError();
 }
