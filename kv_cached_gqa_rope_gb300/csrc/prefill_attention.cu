@@ -286,35 +286,47 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     const int r = threadIdx.x;  // query row in the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const float c = p.scale_log2;
+    const float ce = c > 0.f ? c : 1.f;
     float m_ref = -INFINITY, l = 0.f;
     for (int t = 0; walk.ok; ++t, walk.advance()) {
       const bool first = walk.first_tile(), diag = walk.last_tile();
       if (!__all_sync(FULLMASK, mbar_wait_bounded(&s_full[t & 1], (t >> 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
+      // the four 32-column loads are issued back to back, then waited for once
+      uint32_t u0[32], u1[32], u2[32], u3[32];
+      tmem_ld32(tmem + lane_base + (t & 1) * BN + 0, u0);
+      tmem_ld32(tmem + lane_base + (t & 1) * BN + 32, u1);
+      tmem_ld32(tmem + lane_base + (t & 1) * BN + 64, u2);
+      tmem_ld32(tmem + lane_base + (t & 1) * BN + 96, u3);
+      tmem_wait_ld();
       float sv[BN];
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + (t & 1) * BN + q * 32, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[q * 32 + i] = __uint_as_float(u[i]);
+      for (int i = 0; i < 32; ++i) {
+        sv[i] = __uint_as_float(u0[i]);
+        sv[32 + i] = __uint_as_float(u1[i]);
+        sv[64 + i] = __uint_as_float(u2[i]);
+        sv[96 + i] = __uint_as_float(u3[i]);
       }
-      // Scaled scores are s * c; with c > 0 the row maximum is c * max(s).
-      // Masked entries (keys after the query on the diagonal tile) become NaN-free zeros below.
+      // Scores enter the softmax as s * ce with ce > 0 (a non-positive scale is
+      // folded into the scores first, a path no usual caller takes).  On the
+      // diagonal tile, keys after the query become -inf, so they weigh zero.
+      if (c <= 0.f) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) sv[i] *= c;
+      }
+      if (diag) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) sv[i] = i <= r ? sv[i] : -INFINITY;
+      }
       float mx[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+      for (int k = 0; k < 8; ++k) mx[k] = sv[k];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
-        const bool keep = !diag || i <= r;
-        const float v = c > 0.f ? sv[i] : -sv[i];
-        mx[i & 7] = keep ? fmaxf(mx[i & 7], v) : mx[i & 7];
-      }
+      for (int i = 8; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
       const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float mt = c > 0.f ? mraw * c : -mraw * c;  // tile maximum of the scaled scores
-      const bool grow = first || mt > m_ref + 8.f;       // keep the old base unless it grew by 2^8
+      const float mt = mraw * ce;                    // tile maximum of the scaled scores
+      const bool grow = first || mt > m_ref + 8.f;   // keep the old base unless it grew by 2^8
       float alpha = 1.f;
       if (grow) {
         alpha = first ? 0.f : ex2(m_ref - mt);
@@ -342,27 +354,24 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         }
         tmem_wait_st();
       }
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 ls = make_float2(0.f, 0.f);
+      const float2 c2 = make_float2(ce, ce), nm2 = make_float2(-m_ref, -m_ref);
       unsigned char* prow = smem + C::P_OFF + (t & 1) * 2 * SUB + r * 128;
 #pragma unroll
       for (int ch = 0; ch < BN / 8; ++ch) {  // 16 chunks of 8 keys
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int i0 = ch * 8 + 2 * e, i1 = i0 + 1;
-          float p0 = ex2(fmaf(sv[i0], c, -m_ref));
-          float p1 = ex2(fmaf(sv[i1], c, -m_ref));
-          if (diag) {
-            p0 = i0 <= r ? p0 : 0.f;
-            p1 = i1 <= r ? p1 : 0.f;
-          }
-          ls[e] += p0 + p1;
-          w[e] = pack2(p0, p1);
+          const int i0 = ch * 8 + 2 * e;
+          const float2 x = ffma2(make_float2(sv[i0], sv[i0 + 1]), c2, nm2);
+          const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          ls = fadd2(ls, pr);
+          w[e] = pack2(pr.x, pr.y);
         }
         const int sub = ch / 8, cc = ch % 8;
         *reinterpret_cast<uint4*>(prow + sub * SUB + ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l += ls.x + ls.y;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[t & 1]);
@@ -374,21 +383,19 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         const int tq = walk.qt * BM + r;
         const float inv = 1.f / l;
         uint16_t* dst = p.out + ((static_cast<size_t>(walk.a) * p.T + tq) * p.H_q + walk.h) * D;
+        uint32_t u[D];
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_base + 2 * BN + q * 32, u);
-          tmem_wait_ld();
-          if (tq < p.T) {
+        for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + 2 * BN + q * 32, *reinterpret_cast<uint32_t(*)[32]>(u + q * 32));
+        tmem_wait_ld();
+        if (tq < p.T) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 o;
-              o.x = pack2(__uint_as_float(u[q4 * 8 + 0]) * inv, __uint_as_float(u[q4 * 8 + 1]) * inv);
-              o.y = pack2(__uint_as_float(u[q4 * 8 + 2]) * inv, __uint_as_float(u[q4 * 8 + 3]) * inv);
-              o.z = pack2(__uint_as_float(u[q4 * 8 + 4]) * inv, __uint_as_float(u[q4 * 8 + 5]) * inv);
-              o.w = pack2(__uint_as_float(u[q4 * 8 + 6]) * inv, __uint_as_float(u[q4 * 8 + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + q * 32 + q4 * 8) = o;
-            }
+          for (int q8 = 0; q8 < D / 8; ++q8) {
+            uint4 o;
+            o.x = pack2(__uint_as_float(u[q8 * 8 + 0]) * inv, __uint_as_float(u[q8 * 8 + 1]) * inv);
+            o.y = pack2(__uint_as_float(u[q8 * 8 + 2]) * inv, __uint_as_float(u[q8 * 8 + 3]) * inv);
+            o.z = pack2(__uint_as_float(u[q8 * 8 + 4]) * inv, __uint_as_float(u[q8 * 8 + 5]) * inv);
+            o.w = pack2(__uint_as_float(u[q8 * 8 + 6]) * inv, __uint_as_float(u[q8 * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + q8 * 8) = o;
           }
         }
       }
