@@ -42,21 +42,23 @@ namespace {
 constexpr int BM = 128;        // query rows per tile
 constexpr int BN = 128;        // keys per tile
 constexpr int SUB = 16384;     // one [128 rows x 64 bf16] swizzled sub-tile
-constexpr int THREADS = 192;   // 4 softmax warps + producer + MMA
-constexpr int TMEM_COLS = 512;
+constexpr int THREADS = 224;   // 4 softmax warps + Q/K producer + MMA + V producer
+constexpr int TMEM_COLS = 512; // S x2 (128 cols each), O (128), P x2 (64 each)
+constexpr int P_COL = 3 * BN;  // P buffers: BF16 pairs packed in 32-bit columns
 constexpr unsigned FULLMASK = 0xffffffffu;
 
 template <int D>
 struct PCfg {
   static constexpr int NSUB = D / 64;               // 64-wide sub-tiles per row
-  static constexpr int NS = D == 128 ? 2 : 3;       // K/V stages
+  static constexpr int NK = D == 128 ? 3 : 4;       // K stages
+  static constexpr int NV = NK;                     // V stages
+  static constexpr int TILE = NSUB * SUB;           // one K or V tile
   static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = NSUB * SUB;
-  static constexpr int STAGE = 2 * NSUB * SUB;      // K then V
-  static constexpr int P_OFF = KV_OFF + NS * STAGE; // two P buffers of [128 x 128] BF16
-  static constexpr int BAR_OFF = P_OFF + 2 * 2 * SUB;
-  // q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NBAR = 2 + 2 * NS + 7;
+  static constexpr int K_OFF = TILE;
+  static constexpr int V_OFF = K_OFF + NK * TILE;
+  static constexpr int BAR_OFF = V_OFF + NV * TILE;
+  // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 7;
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 8;
   static constexpr int SMEM = FLAG_OFF + 16 + 1024;  // + alignment slack
@@ -137,9 +139,11 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;
-  uint64_t* kv_empty = kv_full + C::NS;
-  uint64_t* s_full = kv_empty + C::NS;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = k_full + C::NK;
+  uint64_t* v_full = k_empty + C::NK;
+  uint64_t* v_empty = v_full + C::NV;
+  uint64_t* s_full = v_empty + C::NV;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint64_t* drain = o_done + 2;
@@ -162,9 +166,13 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -186,7 +194,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   const uint32_t sbase = smem_u32(smem);
 
   if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       const uint64_t pol_q = l2_evict_first_policy();
       const uint64_t pol_kv = l2_evict_last_policy();  // K/V tiles are re-read by the group's heads
@@ -196,34 +204,47 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         if (r < 0 || r >= p.S) { atomicOr(p.status, KVGQA_FLAG_ROW_RANGE); break; }
       }
       int it = 0, qi = 0;
-      bool ok = true;
-      for (; walk.ok && ok; walk.advance()) {
+      for (; walk.ok; walk.advance()) {
         if (walk.first_tile()) {
-          if (qi >= 1 && !mbar_wait_bounded(q_empty, (qi - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (qi >= 1 && !mbar_wait_bounded(q_empty, (qi - 1) & 1, abort_flag, p.status)) break;
           mbar_arrive_expect_tx(q_full, BM * D * 2);
           for (int sub = 0; sub < C::NSUB; ++sub)
             tma_load_4d(smem + C::Q_OFF + sub * SUB, &map_q, sub * 64, walk.h, walk.qt * BM, walk.a, q_full, pol_q);
           ++qi;
         }
-        const int s = it % C::NS;
-        if (it >= C::NS && !mbar_wait_bounded(&kv_empty[s], ((it / C::NS) - 1) & 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        unsigned char* st = smem + C::KV_OFF + s * C::STAGE;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * BN * D * 2);
-        for (int sub = 0; sub < C::NSUB; ++sub) {
-          tma_load_3d(st + sub * SUB, &map_k, sub * 64, walk.j * BN, walk.kv_row, &kv_full[s], pol_kv);
-          tma_load_3d(st + (C::NSUB + sub) * SUB, &map_v, sub * 64, walk.j * BN, walk.kv_row, &kv_full[s], pol_kv);
-        }
+        const int s = it % C::NK;
+        if (it >= C::NK && !mbar_wait_bounded(&k_empty[s], ((it / C::NK) - 1) & 1, abort_flag, p.status)) break;
+        unsigned char* st = smem + C::K_OFF + s * C::TILE;
+        mbar_arrive_expect_tx(&k_full[s], BN * D * 2);
+        for (int sub = 0; sub < C::NSUB; ++sub)
+          tma_load_3d(st + sub * SUB, &map_k, sub * 64, walk.j * BN, walk.kv_row, &k_full[s], pol_kv);
         ++it;
       }
       if (*abort_flag) {
-        // drain: wait (bounded) for the copies that may still be landing
         volatile int none = 0;
         if (qi >= 1) mbar_wait_bounded(q_full, (qi - 1) & 1, &none, nullptr);
-        for (int t = it - C::NS < 0 ? 0 : it - C::NS; t < it; ++t)
-          mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, &none, nullptr);
+        for (int t = it - C::NK < 0 ? 0 : it - C::NK; t < it; ++t)
+          mbar_wait_bounded(&k_full[t % C::NK], (t / C::NK) & 1, &none, nullptr);
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ V producer
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_evict_last_policy();
+      int it = 0;
+      for (; walk.ok; walk.advance()) {
+        const int s = it % C::NV;
+        if (it >= C::NV && !mbar_wait_bounded(&v_empty[s], ((it / C::NV) - 1) & 1, abort_flag, p.status)) break;
+        unsigned char* st = smem + C::V_OFF + s * C::TILE;
+        mbar_arrive_expect_tx(&v_full[s], BN * D * 2);
+        for (int sub = 0; sub < C::NSUB; ++sub)
+          tma_load_3d(st + sub * SUB, &map_v, sub * 64, walk.j * BN, walk.kv_row, &v_full[s], pol_kv);
+        ++it;
+      }
+      if (*abort_flag) {
+        volatile int none = 0;
+        for (int t = it - C::NV < 0 ? 0 : it - C::NV; t < it; ++t)
+          mbar_wait_bounded(&v_full[t % C::NV], (t / C::NV) & 1, &none, nullptr);
       }
     }
   } else if (warp == 5) {
@@ -231,19 +252,19 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);
-      const uint32_t q_addr = sbase + C::Q_OFF, p_addr = sbase + C::P_OFF;
+      const uint32_t q_addr = sbase + C::Q_OFF;
       bool issued = false;
       int qi_next = 0;  // Q loads consumed so far by the look-ahead walk
       TileWalk ahead = walk;
-      // S = Q K^T of look-ahead tile t; the last key tile of an item frees Q
+      // S = Q K^T of look-ahead tile t; K stage and (after an item's last tile) Q are freed on completion
       auto issue_qk = [&](int t) -> bool {
         if (ahead.first_tile()) {
           if (!mbar_wait_bounded(q_full, qi_next & 1, abort_flag, p.status)) return false;
           ++qi_next;
         }
-        if (!mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait_bounded(&k_full[t % C::NK], (t / C::NK) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t k_addr = sbase + C::KV_OFF + (t % C::NS) * C::STAGE;
+        const uint32_t k_addr = sbase + C::K_OFF + (t % C::NK) * C::TILE;
         const uint32_t d_tmem = tmem + (t & 1) * BN;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -252,6 +273,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
                       IDESC_QK, ks > 0);
         }
         umma_commit(&s_full[t & 1]);
+        umma_commit(&k_empty[t % C::NK]);
         if (ahead.last_tile()) umma_commit(q_empty);
         issued = true;
         ahead.advance();
@@ -261,18 +283,17 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
       for (int t = 0; ok && walk.ok; ++t, walk.advance()) {
         if (ahead.ok && !issue_qk(t + 1)) break;
         if (!mbar_wait_bounded(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.status)) break;
+        if (!mbar_wait_bounded(&v_full[t % C::NV], (t / C::NV) & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t v_addr = sbase + C::KV_OFF + (t % C::NS) * C::STAGE + C::NSUB * SUB;
-        const uint32_t pb = p_addr + (t & 1) * 2 * SUB;
+        const uint32_t v_addr = sbase + C::V_OFF + (t % C::NV) * C::TILE;
+        const uint32_t p_tmem = tmem + P_COL + (t & 1) * (BN / 2);
         const uint32_t acc0 = walk.first_tile() ? 0u : 1u;
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint32_t poff = (ks / 4) * SUB + (ks % 4) * 32;
-          umma_f16_ss(tmem + 2 * BN, smem_desc_sw128(pb + poff, 16, 1024),
-                      smem_desc_sw128(v_addr + ks * 2048, SUB, 1024), IDESC_PV, ks > 0 ? 1u : acc0);
-        }
+        for (int ks = 0; ks < BN / 16; ++ks)
+          umma_f16_ts(tmem + 2 * BN, p_tmem + ks * 8, smem_desc_sw128(v_addr + ks * 2048, SUB, 1024), IDESC_PV,
+                      ks > 0 ? 1u : acc0);
         umma_commit(&o_done[t & 1]);
-        umma_commit(&kv_empty[t % C::NS]);
+        umma_commit(&v_empty[t % C::NV]);
       }
       if (*abort_flag && issued) {
         // let every MMA issued so far finish before TMEM is released
@@ -333,8 +354,8 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         m_ref = mt;
         l *= alpha;
       }
-      // P buffer t&1 was last read by the P.V of tile t-2; an O rescale needs
-      // the P.V of tile t-1 complete.
+      // P buffer t&1 in TMEM was last read by the P.V of tile t-2; an O rescale
+      // needs the P.V of tile t-1 complete.
       if (t >= 2 && !__all_sync(FULLMASK, mbar_wait_bounded(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag, p.status)))
         break;
       const bool rescale = __any_sync(FULLMASK, grow && !first);
@@ -354,25 +375,26 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         }
         tmem_wait_st();
       }
+      // P as BF16 pairs into TMEM buffer t&1 (the A operand of P.V): row r, key
+      // pair j in 32-bit column j.
       float2 ls = make_float2(0.f, 0.f);
       const float2 c2 = make_float2(ce, ce), nm2 = make_float2(-m_ref, -m_ref);
-      unsigned char* prow = smem + C::P_OFF + (t & 1) * 2 * SUB + r * 128;
+      const uint32_t p_tmem = tmem + lane_base + P_COL + (t & 1) * (BN / 2);
 #pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {  // 16 chunks of 8 keys
-        uint32_t w[4];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i0 = ch * 8 + 2 * e;
+        for (int e = 0; e < 32; ++e) {
+          const int i0 = half * 64 + 2 * e;
           const float2 x = ffma2(make_float2(sv[i0], sv[i0 + 1]), c2, nm2);
           const float2 pr = make_float2(ex2(x.x), ex2(x.y));
           ls = fadd2(ls, pr);
           w[e] = pack2(pr.x, pr.y);
         }
-        const int sub = ch / 8, cc = ch % 8;
-        *reinterpret_cast<uint4*>(prow + sub * SUB + ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        tmem_st32(p_tmem + half * 32, w);
       }
+      tmem_wait_st();
       l += ls.x + ls.y;
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[t & 1]);
 
