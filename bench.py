@@ -352,7 +352,7 @@ def run_ours(args, rank, world, local):
                    "kv_bytes_per_step": attn_bytes, "step_bytes": step_bytes,
                    "kv_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm_peak, 4),
                    "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1)},
-        "roofline": {"kernel": "flash_decode_splitk + decode_combine (one cached_gqa_attention_out_ call)",
+        "roofline": {"kernel": "flash_decode_splitk (split-K with the combine run by the last CTA of each cut segment; one cached_gqa_attention_out_ call)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s"},

@@ -268,11 +268,10 @@ kvgqa_status cached_gqa_attention_workspace_size(int64_t A, int64_t H_q, int64_t
     check_heads(H_q, H_kv);
     const int G = (int)(H_q / H_kv);
     if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
-    int ctas = 0;
-    size_t part = 0;
-    check_cuda(kvgqa::decode_launch_shape(device, (int)D, kvgqa::decode_group_pad(G), &ctas, &part),
+    kvgqa::DecodeLayout lay;
+    check_cuda(kvgqa::decode_layout(device, (int)D, kvgqa::decode_group_pad(G), A, H_kv, &lay),
                "decode kernel set-up");
-    *bytes = KVGQA_STATUS_BYTES + part;
+    *bytes = KVGQA_STATUS_BYTES + lay.counter_bytes + lay.partial_bytes;
   });
 }
 
@@ -306,11 +305,10 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
     View vws0 = check_workspace(workspace, KVGQA_STATUS_BYTES);
     check_no_alias({&vo, &vws0}, {&vq, &vkc, &vvc, &vp, &vr, &vo, &vws0});
     const int dev = current_device();
-    int ctas = 0;
-    size_t part = 0;
-    check_cuda(kvgqa::decode_launch_shape(dev, (int)D, kvgqa::decode_group_pad(G), &ctas, &part),
+    kvgqa::DecodeLayout lay;
+    check_cuda(kvgqa::decode_layout(dev, (int)D, kvgqa::decode_group_pad(G), A, H_kv, &lay),
                "decode kernel set-up");
-    View vws = check_workspace(workspace, KVGQA_STATUS_BYTES + part);
+    View vws = check_workspace(workspace, KVGQA_STATUS_BYTES + lay.counter_bytes + lay.partial_bytes);
     check_device({&vq, &vkc, &vvc, &vp, &vr, &vo, &vws}, dev);
     if (A == 0) return;
     kvgqa::DecodeParams p{};
@@ -320,10 +318,12 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
     p.positions = static_cast<const int32_t*>(positions->data);
     p.cache_rows = static_cast<const int32_t*>(cache_rows->data);
     p.out = static_cast<uint16_t*>(out->data);
-    p.status = static_cast<int32_t*>(workspace->data);
-    p.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace->data) + KVGQA_STATUS_BYTES);
+    unsigned char* ws = static_cast<unsigned char*>(workspace->data);
+    p.status = reinterpret_cast<int32_t*>(ws);
+    p.counters = reinterpret_cast<int32_t*>(ws + KVGQA_STATUS_BYTES);
+    p.partials = reinterpret_cast<float*>(ws + KVGQA_STATUS_BYTES + lay.counter_bytes);
     p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
-    p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = ctas;
+    p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
     p.scale_log2 = scale * 1.4426950408889634f;
     check_cuda(kvgqa::launch_cached_gqa_attention(p, static_cast<cudaStream_t>(stream)),
                "cached_gqa_attention launch");
@@ -361,13 +361,13 @@ kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
     check_no_alias({&vo}, {&vq, &vkc, &vvc, &vp, &vr, &vo});
     const int dev = current_device();
     check_device({&vq, &vkc, &vvc, &vp, &vr, &vo}, dev);
-    int ctas = 0;
-    size_t part = 0;
-    check_cuda(kvgqa::decode_launch_shape(dev, (int)D, kvgqa::decode_group_pad(G), &ctas, &part),
+    kvgqa::DecodeLayout lay;
+    check_cuda(kvgqa::decode_layout(dev, (int)D, kvgqa::decode_group_pad(G), A, H_kv, &lay),
                "decode kernel set-up");
-    if (KVGQA_STATUS_BYTES + part > kvgqa::kStaticScratchBytes)
+    const size_t need = KVGQA_STATUS_BYTES + lay.counter_bytes + lay.partial_bytes;
+    if (need > kvgqa::kStaticScratchBytes)
       fail(KVGQA_EUNSUPPORTED, "needs %zu bytes of scratch; the library's static scratch holds %zu",
-           KVGQA_STATUS_BYTES + part, kvgqa::kStaticScratchBytes);
+           need, kvgqa::kStaticScratchBytes);
     void* scratch = nullptr;
     check_cuda(kvgqa::static_scratch_address(dev, &scratch), "static scratch address");
     if (A == 0) return;
@@ -378,10 +378,12 @@ kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
     p.positions = static_cast<const int32_t*>(positions->data);
     p.cache_rows = static_cast<const int32_t*>(cache_rows->data);
     p.out = static_cast<uint16_t*>(out->data);
-    p.status = static_cast<int32_t*>(scratch);
-    p.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + KVGQA_STATUS_BYTES);
+    unsigned char* sc = static_cast<unsigned char*>(scratch);
+    p.status = reinterpret_cast<int32_t*>(sc);
+    p.counters = reinterpret_cast<int32_t*>(sc + KVGQA_STATUS_BYTES);
+    p.partials = reinterpret_cast<float*>(sc + KVGQA_STATUS_BYTES + lay.counter_bytes);
     p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
-    p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = ctas;
+    p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
     p.scale_log2 = scale * 1.4426950408889634f;
     check_cuda(kvgqa::launch_cached_gqa_attention(p, static_cast<cudaStream_t>(stream)),
                "cached_gqa_attention launch");

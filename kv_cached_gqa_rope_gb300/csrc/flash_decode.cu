@@ -1,5 +1,6 @@
 // K2: split-K flash-decode over the shared slot KV cache on tcgen05 tensor
-// cores, and K3: the combine.
+// cores, with K3, the combine of split segments, run by the CTA that finishes
+// a segment last.
 //
 // microLLM-rocm ARCHITECTURE.md, section "Tensor ownership boundary": each
 // survivor token attends to its own row's cached prefix, with device
@@ -17,8 +18,11 @@
 // of the persistent grid (one CTA per SM) takes the virtual range
 // [b*W, (b+1)*W), W = ceil(V_tot / grid), and processes the real keys in it.
 // A segment whose real keys lie inside one CTA is finished there (BF16 out
-// written); a segment cut by a CTA boundary leaves FP32 partials (m, l, o)
-// that K3 merges: the CTA where it starts writes slot 1, each later CTA slot 0.
+// written); a segment cut by a CTA boundary leaves FP32 partials (m, l, o):
+// the CTA where it starts writes slot 1, each later CTA slot 0.  The combine
+// (K3) runs in whichever of those CTAs finishes last: each counts its partial
+// in a per-segment counter, and the one that completes the count merges the
+// segment's partials, writes the BF16 output and resets the counter to zero.
 //
 // Inside a CTA, per tile of up to 128 keys of one segment:
 //   warp 4     TMA producer: K and V tiles (128B swizzle, 32-row boxes, so a
@@ -213,6 +217,30 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return *reinterpret_cast<const uint16_t*>(&b);
 }
 
+// K3, the combine: merge the partials of CTAs b0..b1 for segment (a, g) and
+// write the BF16 output of its G query heads.  One thread per d (d < D) of
+// the 128 softmax threads.  Partials of other CTAs are read past L1.
+template <int D, int GP>
+__device__ void combine_segment(const DecodeParams& p, int a, int g, int b0, int b1, int d) {
+  if (d >= D) return;
+  constexpr size_t SLOT = slot_floats(GP, D);
+  for (int h = 0; h < p.G; ++h) {
+    float M = -INFINITY;
+    for (int b = b0; b <= b1; ++b) {
+      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? 1 : 0)) * SLOT;
+      M = fmaxf(M, __ldcg(sp + GP * D + h));
+    }
+    float lsum = 0.f, acc = 0.f;
+    for (int b = b0; b <= b1; ++b) {
+      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? 1 : 0)) * SLOT;
+      const float sc = exp2f(__ldcg(sp + GP * D + h) - M);
+      lsum += __ldcg(sp + slot_l_offset(GP, D) + h) * sc;
+      acc += __ldcg(sp + h * D + d) * sc;
+    }
+    p.out[(static_cast<size_t>(a) * p.H_q + g * p.G + h) * D + d] = bf16_bits(acc / lsum);
+  }
+}
+
 template <int D, int GP>
 __global__ void __launch_bounds__(THREADS, 1)
 flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap map_k,
@@ -232,6 +260,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
+  volatile int* merge_flag = abort_flag + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -249,7 +278,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     fence_mbar_init();
   }
   pdl_wait();     // everything below may read what the previous kernel wrote
-  pdl_trigger();  // let the combine kernel launch and run its own set-up
+  pdl_trigger();  // the next kernel in the stream may launch and set itself up
   build_prefix(p, prefix, nkeys, blockIdx.x == 0);  // ends with __syncthreads
 
   const int v_tot = prefix[p.A];
@@ -475,6 +504,21 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             }
           }
         }
+        if (!cur.whole()) {
+          // Count this CTA's partial; the CTA that completes the count merges.
+          const int b0 = cur.vlo / W, b1 = (cur.vlo + cur.n - 1) / W;
+          int* cnt = p.counters + cur.a * p.H_kv + cur.g;
+          __threadfence();  // this CTA's partial is visible before it is counted
+          named_bar_sync(1, BN);
+          if (r == 0) *merge_flag = atomicAdd(cnt, 1) == b1 - b0;
+          named_bar_sync(1, BN);
+          if (*merge_flag) {
+            __threadfence();
+            combine_segment<D, GP>(p, cur.a, cur.g, b0, b1, r);
+            if (r == 0) *cnt = 0;  // ready for the next call
+          }
+          named_bar_sync(1, BN);  // merge_flag is reused at the next segment end
+        }
       }
     }
   }
@@ -484,57 +528,6 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   __syncthreads();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
-}
-
-// K3: for every segment cut by a CTA boundary, merge the partials of the CTAs
-// b0..b1 that cover it and write the BF16 output of its G query heads.
-template <int D, int GP>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
-  __shared__ int prefix[kMaxActiveRows + 1];
-  __shared__ int nkeys[kMaxActiveRows];
-  // The split-K kernel passed its own wait before letting this grid start, so
-  // positions and cache rows are final; the partials are not until pdl_wait().
-  build_prefix(p, prefix, nkeys, false);
-  const int a = blockIdx.x / p.H_kv, g = blockIdx.x - a * p.H_kv;
-  const int vlen = (prefix[a + 1] - prefix[a]) / p.H_kv;
-  pdl_wait();
-  if (vlen == 0) return;
-  const int n = nkeys[a];
-  const int W = keys_per_cta(prefix[p.A], p.num_ctas);
-  const int vlo = prefix[a] + g * vlen;
-  const int b0 = vlo / W, b1 = (vlo + n - 1) / W;
-  if (b0 == b1) return;  // finished by the split-K kernel
-  const int slot0 = 1;   // the CTA where the segment starts wrote slot 1
-  constexpr size_t SLOT = slot_floats(GP, D);
-  for (int item = threadIdx.x; item < p.G * (D / 8); item += blockDim.x) {
-    const int h = item / (D / 8), c8 = item - h * (D / 8);
-    float M = -INFINITY;
-    for (int b = b0; b <= b1; ++b) {
-      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? slot0 : 0)) * SLOT;
-      M = fmaxf(M, sp[GP * D + h]);
-    }
-    float lsum = 0.f, acc[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    for (int b = b0; b <= b1; ++b) {
-      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? slot0 : 0)) * SLOT;
-      const float sc = exp2f(sp[GP * D + h] - M);
-      lsum += sp[slot_l_offset(GP, D) + h] * sc;
-      const float4 u0 = *reinterpret_cast<const float4*>(sp + h * D + c8 * 8);
-      const float4 u1 = *reinterpret_cast<const float4*>(sp + h * D + c8 * 8 + 4);
-      acc[0] += u0.x * sc; acc[1] += u0.y * sc; acc[2] += u0.z * sc; acc[3] += u0.w * sc;
-      acc[4] += u1.x * sc; acc[5] += u1.y * sc; acc[6] += u1.z * sc; acc[7] += u1.w * sc;
-    }
-    const float inv = 1.f / lsum;
-    uint4 pk;
-    __nv_bfloat162 q0 = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-    __nv_bfloat162 q1 = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-    __nv_bfloat162 q2 = __floats2bfloat162_rn(acc[4] * inv, acc[5] * inv);
-    __nv_bfloat162 q3 = __floats2bfloat162_rn(acc[6] * inv, acc[7] * inv);
-    pk.x = *reinterpret_cast<uint32_t*>(&q0); pk.y = *reinterpret_cast<uint32_t*>(&q1);
-    pk.z = *reinterpret_cast<uint32_t*>(&q2); pk.w = *reinterpret_cast<uint32_t*>(&q3);
-    *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(a) * p.H_q + g * p.G + h) * D + c8 * 8) = pk;
-  }
 }
 
 cudaError_t make_decode_maps(const DecodeParams& p, DecodeMaps* m) {
@@ -593,12 +586,7 @@ struct Kernels {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP>, p, m.kc, m.vc, m.q);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(p.A * p.H_kv);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, GP>, p);
+    return cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP>, p, m.kc, m.vc, m.q);
   }
 };
 
@@ -632,12 +620,13 @@ int decode_group_pad(int G) {
   return gp;
 }
 
-cudaError_t decode_launch_shape(int device, int D, int GP, int* num_ctas, size_t* partial_bytes) {
+cudaError_t decode_layout(int device, int D, int GP, int64_t A, int64_t H_kv, DecodeLayout* out) {
   int n = 0;
   const cudaError_t e = dispatch(D, GP, [&](auto k) { return decltype(k)::prepare(device, &n); });
   if (e != cudaSuccess) return e;
-  *num_ctas = n;
-  *partial_bytes = static_cast<size_t>(n) * 2 * slot_floats(GP, D) * sizeof(float);
+  out->num_ctas = n;
+  out->counter_bytes = (static_cast<size_t>(A) * H_kv * sizeof(int32_t) + 255) / 256 * 256;
+  out->partial_bytes = static_cast<size_t>(n) * 2 * slot_floats(GP, D) * sizeof(float);
   return cudaSuccess;
 }
 

@@ -41,6 +41,7 @@ struct DecodeParams {
   const int32_t* cache_rows;  // [A]
   uint16_t* out;              // [A,H_q,D]
   float* partials;            // split-K partial results (workspace)
+  int32_t* counters;          // per (row, KV head): partials written so far (zero between calls)
   int32_t* status;
   int A, H_q, H_kv, G, D, S, max_seq;
   int num_ctas;               // grid size of the split-K kernel
@@ -49,8 +50,14 @@ struct DecodeParams {
 
 // Padded group size used by the decode kernels: the next power of two >= G.
 int decode_group_pad(int G);
-// Grid size of the split-K kernel on `device`, and the partial-buffer bytes.
-cudaError_t decode_launch_shape(int device, int D, int GP, int* num_ctas, size_t* partial_bytes);
+// Workspace of the decode attention behind the status block: per-segment
+// counters (A * H_kv ints, rounded up to 256 bytes), then the split-K
+// partials of the grid the kernel uses on `device`.
+struct DecodeLayout {
+  int num_ctas;
+  size_t counter_bytes, partial_bytes;
+};
+cudaError_t decode_layout(int device, int D, int GP, int64_t A, int64_t H_kv, DecodeLayout* out);
 cudaError_t launch_cached_gqa_attention(const DecodeParams& p, cudaStream_t stream);
 
 // Size of the library's own device scratch array (status block + partials)
