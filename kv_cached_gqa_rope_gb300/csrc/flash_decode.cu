@@ -225,17 +225,18 @@ __device__ void combine_segment(const DecodeParams& p, int a, int g, int b0, int
   if (d >= D) return;
   constexpr size_t SLOT = slot_floats(GP, D);
   for (int h = 0; h < p.G; ++h) {
-    float M = -INFINITY;
+    // one pass over the partials, rescaling the running sums as the maximum grows
+    float M = -INFINITY, lsum = 0.f, acc = 0.f;
     for (int b = b0; b <= b1; ++b) {
       const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? 1 : 0)) * SLOT;
-      M = fmaxf(M, __ldcg(sp + GP * D + h));
-    }
-    float lsum = 0.f, acc = 0.f;
-    for (int b = b0; b <= b1; ++b) {
-      const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? 1 : 0)) * SLOT;
-      const float sc = exp2f(__ldcg(sp + GP * D + h) - M);
-      lsum += __ldcg(sp + slot_l_offset(GP, D) + h) * sc;
-      acc += __ldcg(sp + h * D + d) * sc;
+      const float m = __ldcg(sp + GP * D + h);
+      const float lb = __ldcg(sp + slot_l_offset(GP, D) + h);
+      const float ob = __ldcg(sp + h * D + d);
+      const float mn = fmaxf(M, m);
+      const float s_old = exp2f(M - mn), s_new = exp2f(m - mn);
+      lsum = lsum * s_old + lb * s_new;
+      acc = acc * s_old + ob * s_new;
+      M = mn;
     }
     p.out[(static_cast<size_t>(a) * p.H_q + g * p.G + h) * D + d] = bf16_bits(acc / lsum);
   }
@@ -508,12 +509,18 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
           // Count this CTA's partial; the CTA that completes the count merges.
           const int b0 = cur.vlo / W, b1 = (cur.vlo + cur.n - 1) / W;
           int* cnt = p.counters + cur.a * p.H_kv + cur.g;
-          __threadfence();  // this CTA's partial is visible before it is counted
+          // release: the barrier orders every thread's partial stores before
+          // thread 0's fence and count; acquire: the merging CTA fences after
+          // seeing the count complete, then the barrier hands that on.
           named_bar_sync(1, BN);
-          if (r == 0) *merge_flag = atomicAdd(cnt, 1) == b1 - b0;
+          if (r == 0) {
+            __threadfence();
+            const bool last_one = atomicAdd(cnt, 1) == b1 - b0;
+            if (last_one) __threadfence();
+            *merge_flag = last_one;
+          }
           named_bar_sync(1, BN);
           if (*merge_flag) {
-            __threadfence();
             combine_segment<D, GP>(p, cur.a, cur.g, b0, b1, r);
             if (r == 0) *cnt = 0;  // ready for the next call
           }
