@@ -271,7 +271,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], BN);
+      mbar_init(&p_full[b], 1);
       mbar_init(&o_done[b], 1);
     }
     mbar_init(drain, 1);
@@ -469,13 +469,16 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
 #pragma unroll
           for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + sb * SUB + c * 16) = make_uint4(0, 0, 0, 0);
       }
+      // Every thread's P^T stores and TMEM reads are done and fenced before the
+      // group synchronises; then one thread arrives (a single arrival instead
+      // of 128 serialised ones on the same barrier).
       fence_proxy_async_smem();
+      tc_fence_before();
       named_bar_sync(1, BN);
+      if (r == 0) mbar_arrive(&p_full[it & 1]);
 #pragma unroll
       for (int h = 0; h < GP; ++h)
         l[h] += (red_sum[h] + red_sum[NQ + h]) + (red_sum[2 * NQ + h] + red_sum[3 * NQ + h]);
-      tc_fence_before();
-      mbar_arrive(&p_full[it & 1]);
 
       if (cur.last()) {
         // ---------------------------------------------------- segment end

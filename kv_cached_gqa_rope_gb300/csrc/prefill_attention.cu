@@ -9,22 +9,27 @@
 // The rotated K and V have already been stored into the target cache rows
 // (K1), so this kernel reads them straight from the cache.
 //
-// A persistent grid (one CTA per SM) walks (128-query tile, prompt a, query
-// head h) items, longest first, dealt round-robin; per item:
-//   warp 4      TMA producer: the Q tile once, then 128-key K and V tiles of
-//               the row's cached prefix into a 2-stage ring (128B swizzle);
-//   warp 5      one thread issues tcgen05.mma: S = Q K^T into one of two TMEM
-//               buffers (the next tile's S overlaps this tile's softmax), and
-//               O += P V into a TMEM accumulator;
-//   warps 0-3   softmax, one thread per query row: S row from TMEM, scale,
-//               causal mask on the diagonal tile, FP32 online softmax, P as
-//               BF16 into shared memory (the A operand of P V), O rescaled in
-//               TMEM only when the row maximum grew by more than 2^8 (the
-//               exponent base is otherwise kept, which leaves O / l exact);
-//               at the end O / l is rounded to BF16 and stored token-major.
-// Key tiles past the diagonal are never visited.  Tensor maps bound the key
-// and query ranges by T, so tile rows past the prompt read as zeros.
-// Tiles are scheduled longest first (the last query tiles have the most keys).
+// A persistent grid (one CTA per SM) walks items (128-query tile qt, prompt a,
+// pair of query heads of one KV group), longest first, dealt round-robin.
+// Both heads of a pair read the same K/V tiles, so each tile staged in shared
+// memory feeds four MMAs.  Per item:
+//   warp 8      TMA: the two Q tiles, then 128-key K tiles (3-stage ring);
+//   warp 9      TMA: the matching V tiles (2-stage ring);
+//   warp 10     one thread issues tcgen05.mma: S_x = Q_x K^T into TMEM and
+//               O_x += P_x V with P_x read from TMEM (x = A, B);
+//   warps 0-3   softmax of head A, warps 4-7 softmax of head B, one thread
+//               per query row: S row from TMEM, scale and diagonal causal mask,
+//               FP32 online softmax, P as BF16 pairs written back over the S
+//               columns, O rescaled in TMEM only when the row maximum grew by
+//               more than 2^8 (otherwise the old base is kept; O / l stays
+//               exact); at the item end O / l is rounded to BF16 and stored.
+// The two softmax groups alternate with the tensor core: while one works on
+// its head's scores, the MMAs of the other head run.  MMAs issued by one
+// thread complete in order and a commit covers every earlier MMA, so S_x of
+// tile t being ready means P_x of tile t-1 has been consumed.
+// Key tiles past the diagonal are never visited; tensor maps bound the key and
+// query ranges by T so rows past the prompt read as zeros.  With an odd group
+// size, items hold one head (the B group idles).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,23 +47,32 @@ namespace {
 constexpr int BM = 128;        // query rows per tile
 constexpr int BN = 128;        // keys per tile
 constexpr int SUB = 16384;     // one [128 rows x 64 bf16] swizzled sub-tile
-constexpr int THREADS = 224;   // 4 softmax warps + Q/K producer + MMA + V producer
-constexpr int TMEM_COLS = 512; // S x2 (128 cols each), O (128), P x2 (64 each)
-constexpr int P_COL = 3 * BN;  // P buffers: BF16 pairs packed in 32-bit columns
+constexpr int NWARPS = 12;     // 2 x 4 softmax + Q/K producer + V producer + MMA + spare
+constexpr int THREADS = NWARPS * 32;
+constexpr int W_QK = 8, W_V = 9, W_MMA = 10;
+// Register split (setmaxnreg): the launch gives every thread kLaunchRegs; the
+// third warpgroup (producers, MMA issuer) drops to kRoleRegs so the two
+// softmax warpgroups can rise to kSoftmaxRegs and hold a whole score row.
+// The sum stays within the launch's registers (checked on the host against
+// the compiled kernel before every launch).
+constexpr int kLaunchRegs = 168, kRoleRegs = 72, kSoftmaxRegs = 216;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kRoleRegs <= THREADS * kLaunchRegs, "register split");
+constexpr int TMEM_COLS = 512; // S_A, S_B, O_A, O_B: 128 columns each
 constexpr unsigned FULLMASK = 0xffffffffu;
 
 template <int D>
 struct PCfg {
   static constexpr int NSUB = D / 64;               // 64-wide sub-tiles per row
+  static constexpr int TILE = NSUB * SUB;           // one Q, K or V tile
   static constexpr int NK = D == 128 ? 3 : 4;       // K stages
-  static constexpr int NV = NK;                     // V stages
-  static constexpr int TILE = NSUB * SUB;           // one K or V tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = TILE;
+  static constexpr int NV = D == 128 ? 2 : 4;       // V stages
+  static constexpr int Q_OFF = 0;                   // Q_A, Q_B
+  static constexpr int K_OFF = 2 * TILE;
   static constexpr int V_OFF = K_OFF + NK * TILE;
   static constexpr int BAR_OFF = V_OFF + NV * TILE;
-  // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 7;
+  // q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
+  // s_full[2], p_full[2], o_done[2], turn[2], drain (index [2] = head A / B)
+  static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 9;
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 8;
   static constexpr int SMEM = FLAG_OFF + 16 + 1024;  // + alignment slack
@@ -76,6 +90,30 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
+// One lane of a converged warp (the same one every lane agrees on).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Maximum of three values (one instruction on sm_100 and later; NaN inputs
+// are ignored like fmaxf does).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 2^x on the special-function unit (flushes results below 2^-126 to zero,
 // which no BF16 probability needs).
 __device__ __forceinline__ float ex2(float x) {
@@ -84,25 +122,28 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// The work of the persistent grid: items (query tile qt, prompt a, head h),
-// longest first (tile qt visits qt + 1 key tiles), dealt round-robin to the
-// CTAs; every role of a CTA walks the same sequence, tile by tile.
+// The work of the persistent grid: items (query tile qt, prompt a, head pair),
+// longest first (tile qt visits qt + 1 key tiles), dealt round-robin; every
+// role of a CTA walks the same sequence, key tile by key tile.
 struct TileWalk {
-  int i, stride, n_items, nqt, heads, H_q, H_kv, G, S;
+  int i, stride, n_items, nqt, units, per_tok, H_q, H_kv, G, S;
+  bool pairs;                 // two heads of one KV group per item (G even)
   const int32_t* rows;
-  int qt, a, h, kv_row;  // current item
-  int j;                 // key tile within the item
-  bool ok;               // false past the last item
+  int qt, a, hA, hB, kv_row;  // current item (hB < 0: single head)
+  int j;                      // key tile within the item
+  bool ok;                    // false past the last item
 
   __device__ bool load_item() {
     while (i < n_items) {
-      qt = nqt - 1 - i / heads;
-      const int rem = i % heads;
-      a = rem / H_q;
-      h = rem % H_q;
+      qt = nqt - 1 - i / units;
+      const int rem = i % units;
+      a = rem / per_tok;
+      const int k = rem % per_tok;
+      hA = pairs ? 2 * k : k;
+      hB = pairs ? 2 * k + 1 : -1;
       const int r = rows[a];
       if (r >= 0 && r < S) {
-        kv_row = r * H_kv + h / G;
+        kv_row = r * H_kv + hA / G;
         j = 0;
         return true;
       }
@@ -111,9 +152,11 @@ struct TileWalk {
     return false;
   }
   __device__ void init(const PrefillParams& p, int first, int step) {
+    pairs = (p.G % 2) == 0;
+    per_tok = pairs ? p.H_q / 2 : p.H_q;
     nqt = (p.T + BM - 1) / BM;
-    heads = p.A * p.H_q;
-    n_items = nqt * heads;
+    units = p.A * per_tok;
+    n_items = nqt * units;
     H_q = p.H_q; H_kv = p.H_kv; G = p.G; S = p.S; rows = p.cache_rows;
     i = first;
     stride = step;
@@ -137,16 +180,17 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
+  uint64_t* q_full = bars;       // [head]
+  uint64_t* q_empty = bars + 2;  // [head]
+  uint64_t* k_full = bars + 4;
   uint64_t* k_empty = k_full + C::NK;
   uint64_t* v_full = k_empty + C::NK;
   uint64_t* v_empty = v_full + C::NV;
-  uint64_t* s_full = v_empty + C::NV;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* drain = o_done + 2;
+  uint64_t* s_full = v_empty + C::NV;  // [head]
+  uint64_t* p_full = s_full + 2;       // [head]
+  uint64_t* o_done = p_full + 2;       // [head]
+  uint64_t* turn = o_done + 2;         // [head]: that head's softmax group finished a tile
+  uint64_t* drain = turn + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -156,7 +200,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   if (!walk.ok) {  // uniform: this CTA has no valid item
     if (threadIdx.x == 0) {
       for (int i = blockIdx.x; i < walk.n_items; i += gridDim.x) {
-        const int r = p.cache_rows[(i % walk.heads) / p.H_q];
+        const int r = p.cache_rows[(i % walk.units) / walk.per_tok];
         if (r < 0 || r >= p.S) { atomicOr(p.status, KVGQA_FLAG_ROW_RANGE); break; }
       }
     }
@@ -164,8 +208,6 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   }
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -174,16 +216,19 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], BM);
-      mbar_init(&o_done[b], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&q_full[x], 1);
+      mbar_init(&q_empty[x], 1);
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 4);  // one arrival per softmax warp
+      mbar_init(&o_done[x], 1);
+      mbar_init(&turn[x], 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
@@ -193,25 +238,31 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(smem);
 
-  if (warp == 4) {
+  if (warp >= 8) {
+  regs_dec<kRoleRegs>();
+  if (warp == W_QK) {
     // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       const uint64_t pol_q = l2_evict_first_policy();
       const uint64_t pol_kv = l2_evict_last_policy();  // K/V tiles are re-read by the group's heads
-      // prompts whose cache row is invalid are skipped by every role; flag them here
       for (int i = blockIdx.x; i < walk.n_items; i += gridDim.x) {
-        const int r = p.cache_rows[(i % walk.heads) / p.H_q];
+        const int r = p.cache_rows[(i % walk.units) / walk.per_tok];
         if (r < 0 || r >= p.S) { atomicOr(p.status, KVGQA_FLAG_ROW_RANGE); break; }
       }
-      int it = 0, qi = 0;
+      // Per item: Q_A, the first K tile, Q_B (the order the MMAs need them).
+      int it = 0, qa = 0, qb = 0;  // K tiles and Q tiles (per head) loaded so far
+      auto load_q = [&](int x, int& qn) -> bool {
+        if (qn >= 1 && !mbar_wait_bounded(&q_empty[x], (qn - 1) & 1, abort_flag, p.status)) return false;
+        mbar_arrive_expect_tx(&q_full[x], BM * D * 2);
+        for (int sub = 0; sub < C::NSUB; ++sub)
+          tma_load_4d(smem + C::Q_OFF + x * C::TILE + sub * SUB, &map_q, sub * 64, x ? walk.hB : walk.hA,
+                      walk.qt * BM, walk.a, &q_full[x], pol_q);
+        ++qn;
+        return true;
+      };
       for (; walk.ok; walk.advance()) {
-        if (walk.first_tile()) {
-          if (qi >= 1 && !mbar_wait_bounded(q_empty, (qi - 1) & 1, abort_flag, p.status)) break;
-          mbar_arrive_expect_tx(q_full, BM * D * 2);
-          for (int sub = 0; sub < C::NSUB; ++sub)
-            tma_load_4d(smem + C::Q_OFF + sub * SUB, &map_q, sub * 64, walk.h, walk.qt * BM, walk.a, q_full, pol_q);
-          ++qi;
-        }
+        const bool fresh = walk.first_tile();
+        if (fresh && !load_q(0, qa)) break;
         const int s = it % C::NK;
         if (it >= C::NK && !mbar_wait_bounded(&k_empty[s], ((it / C::NK) - 1) & 1, abort_flag, p.status)) break;
         unsigned char* st = smem + C::K_OFF + s * C::TILE;
@@ -219,15 +270,17 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         for (int sub = 0; sub < C::NSUB; ++sub)
           tma_load_3d(st + sub * SUB, &map_k, sub * 64, walk.j * BN, walk.kv_row, &k_full[s], pol_kv);
         ++it;
+        if (fresh && walk.hB >= 0 && !load_q(1, qb)) break;
       }
       if (*abort_flag) {
         volatile int none = 0;
-        if (qi >= 1) mbar_wait_bounded(q_full, (qi - 1) & 1, &none, nullptr);
+        if (qa >= 1) mbar_wait_bounded(&q_full[0], (qa - 1) & 1, &none, nullptr);
+        if (qb >= 1) mbar_wait_bounded(&q_full[1], (qb - 1) & 1, &none, nullptr);
         for (int t = it - C::NK < 0 ? 0 : it - C::NK; t < it; ++t)
           mbar_wait_bounded(&k_full[t % C::NK], (t / C::NK) & 1, &none, nullptr);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == W_V) {
     // ------------------------------------------------------------ V producer
     if (lane == 0) {
       const uint64_t pol_kv = l2_evict_last_policy();
@@ -247,90 +300,118 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
           mbar_wait_bounded(&v_full[t % C::NV], (t / C::NV) & 1, &none, nullptr);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (uniform control flow); one elected
+    // lane issues each group of MMAs and its commits.
+    {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);
-      const uint32_t q_addr = sbase + C::Q_OFF;
+      const bool pairs = walk.pairs;
+      const int nh = pairs ? 2 : 1;
       bool issued = false;
-      int qi_next = 0;  // Q loads consumed so far by the look-ahead walk
-      TileWalk ahead = walk;
-      // S = Q K^T of look-ahead tile t; K stage and (after an item's last tile) Q are freed on completion
-      auto issue_qk = [&](int t) -> bool {
-        if (ahead.first_tile()) {
-          if (!mbar_wait_bounded(q_full, qi_next & 1, abort_flag, p.status)) return false;
-          ++qi_next;
-        }
-        if (!mbar_wait_bounded(&k_full[t % C::NK], (t / C::NK) & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint32_t k_addr = sbase + C::K_OFF + (t % C::NK) * C::TILE;
-        const uint32_t d_tmem = tmem + (t & 1) * BN;
+      int qn = 0;             // items whose Q tiles have been consumed
+      TileWalk ahead = walk;  // the tile whose S is issued next
+      bool ok = true;
+      bool first_next = true; // first-tile flag of the newest tile whose S was issued
+      // Returns whether every lane's wait succeeded (a timeout anywhere stops the warp).
+#define KVGQA_WAIT(bar, parity) (ok = ok && __all_sync(FULLMASK, mbar_wait_bounded((bar), (parity), abort_flag, p.status)))
+      for (int t = -1; ok; ++t) {
+        // ---- P.V of tile t (t >= 0) interleaved with S of tile t + 1, head by head.
+        // The K tile of tile t + 1 is waited for before the first P.V so that no
+        // wait separates the groups (the tensor pipe's queue is short; a stalled
+        // issuer leaves it idle).
+        const bool first = first_next, more = ahead.ok;
+        const int sv = t % C::NV, kn = (t + 1) % C::NK;
+        if (t >= 0) KVGQA_WAIT(&v_full[sv], (t / C::NV) & 1);
+        if (more) KVGQA_WAIT(&k_full[kn], ((t + 1) / C::NK) & 1);
+        const uint32_t v_addr = sbase + C::V_OFF + sv * C::TILE;
+        const uint32_t k_addr = sbase + C::K_OFF + kn * C::TILE;
+        const bool a_first = ahead.first_tile(), a_last = ahead.last_tile();
+        for (int x = 0; x < nh && ok; ++x) {
+          if (t >= 0) {
+            // O_x += P_x V, P_x read from TMEM over S_x's first half
+            KVGQA_WAIT(&p_full[x], t & 1);
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks / 4) * SUB + (ks % 4) * 32;
-          umma_f16_ss(d_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024),
-                      IDESC_QK, ks > 0);
+              for (int ks = 0; ks < BN / 16; ++ks)
+                umma_f16_ts(tmem + (2 + x) * BN, tmem + x * BN + ks * 8, smem_desc_sw128(v_addr + ks * 2048, SUB, 1024),
+                            IDESC_PV, (ks > 0 || !first) ? 1u : 0u);
+              umma_commit(&o_done[x]);
+              if (x == nh - 1) umma_commit(&v_empty[sv]);
+            }
+            __syncwarp();
+          }
+          if (more) {
+            // S_x = Q_x K^T of tile t + 1; the last head frees the K stage, and
+            // after an item's last tile Q_x is freed, once the MMAs complete
+            if (a_first) KVGQA_WAIT(&q_full[x], qn & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t q_addr = sbase + C::Q_OFF + x * C::TILE;
+            if (elect_one()) {
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t off = (ks / 4) * SUB + (ks % 4) * 32;
+                umma_f16_ss(tmem + x * BN, smem_desc_sw128(q_addr + off, 16, 1024),
+                            smem_desc_sw128(k_addr + off, 16, 1024), IDESC_QK, ks > 0);
+              }
+              umma_commit(&s_full[x]);
+              if (a_last) umma_commit(&q_empty[x]);
+              if (x == nh - 1) umma_commit(&k_empty[kn]);
+            }
+            __syncwarp();
+            issued = true;
+          }
         }
-        umma_commit(&s_full[t & 1]);
-        umma_commit(&k_empty[t % C::NK]);
-        if (ahead.last_tile()) umma_commit(q_empty);
-        issued = true;
+        if (!more) break;
+        first_next = a_first;
+        if (a_first) ++qn;
         ahead.advance();
-        return true;
-      };
-      bool ok = issue_qk(0);
-      for (int t = 0; ok && walk.ok; ++t, walk.advance()) {
-        if (ahead.ok && !issue_qk(t + 1)) break;
-        if (!mbar_wait_bounded(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.status)) break;
-        if (!mbar_wait_bounded(&v_full[t % C::NV], (t / C::NV) & 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t v_addr = sbase + C::V_OFF + (t % C::NV) * C::TILE;
-        const uint32_t p_tmem = tmem + P_COL + (t & 1) * (BN / 2);
-        const uint32_t acc0 = walk.first_tile() ? 0u : 1u;
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          umma_f16_ts(tmem + 2 * BN, p_tmem + ks * 8, smem_desc_sw128(v_addr + ks * 2048, SUB, 1024), IDESC_PV,
-                      ks > 0 ? 1u : acc0);
-        umma_commit(&o_done[t & 1]);
-        umma_commit(&v_empty[t % C::NV]);
       }
+#undef KVGQA_WAIT
       if (*abort_flag && issued) {
         // let every MMA issued so far finish before TMEM is released
-        umma_commit(drain);
+        if (elect_one()) umma_commit(drain);
+        __syncwarp();
         volatile int none = 0;
         mbar_wait_bounded(drain, 0, &none, nullptr);
       }
     }
+  }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    const int r = threadIdx.x;  // query row in the tile == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    regs_inc<kSoftmaxRegs>();
+    const int x = warp >> 2;           // head of the pair this group serves
+    const int r = threadIdx.x & 127;   // query row in the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_col = tmem + lane_base + x * BN;
+    const uint32_t o_col = tmem + lane_base + (2 + x) * BN;
     const float c = p.scale_log2;
     const float ce = c > 0.f ? c : 1.f;
     float m_ref = -INFINITY, l = 0.f;
     for (int t = 0; walk.ok; ++t, walk.advance()) {
+      if (x == 1 && walk.hB < 0) continue;  // single-head item: the B group has nothing to do
       const bool first = walk.first_tile(), diag = walk.last_tile();
-      if (!__all_sync(FULLMASK, mbar_wait_bounded(&s_full[t & 1], (t >> 1) & 1, abort_flag, p.status))) break;
+      if (!__all_sync(FULLMASK, mbar_wait_bounded(&s_full[x], t & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      // the four 32-column loads are issued back to back, then waited for once
-      uint32_t u0[32], u1[32], u2[32], u3[32];
-      tmem_ld32(tmem + lane_base + (t & 1) * BN + 0, u0);
-      tmem_ld32(tmem + lane_base + (t & 1) * BN + 32, u1);
-      tmem_ld32(tmem + lane_base + (t & 1) * BN + 64, u2);
-      tmem_ld32(tmem + lane_base + (t & 1) * BN + 96, u3);
-      tmem_wait_ld();
-      float sv[BN];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sv[i] = __uint_as_float(u0[i]);
-        sv[32 + i] = __uint_as_float(u1[i]);
-        sv[64 + i] = __uint_as_float(u2[i]);
-        sv[96 + i] = __uint_as_float(u3[i]);
+      // With head pairs the two groups take turns (A0 B0 A1 B1 ...): each runs
+      // its softmax alone on the SM's issue slots while the tensor core
+      // works for the other head.
+      if (walk.pairs && (x == 1 || t > 0)) {
+        const int k = x == 0 ? t - 1 : t;  // completion of the other group to wait for
+        if (!__all_sync(FULLMASK, mbar_wait_bounded(&turn[1 - x], k & 1, abort_flag, p.status))) break;
       }
       // Scores enter the softmax as s * ce with ce > 0 (a non-positive scale is
       // folded into the scores first, a path no usual caller takes).  On the
       // diagonal tile, keys after the query become -inf, so they weigh zero.
+      uint32_t u[BN];
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) tmem_ld32(s_col + q * 32, *reinterpret_cast<uint32_t(*)[32]>(u + q * 32));
+      tmem_wait_ld();
+      float* sv = reinterpret_cast<float*>(u);
       if (c <= 0.f) {
 #pragma unroll
         for (int i = 0; i < BN; ++i) sv[i] *= c;
@@ -341,11 +422,13 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
       }
       float mx[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(sv[2 * k], sv[2 * k + 1]);
 #pragma unroll
-      for (int i = 8; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
-      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int i = 16; i < BN; i += 16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], sv[i + 2 * k], sv[i + 2 * k + 1]);
+      }
+      const float mraw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float mt = mraw * ce;                    // tile maximum of the scaled scores
       const bool grow = first || mt > m_ref + 8.f;   // keep the old base unless it grew by 2^8
       float alpha = 1.f;
@@ -354,70 +437,70 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         m_ref = mt;
         l *= alpha;
       }
-      // P buffer t&1 in TMEM was last read by the P.V of tile t-2; an O rescale
-      // needs the P.V of tile t-1 complete.
-      if (t >= 2 && !__all_sync(FULLMASK, mbar_wait_bounded(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag, p.status)))
-        break;
-      const bool rescale = __any_sync(FULLMASK, grow && !first);
-      if (rescale && !__all_sync(FULLMASK, mbar_wait_bounded(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag,
-                                                          p.status)))
-        break;
-      tc_fence_after();
-      if (rescale) {
-#pragma unroll
+      // S_x of this tile being ready means the P.V of the previous tile is
+      // complete, so O_x may be rescaled here without a further wait.
+      if (__any_sync(FULLMASK, grow && !first)) {
+#pragma unroll 1
         for (int q = 0; q < D / 32; ++q) {
           uint32_t u[32];
-          tmem_ld32(tmem + lane_base + 2 * BN + q * 32, u);
+          tmem_ld32(o_col + q * 32, u);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(tmem + lane_base + 2 * BN + q * 32, u);
+          tmem_st32(o_col + q * 32, u);
         }
-        tmem_wait_st();
       }
-      // P as BF16 pairs into TMEM buffer t&1 (the A operand of P.V): row r, key
-      // pair j in 32-bit column j.
+      // P as BF16 pairs over the first 64 columns of S_x (the A operand of P.V).
       float2 ls = make_float2(0.f, 0.f);
       const float2 c2 = make_float2(ce, ce), nm2 = make_float2(-m_ref, -m_ref);
-      const uint32_t p_tmem = tmem + lane_base + P_COL + (t & 1) * (BN / 2);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int i0 = half * 64 + 2 * e;
-          const float2 x = ffma2(make_float2(sv[i0], sv[i0 + 1]), c2, nm2);
-          const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          const float2 xx = ffma2(make_float2(sv[i0], sv[i0 + 1]), c2, nm2);
+          const float2 pr = make_float2(ex2(xx.x), ex2(xx.y));
           ls = fadd2(ls, pr);
           w[e] = pack2(pr.x, pr.y);
         }
-        tmem_st32(p_tmem + half * 32, w);
+        tmem_st32(s_col + half * 32, w);
       }
       tmem_wait_st();
       l += ls.x + ls.y;
+      // Each warp arrives once (128 single-thread arrivals on one barrier
+      // serialise): every lane's TMEM stores are complete (wait::st) and
+      // fenced before the warp synchronises, then lane 0 arrives.
       tc_fence_before();
-      mbar_arrive(&p_full[t & 1]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&p_full[x]);
+        if (walk.pairs) mbar_arrive(&turn[x]);
+      }
 
       if (diag) {
         // ---------------------------------------------------- item epilogue
-        if (!__all_sync(FULLMASK, mbar_wait_bounded(&o_done[t & 1], (t >> 1) & 1, abort_flag, p.status))) break;
+        if (!__all_sync(FULLMASK, mbar_wait_bounded(&o_done[x], t & 1, abort_flag, p.status))) break;
         tc_fence_after();
         const int tq = walk.qt * BM + r;
         const float inv = 1.f / l;
-        uint16_t* dst = p.out + ((static_cast<size_t>(walk.a) * p.T + tq) * p.H_q + walk.h) * D;
-        uint32_t u[D];
+        const int h = x ? walk.hB : walk.hA;
+        uint16_t* dst = p.out + ((static_cast<size_t>(walk.a) * p.T + tq) * p.H_q + h) * D;
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + 2 * BN + q * 32, *reinterpret_cast<uint32_t(*)[32]>(u + q * 32));
-        tmem_wait_ld();
-        if (tq < p.T) {
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t u[32];
+          tmem_ld32(o_col + q * 32, u);  // warp-wide: rows past T load too, only their store is skipped
+          tmem_wait_ld();
+          if (tq < p.T) {
 #pragma unroll
-          for (int q8 = 0; q8 < D / 8; ++q8) {
-            uint4 o;
-            o.x = pack2(__uint_as_float(u[q8 * 8 + 0]) * inv, __uint_as_float(u[q8 * 8 + 1]) * inv);
-            o.y = pack2(__uint_as_float(u[q8 * 8 + 2]) * inv, __uint_as_float(u[q8 * 8 + 3]) * inv);
-            o.z = pack2(__uint_as_float(u[q8 * 8 + 4]) * inv, __uint_as_float(u[q8 * 8 + 5]) * inv);
-            o.w = pack2(__uint_as_float(u[q8 * 8 + 6]) * inv, __uint_as_float(u[q8 * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + q8 * 8) = o;
+            for (int q8 = 0; q8 < 4; ++q8) {
+              uint4 o;
+              o.x = pack2(__uint_as_float(u[q8 * 8 + 0]) * inv, __uint_as_float(u[q8 * 8 + 1]) * inv);
+              o.y = pack2(__uint_as_float(u[q8 * 8 + 2]) * inv, __uint_as_float(u[q8 * 8 + 3]) * inv);
+              o.z = pack2(__uint_as_float(u[q8 * 8 + 4]) * inv, __uint_as_float(u[q8 * 8 + 5]) * inv);
+              o.w = pack2(__uint_as_float(u[q8 * 8 + 6]) * inv, __uint_as_float(u[q8 * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + q * 32 + q8 * 8) = o;
+            }
           }
         }
       }
@@ -428,7 +511,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == W_MMA) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 cudaError_t make_maps(const PrefillParams& p, PrefillMaps* m) {
@@ -474,6 +557,11 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t 
   std::call_once(flags[dev], [&] {
     errs[dev] = cudaFuncSetAttribute(prefill_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      PCfg<D>::SMEM);
+    // The in-kernel register split needs the launch to hand out kLaunchRegs
+    // per thread; with fewer, setmaxnreg.inc could never be satisfied.
+    cudaFuncAttributes attr;
+    if (errs[dev] == cudaSuccess) errs[dev] = cudaFuncGetAttributes(&attr, prefill_attention_kernel<D>);
+    if (errs[dev] == cudaSuccess && attr.numRegs < kLaunchRegs) errs[dev] = cudaErrorInvalidConfiguration;
   });
   if (errs[dev] != cudaSuccess) return errs[dev];
   static int sms[64];
@@ -482,7 +570,8 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t 
     if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms[dev] = 0;
   });
   if (sms[dev] <= 0) return cudaErrorInvalidDevice;
-  const long long items = static_cast<long long>((p.T + BM - 1) / BM) * p.A * p.H_q;
+  const int per_tok = p.G % 2 == 0 ? p.H_q / 2 : p.H_q;  // head pairs when the group size is even
+  const long long items = static_cast<long long>((p.T + BM - 1) / BM) * p.A * per_tok;
   const unsigned grid = static_cast<unsigned>(items < sms[dev] ? items : sms[dev]);  // one CTA per SM
   prefill_attention_kernel<D><<<grid, THREADS, PCfg<D>::SMEM, stream>>>(p, m.q, m.k, m.v);
   return cudaGetLastError();
