@@ -219,27 +219,55 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 
 // K3, the combine: merge the partials of CTAs b0..b1 for segment (a, g) and
 // write the BF16 output of its G query heads.  One thread per d (d < D) of
-// the 128 softmax threads.  Partials of other CTAs are read past L1.
+// the 128 softmax threads.  Partials of other CTAs are read past L1, in
+// batches of kMaxParts partials whose loads (all heads) are issued before any
+// is used: one L2 round trip per batch instead of one per partial and head.
 template <int D, int GP>
 __device__ void combine_segment(const DecodeParams& p, int a, int g, int b0, int b1, int d) {
   if (d >= D) return;
   constexpr size_t SLOT = slot_floats(GP, D);
-  for (int h = 0; h < p.G; ++h) {
-    // one pass over the partials, rescaling the running sums as the maximum grows
-    float M = -INFINITY, lsum = 0.f, acc = 0.f;
-    for (int b = b0; b <= b1; ++b) {
+  constexpr int kMaxParts = GP >= 16 ? 1 : (GP >= 8 ? 2 : 4);  // bounded by registers
+  float M[GP], lsum[GP], acc[GP];
+#pragma unroll
+  for (int h = 0; h < GP; ++h) { M[h] = -INFINITY; lsum[h] = 0.f; acc[h] = 0.f; }
+  for (int bb = b0; bb <= b1; bb += kMaxParts) {
+    float m[kMaxParts][GP], lb[kMaxParts][GP], ob[kMaxParts][GP];
+#pragma unroll
+    for (int j = 0; j < kMaxParts; ++j) {
+      const int b = bb + j;
       const float* sp = p.partials + (static_cast<size_t>(b) * 2 + (b == b0 ? 1 : 0)) * SLOT;
-      const float m = __ldcg(sp + GP * D + h);
-      const float lb = __ldcg(sp + slot_l_offset(GP, D) + h);
-      const float ob = __ldcg(sp + h * D + d);
-      const float mn = fmaxf(M, m);
-      const float s_old = exp2f(M - mn), s_new = exp2f(m - mn);
-      lsum = lsum * s_old + lb * s_new;
-      acc = acc * s_old + ob * s_new;
-      M = mn;
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        const bool use = b <= b1 && h < p.G;
+        m[j][h] = use ? __ldcg(sp + GP * D + h) : -INFINITY;
+        lb[j][h] = use ? __ldcg(sp + slot_l_offset(GP, D) + h) : 0.f;
+        ob[j][h] = use ? __ldcg(sp + h * D + d) : 0.f;
+      }
     }
-    p.out[(static_cast<size_t>(a) * p.H_q + g * p.G + h) * D + d] = bf16_bits(acc / lsum);
+    // one pass over the batch, rescaling the running sums as the maximum grows
+#pragma unroll
+    for (int j = 0; j < kMaxParts; ++j) {
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        if (m[j][h] == -INFINITY) continue;  // unused entry
+        const float mn = fmaxf(M[h], m[j][h]);
+        const float s_old = exp2f(M[h] - mn), s_new = exp2f(m[j][h] - mn);
+        lsum[h] = lsum[h] * s_old + lb[j][h] * s_new;
+        acc[h] = acc[h] * s_old + ob[j][h] * s_new;
+        M[h] = mn;
+      }
+    }
   }
+#pragma unroll
+  for (int h = 0; h < GP; ++h)
+    if (h < p.G) p.out[(static_cast<size_t>(a) * p.H_q + g * p.G + h) * D + d] = bf16_bits(acc[h] / lsum[h]);
+}
+
+// Atomic add with release and acquire semantics at GPU scope.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* ptr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
 }
 
 template <int D, int GP>
@@ -512,16 +540,11 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
           // Count this CTA's partial; the CTA that completes the count merges.
           const int b0 = cur.vlo / W, b1 = (cur.vlo + cur.n - 1) / W;
           int* cnt = p.counters + cur.a * p.H_kv + cur.g;
-          // release: the barrier orders every thread's partial stores before
-          // thread 0's fence and count; acquire: the merging CTA fences after
-          // seeing the count complete, then the barrier hands that on.
+          // The barrier orders every thread's partial stores before thread 0's
+          // release-acquire count; the merging CTA's acquire makes the other
+          // CTAs' partials visible, and the next barrier hands that on.
           named_bar_sync(1, BN);
-          if (r == 0) {
-            __threadfence();
-            const bool last_one = atomicAdd(cnt, 1) == b1 - b0;
-            if (last_one) __threadfence();
-            *merge_flag = last_one;
-          }
+          if (r == 0) *merge_flag = atomic_add_acq_rel_gpu(cnt, 1) == b1 - b0;
           named_bar_sync(1, BN);
           if (*merge_flag) {
             combine_segment<D, GP>(p, cur.a, cur.g, b0, b1, r);

@@ -49,27 +49,29 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // suspension) takes about twice as long.
 constexpr uint32_t kSuspendHintNs = 50;
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = kSuspendHintNs) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
 
 // Wait for phase `parity` of `bar` to complete, but never forever: after
 // kWaitLimitNs (or as soon as another warp of the CTA has given up) it sets
-// the CTA's abort flag and the status bit and returns false.
+// the CTA's abort flag and the status bit and returns false.  Waits off the
+// critical path may pass a longer suspend hint (less polling).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort_flag, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                                  volatile int* abort_flag, int* status,
+                                                  uint32_t hint_ns = kSuspendHintNs) {
+  if (mbar_try_wait(bar, parity, hint_ns)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, hint_ns)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
