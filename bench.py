@@ -357,7 +357,7 @@ def run_ours(args, rank, world, local):
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,  # rope_kv_store_kernel + flash_decode_splitk_kernel per step
         "host_us_per_call": host_us,
         "clocks": clocks,
     }
