@@ -184,16 +184,19 @@ def profile_traffic(kernel_source: str, summary_name: str):
 
 # ---------------------------------------------------------------------- decode
 def decode_bytes(wl, positions):
-    """Algorithmic HBM bytes of one decode step: the attention call reads each
-    active row's K and V prefix (p+1 keys, all KV heads) and the rotated Q, and
-    writes the output; the store reads q, k, v and writes q_rot and one K and
-    one V cell per KV head."""
+    """Algorithmic HBM bytes of one decode step.  Attention call: each active
+    row's K and V prefix (p+1 keys, all KV heads), the rotated Q read and the
+    output written.  Two-call step: plus the store (q, k, v read; q_rot and one
+    K and one V cell per KV head written).  Single-launch step: the prefixes,
+    q, k, v read, the output and the cells written (no q_rot round trip)."""
     p = positions.astype(np.int64)
     kv_prefix = int(np.sum(p + 1)) * wl.H_kv * wl.D * 2 * 2
     q_bytes = wl.A * wl.H_q * wl.D * 2
+    kv_new = 2 * wl.A * wl.H_kv * wl.D * 2
     attn = kv_prefix + 2 * q_bytes
     store = 2 * (wl.A * (wl.H_q + 2 * wl.H_kv) * wl.D * 2)
-    return attn, attn + store
+    fused = kv_prefix + 2 * q_bytes + 2 * kv_new
+    return attn, attn + store, fused
 
 
 def hold_gpu(us: float):
@@ -206,11 +209,10 @@ def hold_gpu(us: float):
     sleep(int(min(us, 2e6) * 2000))   # cycles at about 2 GHz; the length only needs to be rough
 
 
-def host_call_us(*calls, n=200):
+def host_call_us(named_calls, n=200):
     """Host time of one prepared C-ABI call (validation + launch), in us."""
-    names = ["store", "attention", "prefill"]
     out = {}
-    for name, c in zip(names, calls):
+    for name, c in named_calls:
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(n):
@@ -242,63 +244,72 @@ def run_ours(args, rank, world, local):
 
     store = kv.prepare_rope_kv_store_out_(q, k, v, pos, rows, wl.theta, q_rot, kc, vc, ws1, stream)
     attend = kv.prepare_cached_gqa_attention_out_(q_rot, kc, vc, pos, rows, wl.scale, out, ws2, stream)
+    ws3 = kv.new_workspace(kv.decode_step_workspace_size(wl.A, wl.H_q, wl.H_kv, wl.D), dev)
+    step = kv.prepare_decode_step_out_(q, k, v, pos, rows, wl.theta, wl.scale, kc, vc, out, ws3, stream)
 
     for _ in range(max(args.warmup, 3)):
         store()
         attend()
+        step()
     torch.cuda.synchronize()
     if args.only == "prefill":
         res = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
         return {"impl": "ours", "only": "prefill", "prefill": res} if rank == 0 else None
-    host_us = host_call_us(store, attend, n=min(200, 10 * args.steps))
-    if kv.kvgqa_read_status(ws1) or kv.kvgqa_read_status(ws2):
+    host_us = host_call_us([("step", step), ("store", store), ("attention", attend)], n=min(200, 10 * args.steps))
+    if kv.kvgqa_read_status(ws1) or kv.kvgqa_read_status(ws2) or kv.kvgqa_read_status(ws3):
         raise RuntimeError("device status flags set during warm-up")
 
     K = args.steps
-    # (1) the step as a user runs it: both calls back to back, events around the pair
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+
+    def timed(body, per_step_host_us):
+        """K iterations of body() with the L2 flushed before each, CUDA events
+        around each body on the launching stream; per-iteration ms."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        torch.cuda.synchronize()
+        hold_gpu(K * (per_step_host_us + 40.0))
+        for i in range(K):
+            flush.zero_()
+            body(evs[i])
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def fused_body(e):
+        e[0].record(stream); step(); e[1].record(stream)
+
+    def two_call_body(e):
+        e[0].record(stream); store(); attend(); e[1].record(stream)
+
+    def attention_body(e):
+        store(); e[0].record(stream); attend(); e[1].record(stream)
+
+    # (1) the step as a user runs it: rope_kv_store_out_ then cached_gqa_attention_out_
     sampler = ClockSampler(dev.index) if rank == 0 and args.only is None else None
     if sampler:
         sampler.start()
     barrier(world)
-    torch.cuda.synchronize()
-    hold_gpu(K * (host_us["store"] + host_us["attention"] + 40.0))
-    for i in range(K):
-        flush.zero_()
-        ev[i][0].record(stream)
-        store()
-        attend()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms = timed(two_call_body, host_us["store"] + host_us["attention"])
     barrier(world)
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(float(sum(step_ms)), world)
-    # (2) the attention call alone (roofline of K2 + K3): the store runs before the
-    # first event so the events bracket exactly one cached_gqa_attention_out_ call
-    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    torch.cuda.synchronize()
-    hold_gpu(K * (host_us["store"] + host_us["attention"] + 40.0))
-    for i in range(K):
-        flush.zero_()
-        store()
-        eva[i][0].record(stream)
-        attend()
-        eva[i][1].record(stream)
-    torch.cuda.synchronize()
-    attn_ms = [a.elapsed_time(b) for a, b in eva]
-    flags = kv.kvgqa_read_status(ws1) | kv.kvgqa_read_status(ws2)
-    if flags:
-        raise RuntimeError(f"device status flags {flags} after the timed region")
-
-    attn_bytes, step_bytes = decode_bytes(wl, inp.positions.numpy())
+    attn_bytes, step_bytes, fused_bytes = decode_bytes(wl, inp.positions.numpy())
     tokens_per_s = wl.A * K * world / (total_ms / 1e3)
-    attn_avg_s = float(np.mean(attn_ms)) / 1e3
+    # (2) the attention call alone: the dominant kernel, for the roofline
+    attn_ms = timed(attention_body, host_us["store"] + host_us["attention"])
+    attn_avg_s = max_over_ranks(float(np.mean(attn_ms)), world) / 1e3
     achieved = attn_bytes / attn_avg_s / 1e9
     if args.only == "decode":
+        flags = kv.kvgqa_read_status(ws1) | kv.kvgqa_read_status(ws2)
+        if flags:
+            raise RuntimeError(f"device status flags {flags} after the timed region")
         return {"impl": "ours", "only": "decode", "value": round(tokens_per_s, 1), "unit": UNIT,
-                "attention_ms": round(attn_avg_s * 1e3, 5), "kv_gbs": round(achieved, 1)} if rank == 0 else None
+                "ms_per_step": round(total_ms / K, 5), "attention_gbs": round(achieved, 1)} if rank == 0 else None
+    # (3) the same step in one launch (decode_step_out_)
+    fused_ms = timed(fused_body, host_us["step"])
+    flags = kv.kvgqa_read_status(ws1) | kv.kvgqa_read_status(ws2) | kv.kvgqa_read_status(ws3)
+    if flags:
+        raise RuntimeError(f"device status flags {flags} after the timed region")
+    fused_avg_ms = max_over_ranks(float(np.mean(fused_ms)), world)
 
-    # ---- end to end: pinned host inputs -> device -> two calls -> host output
+    # ---- end to end: pinned host inputs -> device -> both calls -> host output
     h_q, h_k, h_v = inp.q.pin_memory(), inp.k.pin_memory(), inp.v.pin_memory()
     h_pos, h_rows = inp.positions.pin_memory(), inp.cache_rows.pin_memory()
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -348,11 +359,15 @@ def run_ours(args, rank, world, local):
                    "H_q": wl.H_q, "H_kv": wl.H_kv, "head_dim": wl.D, "theta": wl.theta,
                    "positions": "uniform [1,4096), seed 20261203", "l2": "flushed between timed steps (256 MB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "decode": {"attention_ms": round(attn_avg_s * 1e3, 5),
-                   "kv_bytes_per_step": attn_bytes, "step_bytes": step_bytes,
+        "decode": {"step": "rope_kv_store_out_ then cached_gqa_attention_out_ (two launches)",
+                   "step_bytes": step_bytes,
+                   "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1),
+                   "attention_ms": round(attn_avg_s * 1e3, 5), "attention_bytes": attn_bytes,
                    "kv_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm_peak, 4),
-                   "step_gbs": round(step_bytes / (total_ms / K / 1e3) / 1e9, 1)},
-        "roofline": {"kernel": "flash_decode_splitk (split-K with the combine run by the last CTA of each cut segment; one cached_gqa_attention_out_ call)",
+                   "single_launch_step_ms": round(fused_avg_ms, 5),
+                   "single_launch_tokens_per_s": round(wl.A * world / (fused_avg_ms / 1e3), 1),
+                   "single_launch_step_bytes": fused_bytes},
+        "roofline": {"kernel": "flash_decode_splitk_kernel (the cached_gqa_attention_out_ call; split-K with the combine run by the last CTA of each cut segment)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s"},

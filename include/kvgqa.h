@@ -143,8 +143,10 @@ kvgqa_status rope_kv_store_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
                                 void* stream);
 
 /* Workspace of cached_gqa_attention_out_ for these sizes on `device`: the
- * status block plus FP32 split-K partials (it depends on the device's SM
- * count, not on max_seq or the positions). */
+ * status block, one int32 counter per (row, KV head) and the FP32 split-K
+ * partials (it depends on the device's SM count, not on max_seq or the
+ * positions).  The counters must be zero before the first call (a zero-filled
+ * workspace is ready); every call leaves them at zero. */
 kvgqa_status cached_gqa_attention_workspace_size(int64_t A, int64_t H_q, int64_t H_kv,
                                                  int64_t D, int32_t device, size_t* bytes);
 
@@ -158,8 +160,8 @@ kvgqa_status cached_gqa_attention_workspace_size(int64_t A, int64_t H_q, int64_t
  * i.e. the token attends to its row's prefix including its own position (the
  * cell rope_kv_store_out_ just wrote).  Scores, softmax and the weighted sum
  * are FP32; out is rounded to BF16 once.  Nothing past position p of a row is
- * read.  The work is split over the whole GPU by key ranges; partial results
- * meet in a combine kernel.
+ * read.  The work is split over the whole GPU by key ranges; the CTA that
+ * finishes a split row last merges its partial results (one launch).
  *
  *   q_rot [A,H_q,D] bf16, k_cache/v_cache [S,H_kv,max_seq,D] bf16,
  *   positions/cache_rows [A] int32  (read)
@@ -175,6 +177,41 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
                                        const kvgqa_tensor* cache_rows, float scale,
                                        const kvgqa_tensor* out, const kvgqa_tensor* workspace,
                                        void* stream);
+
+/* Workspace of decode_step_out_: the same as cached_gqa_attention_out_'s. */
+kvgqa_status decode_step_workspace_size(int64_t A, int64_t H_q, int64_t H_kv, int64_t D,
+                                        int32_t device, size_t* bytes);
+
+/*
+ * decode_step_out_ -- the whole decode step of one layer in one launch:
+ * rope_kv_store_out_ followed by cached_gqa_attention_out_, without the
+ * rotated queries ever leaving the chip.
+ *
+ * microLLM-rocm ARCHITECTURE.md, section "Tensor ownership boundary":
+ * positions and cache rows parameterise decode-only RoPE, the K/V store and
+ * cached attention.  For every active token a (p = positions[a],
+ * r = cache_rows[a]): the rotated k[a] and the raw v[a] are stored into
+ * k_cache/v_cache[r,:,p,:] exactly as rope_kv_store_out_ stores them, and
+ * out[a] is the attention of the rotated q[a] over keys 0..p of row r, as
+ * cached_gqa_attention_out_ computes it (the rotated queries are rounded to
+ * BF16 first, as there).  The results are bit-identical to the two calls.
+ *
+ *   q [A,H_q,D], k/v [A,H_kv,D] bf16, positions/cache_rows [A] int32  (read)
+ *   theta > 0 and finite, scale finite
+ *   k_cache/v_cache [S,H_kv,max_seq,D] bf16 (read; the cells (r,:,p,:) written)
+ *   out [A,H_q,D] bf16 (written; rows with invalid metadata are left
+ *     unwritten, their cells untouched, and a status bit is set)
+ *   workspace  >= decode_step_workspace_size(...) bytes, 256-byte aligned,
+ *     counters zero before the first call (left zero by every call)
+ * Limits as cached_gqa_attention_out_.  cache_rows must be distinct.  A = 0
+ * is a no-op.  There is no q_out: callers that need the rotated queries use
+ * the two-call path.
+ */
+kvgqa_status decode_step_out_(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tensor* v,
+                              const kvgqa_tensor* positions, const kvgqa_tensor* cache_rows,
+                              double theta, float scale, const kvgqa_tensor* k_cache,
+                              const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
+                              const kvgqa_tensor* workspace, void* stream);
 
 /*
  * cached_gqa_attention_static_scratch_out_ -- the same attention as
@@ -193,9 +230,10 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
  * The first call on a device looks up the device address of that array (once
  * per device, with that device current); make that first call before any
  * stream capture.  Sizes whose partials do not fit the array are rejected
- * with KVGQA_EUNSUPPORTED.  Every call shares the one array and overwrites the
- * partials of the previous call before reading them, so nothing needs to start
- * at zero; calls whose kernels overlap on the GPU (different streams, or
+ * with KVGQA_EUNSUPPORTED.  Every call shares the one array: it overwrites the
+ * partials of the previous call before reading them, and the per-row counters
+ * it keeps there start at zero when the library loads and are left at zero by
+ * every call; calls whose kernels overlap on the GPU (different streams, or
  * different host threads) race on it.  Device-side range checks still skip
  * rows with invalid positions or cache rows, but this variant has no status
  * word for the caller to read.

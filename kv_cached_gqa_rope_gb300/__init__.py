@@ -71,6 +71,10 @@ def _load():
     lib.prefill_gqa_cached_rows_out_.restype = st
     lib.cached_gqa_attention_static_scratch_out_.argtypes = [P, P, P, P, P, ctypes.c_float, P, ctypes.c_void_p]
     lib.cached_gqa_attention_static_scratch_out_.restype = st
+    lib.decode_step_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.decode_step_workspace_size.restype = st
+    lib.decode_step_out_.argtypes = [P, P, P, P, P, ctypes.c_double, ctypes.c_float, P, P, P, P, ctypes.c_void_p]
+    lib.decode_step_out_.restype = st
     lib.kvgqa_read_status.argtypes = [P, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.kvgqa_read_status.restype = st
     return lib
@@ -82,7 +86,8 @@ EXPORTED_SYMBOLS = ("kvgqa_abi_version", "kvgqa_last_error", "rope_kv_store_work
                     "rope_kv_store_out_", "cached_gqa_attention_workspace_size",
                     "cached_gqa_attention_out_", "prefill_gqa_cached_rows_workspace_size",
                     "prefill_gqa_cached_rows_out_", "kvgqa_read_status",
-                    "cached_gqa_attention_static_scratch_out_")
+                    "cached_gqa_attention_static_scratch_out_", "decode_step_workspace_size",
+                    "decode_step_out_")
 
 
 def library() -> ctypes.CDLL:
@@ -143,6 +148,14 @@ def cached_gqa_attention_workspace_size(A: int, H_q: int, H_kv: int, D: int, dev
     return n.value
 
 
+def decode_step_workspace_size(A: int, H_q: int, H_kv: int, D: int, device: int = None) -> int:
+    if device is None:
+        device = torch.cuda.current_device()
+    n = ctypes.c_size_t()
+    _check(_lib.decode_step_workspace_size(A, H_q, H_kv, D, device, ctypes.byref(n)))
+    return n.value
+
+
 def prefill_gqa_cached_rows_workspace_size(A: int, T: int, H_q: int, H_kv: int, D: int) -> int:
     n = ctypes.c_size_t()
     _check(_lib.prefill_gqa_cached_rows_workspace_size(A, T, H_q, H_kv, D, ctypes.byref(n)))
@@ -161,6 +174,15 @@ def cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_rows, sc
     ds = [describe(t) for t in (q_rot, k_cache, v_cache, positions, cache_rows)]
     o, w = describe(out), describe(workspace)
     _check(_lib.cached_gqa_attention_out_(*map(_ref, ds), float(scale), _ref(o), _ref(w), _stream(stream)))
+
+
+def decode_step_out_(q, k, v, positions, cache_rows, theta, scale, k_cache, v_cache, out, workspace,
+                     stream=None) -> None:
+    """The whole decode step in one launch: the store of rope_kv_store_out_
+    and the attention of cached_gqa_attention_out_ (no q_out)."""
+    ds = [describe(t) for t in (q, k, v, positions, cache_rows)]
+    outs = [describe(t) for t in (k_cache, v_cache, out, workspace)]
+    _check(_lib.decode_step_out_(*map(_ref, ds), float(theta), float(scale), *map(_ref, outs), _stream(stream)))
 
 
 def cached_gqa_attention_static_scratch_out_(q_rot, k_cache, v_cache, positions, cache_rows, scale, out,
@@ -210,6 +232,15 @@ def prepare_cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_
     args = (*map(_ref, ds[:5]), ctypes.c_float(scale), *map(_ref, ds[5:]), ctypes.c_void_p(_stream(stream)))
     return Prepared(_lib.cached_gqa_attention_out_, args,
                     (ds, q_rot, k_cache, v_cache, positions, cache_rows, out, workspace))
+
+
+def prepare_decode_step_out_(q, k, v, positions, cache_rows, theta, scale, k_cache, v_cache, out, workspace,
+                             stream=None) -> Prepared:
+    ds = [describe(t) for t in (q, k, v, positions, cache_rows, k_cache, v_cache, out, workspace)]
+    args = (*map(_ref, ds[:5]), ctypes.c_double(theta), ctypes.c_float(scale), *map(_ref, ds[5:]),
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared(_lib.decode_step_out_, args,
+                    (ds, q, k, v, positions, cache_rows, k_cache, v_cache, out, workspace))
 
 
 def prepare_prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_cache, out, workspace,

@@ -330,6 +330,75 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
   });
 }
 
+kvgqa_status decode_step_workspace_size(int64_t A, int64_t H_q, int64_t H_kv, int64_t D, int32_t device,
+                                        size_t* bytes) {
+  return cached_gqa_attention_workspace_size(A, H_q, H_kv, D, device, bytes);
+}
+
+kvgqa_status decode_step_out_(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tensor* v,
+                              const kvgqa_tensor* positions, const kvgqa_tensor* cache_rows, double theta,
+                              float scale, const kvgqa_tensor* k_cache, const kvgqa_tensor* v_cache,
+                              const kvgqa_tensor* out, const kvgqa_tensor* workspace, void* stream) {
+  return guarded([&] {
+    if (!q || !k_cache) fail(KVGQA_EINVAL, "null descriptor");
+    if (q->ndim != 3 || k_cache->ndim != 4) fail(KVGQA_EINVAL, "q must be [A,H_q,D], caches [S,H_kv,max_seq,D]");
+    const int64_t A = q->shape[0], H_q = q->shape[1], D = q->shape[2];
+    const int64_t S = k_cache->shape[0], H_kv = k_cache->shape[1], max_seq = k_cache->shape[2];
+    check_head_dim(D);
+    check_heads(H_q, H_kv);
+    check_theta(theta);
+    if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
+    const int G = (int)(H_q / H_kv);
+    if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
+    if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
+    if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
+    View vq = check_tensor("q", q, 3, KVGQA_BF16, 16);
+    View vk = check_tensor("k", k, 3, KVGQA_BF16, 16);
+    View vv = check_tensor("v", v, 3, KVGQA_BF16, 16);
+    View vp = check_tensor("positions", positions, 1, KVGQA_I32, 4);
+    View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
+    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+    View vo = check_tensor("out", out, 3, KVGQA_BF16, 16);
+    require_shape(vk, {A, H_kv, D});
+    require_shape(vv, {A, H_kv, D});
+    require_shape(vp, {A});
+    require_shape(vr, {A});
+    require_shape(vvc, {S, H_kv, max_seq, D});
+    require_shape(vo, {A, H_q, D});
+    View vws0 = check_workspace(workspace, KVGQA_STATUS_BYTES);
+    check_no_alias({&vkc, &vvc, &vo, &vws0}, {&vq, &vk, &vv, &vp, &vr, &vkc, &vvc, &vo, &vws0});
+    const int dev = current_device();
+    kvgqa::DecodeLayout lay;
+    check_cuda(kvgqa::decode_layout(dev, (int)D, kvgqa::decode_group_pad(G), A, H_kv, &lay),
+               "decode kernel set-up");
+    View vws = check_workspace(workspace, KVGQA_STATUS_BYTES + lay.counter_bytes + lay.partial_bytes);
+    check_device({&vq, &vk, &vv, &vp, &vr, &vkc, &vvc, &vo, &vws}, dev);
+    if (A == 0) return;
+    kvgqa::DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q->data);
+    p.k_cache = static_cast<const uint16_t*>(k_cache->data);
+    p.v_cache = static_cast<const uint16_t*>(v_cache->data);
+    p.positions = static_cast<const int32_t*>(positions->data);
+    p.cache_rows = static_cast<const int32_t*>(cache_rows->data);
+    p.out = static_cast<uint16_t*>(out->data);
+    unsigned char* ws = static_cast<unsigned char*>(workspace->data);
+    p.status = reinterpret_cast<int32_t*>(ws);
+    p.counters = reinterpret_cast<int32_t*>(ws + KVGQA_STATUS_BYTES);
+    p.partials = reinterpret_cast<float*>(ws + KVGQA_STATUS_BYTES + lay.counter_bytes);
+    p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
+    p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.fused = 1;
+    p.k_new = static_cast<const uint16_t*>(k->data);
+    p.v_new = static_cast<const uint16_t*>(v->data);
+    p.k_cache_w = static_cast<uint16_t*>(k_cache->data);
+    p.v_cache_w = static_cast<uint16_t*>(v_cache->data);
+    fill_inv_freq(p.inv_freq, (int)D, theta);
+    check_cuda(kvgqa::launch_cached_gqa_attention(p, static_cast<cudaStream_t>(stream)), "decode_step launch");
+  });
+}
+
 kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
                                                       const kvgqa_tensor* k_cache,
                                                       const kvgqa_tensor* v_cache,

@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "kvgqa_internal.h"
+#include "rope_math.cuh"
 #include "tcgen05.cuh"
 
 namespace kvgqa {
@@ -60,7 +61,8 @@ constexpr int NQ = 16;                  // MMA N: query heads of a group, padded
 constexpr int BOX_ROWS = 32;            // rows per TMA box of a K or V tile
 constexpr int SUB = BN * 128;           // one [128 rows x 64 bf16] swizzled sub-tile
 constexpr int QSUB = NQ * 128;          // one [16 rows x 64 bf16] swizzled sub-tile
-constexpr int THREADS = 192;            // 4 softmax warps + producer + MMA
+// 4 softmax warps + producer + MMA, plus the query/cell prep warp of the fused step
+__host__ __device__ constexpr int threads_of(bool fused) { return fused ? 224 : 192; }
 constexpr int TMEM_COLS = 64;           // S^T x2 (16 cols each) + O^T (16 cols)
 constexpr int W_MIN = 256;              // fewest (virtual) keys a CTA is given
 constexpr int SEG_V = 128;              // virtual keys charged for a segment end
@@ -73,21 +75,31 @@ __host__ __device__ constexpr int slot_floats(int GP, int D) { return GP * D + 2
 __host__ __device__ constexpr int slot_l_offset(int GP, int D) { return GP * D + (GP < 2 ? 2 : GP); }
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-template <int D>
+template <int D, bool FUSED>
 struct Cfg {
   static constexpr int NSUB = D / 64;
   static constexpr int NS = D == 128 ? 3 : 4;          // stages
   static constexpr int K_OFF = 0;                      // inside a stage
   static constexpr int V_OFF = NSUB * SUB;
+  // Attention call: each stage also carries the segment's (rotated) query
+  // tile, loaded with every K/V tile.  Fused step: the query tile is rotated
+  // in shared memory once per segment, in a ring of QR buffers, one more than
+  // the stages, so the producer (at most NS tiles, hence NS segments, ahead)
+  // never waits for a query buffer and no per-segment barrier of the ring can
+  // run two phases ahead of its waiter.
   static constexpr int Q_OFF = 2 * NSUB * SUB;
-  static constexpr int STAGE = 2 * NSUB * SUB + NSUB * QSUB;   // multiple of 1024
-  static constexpr int P_OFF = NS * STAGE;                     // P^T x2 buffers, [16 x 128 keys] each
+  static constexpr int STAGE = FUSED ? 2 * NSUB * SUB : 2 * NSUB * SUB + NSUB * QSUB;  // multiple of 1024
+  static constexpr int QR = FUSED ? NS + 1 : 0;
+  static constexpr int QB_OFF = NS * STAGE;            // fused: query tiles [QR][16 x D]
+  static constexpr int QBUF = NSUB * QSUB;
+  static constexpr int P_OFF = QB_OFF + QR * QBUF;             // P^T x2 buffers, [16 x 128 keys] each
   static constexpr int RED_OFF = P_OFF + 2 * 2 * QSUB;         // [2][4 warps][16] floats
   static constexpr int PREFIX_OFF = RED_OFF + 2 * 4 * NQ * 4;  // [kMaxActiveRows + 1] ints
   static constexpr int NKEYS_OFF = PREFIX_OFF + (kMaxActiveRows + 1) * 4;  // [kMaxActiveRows] ints
   static constexpr int BAR_OFF = align_up(NKEYS_OFF + kMaxActiveRows * 4, 16);
-  // kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NBAR = 2 * NS + 7;
+  // kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], q_free[QR],
+  // prep_done[QR], patch_done[QR], last_full[QR], drain
+  static constexpr int NBAR = 2 * NS + 7 + 4 * QR;
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 8;
   static constexpr int SMEM = FLAG_OFF + 16 + 1024;            // + alignment slack
@@ -210,6 +222,10 @@ struct Cursor {
     if (!last()) { x += nt(); return; }
     if (!next_segment()) done_ = true;
   }
+  // Skip the rest of the current segment (a walk over segments only).
+  __device__ void advance_segment() {
+    if (!next_segment()) done_ = true;
+  }
 };
 
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
@@ -270,11 +286,11 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* ptr, int v) {
   return old;
 }
 
-template <int D, int GP>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int D, int GP, bool FUSED>
+__global__ void __launch_bounds__(threads_of(FUSED), 1)
 flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap map_k,
                            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_q) {
-  using C = Cfg<D>;
+  using C = Cfg<D, FUSED>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
@@ -286,7 +302,12 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   uint64_t* s_full = bars + 2 * C::NS;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
-  uint64_t* drain = o_done + 2;
+  // per segment k, slot k % QR, phase k / QR:
+  uint64_t* q_free = o_done + 2;           // the segment's S MMAs are complete
+  uint64_t* prep_done = q_free + C::QR;    // fused step: its query tile is rotated
+  uint64_t* patch_done = prep_done + C::QR;  // fused step: the new key is in its last tile
+  uint64_t* last_full = patch_done + C::QR;  // fused step: the TMA of the tile with the new key landed
+  uint64_t* drain = last_full + C::QR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
   volatile int* merge_flag = abort_flag + 1;
@@ -301,6 +322,12 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 1);
       mbar_init(&o_done[b], 1);
+    }
+    for (int b = 0; b < C::QR; ++b) {
+      mbar_init(&q_free[b], 1);
+      mbar_init(&prep_done[b], 1);
+      mbar_init(&patch_done[b], 1);
+      mbar_init(&last_full[b], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -333,30 +360,82 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     if (lane == 0) {
       const uint64_t pol_kv = l2_evict_first_policy();
       const uint64_t pol_q = l2_evict_last_policy();
-      int it = 0;
-      for (; cur.more(); cur.advance(), ++it) {
-        const int s = it % C::NS;
-        if (it >= C::NS && !mbar_wait_bounded(&kv_empty[s], ((it / C::NS) - 1) & 1, abort_flag, p.status)) break;
-        const int nb = (cur.nt() + BOX_ROWS - 1) / BOX_ROWS;
-        const uint32_t bytes = static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + QSUB);
-        unsigned char* st = smem + s * C::STAGE;
-        const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
-        mbar_arrive_expect_tx(&kv_full[s], bytes);
-        for (int sub = 0; sub < C::NSUB; ++sub) {
-          for (int b = 0; b < nb; ++b) {
-            tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
-                        kv_row, &kv_full[s], pol_kv);
-            tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
-                        kv_row, &kv_full[s], pol_kv);
+      if constexpr (!FUSED) {
+        // each tile brings its K and V rows and the segment's rotated query tile
+        int it = 0;
+        for (; cur.more(); cur.advance(), ++it) {
+          const int s = it % C::NS;
+          if (it >= C::NS && !mbar_wait_bounded(&kv_empty[s], ((it / C::NS) - 1) & 1, abort_flag, p.status)) break;
+          const int nb = (cur.nt() + BOX_ROWS - 1) / BOX_ROWS;
+          const uint32_t bytes = static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + QSUB);
+          unsigned char* st = smem + s * C::STAGE;
+          const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
+          mbar_arrive_expect_tx(&kv_full[s], bytes);
+          for (int sub = 0; sub < C::NSUB; ++sub) {
+            for (int b = 0; b < nb; ++b) {
+              tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
+                          kv_row, &kv_full[s], pol_kv);
+              tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
+                          kv_row, &kv_full[s], pol_kv);
+            }
+            tma_load_3d(st + C::Q_OFF + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, &kv_full[s],
+                        pol_q);
           }
-          tma_load_3d(st + C::Q_OFF + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, &kv_full[s],
-                      pol_q);
         }
-      }
-      if (*abort_flag) {
-        volatile int none = 0;
-        for (int t = it - C::NS < 0 ? 0 : it - C::NS; t < it; ++t)
-          mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, &none, nullptr);
+        if (*abort_flag) {
+          volatile int none = 0;
+          for (int t = it - C::NS < 0 ? 0 : it - C::NS; t < it; ++t)
+            mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, &none, nullptr);
+        }
+      } else {
+        // The segment's raw query tile comes with its first tile, into ring
+        // slot kseg % QR once the S MMAs of segment kseg - QR are done; the prep
+        // warp rotates it in place.  The tile that holds the new key lands on
+        // the segment's own barrier (last_full), which the prep warp waits for
+        // before patching the key in (kv_full of a stage could be several
+        // phases ahead of it); kv_full[s] gets a plain arrival so its phases
+        // stay in step, and the MMA warp waits for the patch instead.
+        int it = 0, kseg = -1;
+        int nk_recent = -1;  // the most recent segment whose new-key tile was issued
+        for (; cur.more(); cur.advance(), ++it) {
+          const int s = it % C::NS;
+          if (cur.first()) ++kseg;
+          if (it >= C::NS && !mbar_wait_bounded(&kv_empty[s], ((it / C::NS) - 1) & 1, abort_flag, p.status)) break;
+          const bool load_q = cur.first();
+          if (load_q && kseg >= C::QR &&
+              !mbar_wait_bounded(&q_free[kseg % C::QR], (kseg / C::QR - 1) & 1, abort_flag, p.status))
+            break;
+          const int nb = (cur.nt() + BOX_ROWS - 1) / BOX_ROWS;
+          const uint32_t bytes = static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + (load_q ? QSUB : 0u));
+          unsigned char* st = smem + s * C::STAGE;
+          unsigned char* qb = smem + C::QB_OFF + (kseg % C::QR) * C::QBUF;
+          const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
+          const bool newkey_tile = cur.last() && cur.x_end == cur.n;
+          uint64_t* bar = newkey_tile ? &last_full[kseg % C::QR] : &kv_full[s];
+          mbar_arrive_expect_tx(bar, bytes);
+          if (newkey_tile) {
+            mbar_arrive(&kv_full[s]);
+            nk_recent = kseg;
+          }
+          for (int sub = 0; sub < C::NSUB; ++sub) {
+            for (int b = 0; b < nb; ++b) {
+              tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
+                          kv_row, bar, pol_kv);
+              tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
+                          kv_row, bar, pol_kv);
+            }
+            if (load_q) tma_load_3d(qb + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, bar, pol_q);
+          }
+        }
+        if (*abort_flag) {
+          volatile int none = 0;
+          for (int t = it - C::NS < 0 ? 0 : it - C::NS; t < it; ++t)
+            mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, &none, nullptr);
+          // the new-key tiles still in flight belong to the last (at most NS)
+          // new-key segments, which are consecutive
+          for (int k = nk_recent; k >= 0 && k > nk_recent - C::NS; --k)
+            mbar_wait_bounded(&last_full[k % C::QR], (k / C::QR) & 1, &none, nullptr);
+        }
       }
     }
   } else if (warp == 5) {
@@ -367,30 +446,53 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       constexpr uint32_t V_LBO = D == 128 ? SUB : 0;  // D = 64: the second M half repeats the first
       const uint32_t p_addr = sbase + C::P_OFF;
       bool issued = false;
-      auto issue_s = [&](int t) {
+      // S^T of tile t.  Attention call: the query tile rides in the tile's
+      // stage.  Fused step: it is ring slot kq % QR of segment kq, rotated by
+      // the prep warp; the slot is released after the segment's last S, and a
+      // tile that holds the new key waits for the prep warp's patch.
+      auto issue_s = [&](int t, int kq, bool seg_first, bool seg_last, bool new_key) -> bool {
+        if (!mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, abort_flag, p.status)) return false;
+        if constexpr (FUSED) {
+          if (seg_first && !mbar_wait_bounded(&prep_done[kq % C::QR], (kq / C::QR) & 1, abort_flag, p.status))
+            return false;
+          if (new_key && !mbar_wait_bounded(&patch_done[kq % C::QR], (kq / C::QR) & 1, abort_flag, p.status))
+            return false;
+        }
+        tc_fence_after();
         const uint32_t st = sbase + (t % C::NS) * C::STAGE;
+        const uint32_t qb = FUSED ? sbase + C::QB_OFF + (kq % C::QR) * C::QBUF : st + C::Q_OFF;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = (ks / 4) * SUB + (ks % 4) * 32;
           const uint32_t qoff = (ks / 4) * QSUB + (ks % 4) * 32;
           umma_f16_ss(tmem + (t & 1) * NQ, smem_desc_sw128(st + C::K_OFF + koff, 16, 1024),
-                      smem_desc_sw128(st + C::Q_OFF + qoff, 16, 1024), IDESC_S, ks > 0);
+                      smem_desc_sw128(qb + qoff, 16, 1024), IDESC_S, ks > 0);
         }
         umma_commit(&s_full[t & 1]);
-        issued = true;
-      };
-      int it = 0;
-      for (; cur.more(); cur.advance(), ++it) {
-        if (it == 0) {
-          if (!mbar_wait_bounded(&kv_full[0], 0, abort_flag, p.status)) break;
-          tc_fence_after();
-          issue_s(0);
+        if constexpr (FUSED) {
+          if (seg_last) umma_commit(&q_free[kq % C::QR]);
         }
-        if (cur.has_next()) {  // another tile follows: overlap its S with this softmax
-          const int t = it + 1;
-          if (!mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, abort_flag, p.status)) break;
-          tc_fence_after();
-          issue_s(t);
+        issued = true;
+        return true;
+      };
+      int it = 0, kseg = -1;
+      for (; cur.more(); cur.advance(), ++it) {
+        if (cur.first()) ++kseg;
+        if (it == 0 && !issue_s(0, 0, true, cur.last(), cur.last() && cur.x_end == cur.n)) break;
+        // another tile follows: overlap its S with this softmax (the next
+        // segment's facts are needed only when this tile ends a segment)
+        if (cur.has_next()) {
+          bool n_last, n_key;
+          if (!cur.last()) {
+            n_last = cur.x_end - (cur.x + cur.nt()) <= BN;
+            n_key = n_last && cur.x_end == cur.n;
+          } else {
+            Cursor nx = cur;
+            nx.advance();
+            n_last = nx.last();
+            n_key = n_last && nx.x_end == nx.n;
+          }
+          if (!issue_s(it + 1, cur.last() ? kseg + 1 : kseg, cur.last(), n_last, n_key)) break;
         }
         if (!mbar_wait_bounded(&p_full[it & 1], (it >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -412,7 +514,112 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         mbar_wait_bounded(drain, 0, &none, nullptr);
       }
     }
-  } else {
+  } else if (FUSED && warp == 6) {
+    // ---------------------------------------------------------- query / cell prep (fused step)
+    // Per segment of this CTA, in order: rotate the group's G raw query rows
+    // (loaded with the segment's first tile into query buffer k % QR, 128B
+    // swizzled, K-major) in place at the row's position; and if this CTA
+    // holds the segment's last key, rotate the new K, store it with the new V
+    // into the row's cell at that position, and write the same row into the
+    // last K/V tile in shared memory (the TMA loaded the stale cell).  Lane l
+    // owns the frequency pairs j = l + 32u.
+    if constexpr (FUSED) {
+      constexpr int HALF = D / 2;
+      constexpr int NU = HALF / 32;
+      auto cell = [&](unsigned char* base, int row, int c) -> uint16_t* {  // 128B-swizzled [rows][64] sub-tiles
+        const int cc = c & 63, chunk = cc >> 3;
+        return reinterpret_cast<uint16_t*>(base + (row * 128 + ((chunk ^ (row & 7)) << 4) + (cc & 7) * 2));
+      };
+      // cos/sin depend on the row's position only: the KV heads of one row
+      // are consecutive segments, so they are evaluated (in FP64, the costly
+      // part) once per row, not once per segment.
+      CosSin cs[NU];
+      int cs_row = -1, t_first = 0;
+      for (int k = 0; cur.more(); ++k) {
+        const int b = k % C::QR, ph = (k / C::QR) & 1;
+        const int pos = nkeys[cur.a] - 1;
+        Cursor c = cur;  // find the segment's last tile in this CTA
+        int t_last = t_first;
+        while (!c.last()) { c.advance(); ++t_last; }
+        const bool new_key = cur.x_end == cur.n;
+        const size_t src_off = (static_cast<size_t>(cur.a) * p.H_kv + cur.g) * D;
+        uint16_t kn[2 * NU], vn[D / 32];
+        if (new_key) {  // issue the loads of the new K/V early
+#pragma unroll
+          for (int u = 0; u < NU; ++u) {
+            kn[2 * u] = p.k_new[src_off + lane + 32 * u];
+            kn[2 * u + 1] = p.k_new[src_off + lane + 32 * u + HALF];
+          }
+#pragma unroll
+          for (int e = 0; e < D / 32; ++e) vn[e] = p.v_new[src_off + lane + 32 * e];
+        }
+        if (cur.a != cs_row) {
+#pragma unroll
+          for (int u = 0; u < NU; ++u) cs[u] = rope_cos_sin(pos, p.inv_freq[lane + 32 * u]);
+          cs_row = cur.a;
+        }
+        // the raw query tile arrives with the segment's first tile (on the
+        // segment's own barrier when that tile also holds the new key)
+        const bool q_on_last = new_key && t_last == t_first;
+        if (!__all_sync(FULL, q_on_last ? mbar_wait_bounded(&last_full[b], ph, abort_flag, p.status)
+                                        : mbar_wait_bounded(&kv_full[t_first % C::NS], (t_first / C::NS) & 1,
+                                                            abort_flag, p.status)))
+          break;
+        unsigned char* qb = smem + C::QB_OFF + b * C::QBUF;
+        for (int h = 0; h < p.G; ++h) {
+#pragma unroll
+          for (int u = 0; u < NU; ++u) {
+            const int j = lane + 32 * u;
+            uint16_t* c1 = cell(qb + (j >> 6) * QSUB, h, j);
+            uint16_t* c2 = cell(qb + ((j + HALF) >> 6) * QSUB, h, j + HALF);
+            const float x1 = bf16_bits_to_f32(*c1), x2 = bf16_bits_to_f32(*c2);
+            *c1 = bf16_rn_bits(rot_first(x1, x2, cs[u]));
+            *c2 = bf16_rn_bits(rot_second(x1, x2, cs[u]));
+          }
+        }
+        fence_proxy_async_smem();  // the query tile is read by the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&prep_done[b]);
+        if (new_key) {
+          uint16_t kr[2 * NU];
+#pragma unroll
+          for (int u = 0; u < NU; ++u) {
+            const float x1 = bf16_bits_to_f32(kn[2 * u]), x2 = bf16_bits_to_f32(kn[2 * u + 1]);
+            kr[2 * u] = bf16_rn_bits(rot_first(x1, x2, cs[u]));
+            kr[2 * u + 1] = bf16_rn_bits(rot_second(x1, x2, cs[u]));
+          }
+          const size_t cell_off = ((static_cast<size_t>(p.cache_rows[cur.a]) * p.H_kv + cur.g) * p.max_seq + pos) * D;
+#pragma unroll
+          for (int u = 0; u < NU; ++u) {
+            p.k_cache_w[cell_off + lane + 32 * u] = kr[2 * u];
+            p.k_cache_w[cell_off + lane + 32 * u + HALF] = kr[2 * u + 1];
+          }
+#pragma unroll
+          for (int e = 0; e < D / 32; ++e) p.v_cache_w[cell_off + lane + 32 * e] = vn[e];
+          // the last tile (rows k0.. of this segment) holds the stale cell at row pos - k0
+          if (!__all_sync(FULL, mbar_wait_bounded(&last_full[b], ph, abort_flag, p.status))) break;
+          const int row = pos - c.k0();
+          unsigned char* st = smem + (t_last % C::NS) * C::STAGE;
+#pragma unroll
+          for (int u = 0; u < NU; ++u) {
+            const int j = lane + 32 * u;
+            *cell(st + C::K_OFF + (j >> 6) * SUB, row, j) = kr[2 * u];
+            *cell(st + C::K_OFF + ((j + HALF) >> 6) * SUB, row, j + HALF) = kr[2 * u + 1];
+          }
+#pragma unroll
+          for (int e = 0; e < D / 32; ++e) {
+            const int j = lane + 32 * e;
+            *cell(st + C::V_OFF + (j >> 6) * SUB, row, j) = vn[e];
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&patch_done[b]);
+        }
+        t_first = t_last + 1;
+        cur.advance_segment();
+      }
+    }
+  } else if (warp < 4) {
     // ---------------------------------------------------------- softmax (warps 0-3)
     const int r = threadIdx.x;  // key row of the tile == TMEM lane == d of O^T
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
@@ -598,8 +805,11 @@ struct Kernels {
     static int ctas[64];
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::call_once(flags[device], [&]() {
-      errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+      errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP, false>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, false>::SMEM);
+      if (errs[device] == cudaSuccess)
+        errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, true>::SMEM);
       int sms = 0;
       if (errs[device] == cudaSuccess)
         errs[device] = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
@@ -608,18 +818,22 @@ struct Kernels {
     *num_ctas = ctas[device];
     return errs[device];
   }
-  static cudaError_t launch(const DecodeParams& p, const DecodeMaps& m, cudaStream_t stream) {
+  template <bool FUSED>
+  static cudaError_t launch_mode(const DecodeParams& p, const DecodeMaps& m, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_ctas);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+    cfg.blockDim = dim3(threads_of(FUSED));
+    cfg.dynamicSmemBytes = Cfg<D, FUSED>::SMEM;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP>, p, m.kc, m.vc, m.q);
+    return cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP, FUSED>, p, m.kc, m.vc, m.q);
+  }
+  static cudaError_t launch(const DecodeParams& p, const DecodeMaps& m, cudaStream_t stream) {
+    return p.fused ? launch_mode<true>(p, m, stream) : launch_mode<false>(p, m, stream);
   }
 };
 

@@ -34,7 +34,7 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, bool prefill, cudaStr
 
 // ------------------------------------------------------------------ decode attention
 struct DecodeParams {
-  const uint16_t* q;          // [A,H_q,D] rotated queries
+  const uint16_t* q;          // [A,H_q,D] rotated queries (attention call) or raw queries (fused step)
   const uint16_t* k_cache;    // [S,H_kv,max_seq,D]
   const uint16_t* v_cache;
   const int32_t* positions;   // [A]
@@ -46,6 +46,14 @@ struct DecodeParams {
   int A, H_q, H_kv, G, D, S, max_seq;
   int num_ctas;               // grid size of the split-K kernel
   float scale_log2;           // scale * log2(e)
+  // Fused decode step only (fused != 0): the kernel rotates q itself and
+  // stores the rotated new K and raw new V into each row's cell at positions[a].
+  int fused;
+  const uint16_t* k_new;      // [A,H_kv,D]
+  const uint16_t* v_new;      // [A,H_kv,D]
+  uint16_t* k_cache_w;        // the same caches, written
+  uint16_t* v_cache_w;
+  double inv_freq[kMaxHeadDim / 2];  // theta^(-2i/D), computed on the host in double
 };
 
 // Padded group size used by the decode kernels: the next power of two >= G.

@@ -19,39 +19,15 @@
 
 #include "kvgqa_internal.h"
 #include "ptx.cuh"
+#include "rope_math.cuh"
 
 namespace kvgqa {
 namespace {
-
-struct __align__(16) CosSin {
-  float ch, cl, sh, sl;  // cos = ch + cl, sin = sh + sl
-};
 
 // The cos/sin table is read eight consecutive entries at a time by lanes that
 // differ in which group of eight they read; one 16-byte pad after every eight
 // entries puts those lanes on different shared-memory banks.
 __device__ __forceinline__ int cs_slot(int i) { return i + (i >> 3); }
-
-// x1 * C - x2 * S with C, S given as hi+lo pairs.  Products are split exactly
-// with FMA; intrinsics keep the compiler from contracting them differently.
-__device__ __forceinline__ float rot_first(float x1, float x2, const CosSin& cs) {
-  const float p = __fmul_rn(x1, cs.ch);
-  const float pe = __fmaf_rn(x1, cs.ch, -p);
-  const float q = __fmul_rn(x2, cs.sh);
-  const float qe = __fmaf_rn(x2, cs.sh, -q);
-  const float lo = __fmaf_rn(x1, cs.cl, __fmaf_rn(-x2, cs.sl, __fsub_rn(pe, qe)));
-  return __fadd_rn(__fsub_rn(p, q), lo);
-}
-
-// x2 * C + x1 * S.
-__device__ __forceinline__ float rot_second(float x1, float x2, const CosSin& cs) {
-  const float p = __fmul_rn(x2, cs.ch);
-  const float pe = __fmaf_rn(x2, cs.ch, -p);
-  const float q = __fmul_rn(x1, cs.sh);
-  const float qe = __fmaf_rn(x1, cs.sh, -q);
-  const float lo = __fmaf_rn(x2, cs.cl, __fmaf_rn(x1, cs.sl, __fadd_rn(pe, qe)));
-  return __fadd_rn(__fadd_rn(p, q), lo);
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
@@ -104,23 +80,7 @@ __global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constan
     }
   }
 
-  for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-    // Cody-Waite reduction of the angle by 2*pi (2*pi split in two doubles,
-    // the products fused), so sincos only ever sees |r| <= pi.
-    constexpr double kTwoPiHi = 6.283185307179586232;    // nearest double to 2*pi
-    constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
-    const double phi = static_cast<double>(pos) * p.inv_freq[i];
-    const double k = rint(phi * 0.15915494309189535);    // 1 / (2*pi)
-    const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, phi));
-    double s, c;
-    sincos(r, &s, &c);
-    CosSin v;
-    v.ch = static_cast<float>(c);
-    v.cl = static_cast<float>(c - static_cast<double>(v.ch));
-    v.sh = static_cast<float>(s);
-    v.sl = static_cast<float>(s - static_cast<double>(v.sh));
-    cs[cs_slot(i)] = v;
-  }
+  for (int i = threadIdx.x; i < HALF; i += blockDim.x) cs[cs_slot(i)] = rope_cos_sin(pos, p.inv_freq[i]);
   __syncthreads();
 
   const int units = (p.H_q + p.H_kv) * RU + p.H_kv * VU;

@@ -201,3 +201,39 @@ def test_prefill_contract():
     a = prefill_args()
     a["k"] = torch.zeros(2, 8, 4, 64, dtype=torch.bfloat16)
     assert code_of(kv.prefill_gqa_cached_rows_out_, **a) == "EINVAL"
+
+
+def step_args(A=2, H_q=4, H_kv=2, D=64, S=4, L=32):
+    bf = torch.bfloat16
+    return dict(q=torch.zeros(A, H_q, D, dtype=bf), k=torch.zeros(A, H_kv, D, dtype=bf),
+                v=torch.zeros(A, H_kv, D, dtype=bf), positions=torch.zeros(A, dtype=torch.int32),
+                cache_rows=torch.arange(A, dtype=torch.int32), theta=1e4, scale=0.125,
+                k_cache=torch.zeros(S, H_kv, L, D, dtype=bf), v_cache=torch.zeros(S, H_kv, L, D, dtype=bf),
+                out=torch.zeros(A, H_q, D, dtype=bf), workspace=aligned_bytes(256))
+
+
+def test_decode_step_contract():
+    a = step_args()
+    a["out"] = a["q"]
+    assert code_of(kv.decode_step_out_, **a) == "EALIAS"
+    a = step_args()
+    a["out"] = a["k_cache"].view(-1)[: 2 * 4 * 64].view(2, 4, 64)
+    assert code_of(kv.decode_step_out_, **a) == "EALIAS"
+    a = step_args()
+    a["theta"] = -1.0
+    assert code_of(kv.decode_step_out_, **a) == "EINVAL"
+    a = step_args()
+    a["scale"] = float("inf")
+    assert code_of(kv.decode_step_out_, **a) == "EINVAL"
+    a = step_args(H_q=64, H_kv=2)               # G = 32 has no decode kernel
+    assert code_of(kv.decode_step_out_, **a) == "EUNSUPPORTED"
+    a = step_args()
+    a["v"] = torch.zeros(2, 3, 64, dtype=torch.bfloat16)
+    assert code_of(kv.decode_step_out_, **a) == "EINVAL"
+    a = step_args()
+    a["k"] = torch.zeros(2, 2, 64, dtype=torch.float32)
+    assert code_of(kv.decode_step_out_, **a) == "EDTYPE"
+    a = step_args(A=1100)
+    assert code_of(kv.decode_step_out_, **a) == "EUNSUPPORTED"
+    # every descriptor check passes: host tensors then fail the device check
+    assert code_of(kv.decode_step_out_, **step_args()) in ("ECUDA", "EDEVICE")
