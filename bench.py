@@ -250,12 +250,14 @@ def run_ours(args, rank, world, local):
     for _ in range(max(args.warmup, 3)):
         store()
         attend()
-        step()
+        if args.only is None:  # profiler runs (--only) launch only the kernels they capture
+            step()
     torch.cuda.synchronize()
     if args.only == "prefill":
         res = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
         return {"impl": "ours", "only": "prefill", "prefill": res} if rank == 0 else None
-    host_us = host_call_us([("step", step), ("store", store), ("attention", attend)], n=min(200, 10 * args.steps))
+    calls = [("store", store), ("attention", attend)] + ([("step", step)] if args.only is None else [])
+    host_us = host_call_us(calls, n=min(200, 10 * args.steps))
     if kv.kvgqa_read_status(ws1) or kv.kvgqa_read_status(ws2) or kv.kvgqa_read_status(ws3):
         raise RuntimeError("device status flags set during warm-up")
 
