@@ -54,7 +54,7 @@ __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const Co
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constant__ RopeStoreParams p,
+__global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_constant__ RopeStoreParams p,
                                                             int prefill) {
   constexpr int HALF = D / 2;
   constexpr int RU = D / 16;  // rotation units per head: 8 pairs each
@@ -83,44 +83,79 @@ __global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constan
   for (int i = threadIdx.x; i < HALF; i += blockDim.x) cs[cs_slot(i)] = rope_cos_sin(pos, p.inv_freq[i]);
   __syncthreads();
 
-  const int units = (p.H_q + p.H_kv) * RU + p.H_kv * VU;
-  for (int ti = 0; ti < ntok; ++ti) {
-    const int a = prefill ? ti : blockIdx.x;
-    const int row = p.cache_rows[a];
-    if (prefill && (row < 0 || row >= p.S)) {
-      if (threadIdx.x == 0) atomicOr(p.status, KVGQA_FLAG_ROW_RANGE);
-      continue;
+  // The work of this position: every token's rotation units (8 pairs of Q or
+  // K) and V copy units (16 bytes).  Each thread takes kBatch items at a time
+  // and issues all their loads before using any, so several DRAM round trips
+  // overlap (one at a time, the loop is bound by load latency, not bandwidth).
+  // Prefill tokens whose cache row is out of range are skipped and flagged.
+  constexpr int kBatch = 4;
+  if (prefill && blockIdx.x == 0) {
+    for (int a = threadIdx.x; a < ntok; a += blockDim.x) {
+      const int row = p.cache_rows[a];
+      if (row < 0 || row >= p.S) atomicOr(p.status, KVGQA_FLAG_ROW_RANGE);
     }
-    const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : static_cast<size_t>(a);
-    const size_t q_base = tok * p.H_q * D;
-    const size_t kv_base = tok * p.H_kv * D;
-    for (int r = threadIdx.x; r < units; r += blockDim.x) {
-      if (r < (p.H_q + p.H_kv) * RU) {
-        const int h = r / RU, c = r % RU;
-        const uint16_t* src;
-        uint16_t* dst;
-        if (h < p.H_q) {
-          src = p.q + q_base + static_cast<size_t>(h) * D;
-          dst = p.q_out + q_base + static_cast<size_t>(h) * D;
-        } else {
-          const int g = h - p.H_q;
-          src = p.k + kv_base + static_cast<size_t>(g) * D;
-          dst = p.k_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D;
-        }
-        const uint4 a8 = *reinterpret_cast<const uint4*>(src + c * 8);
-        const uint4 b8 = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
-        uint4 ya, yb;
-        rotate8(a8, b8, cs + cs_slot(c * 8), ya, yb);
-        *reinterpret_cast<uint4*>(dst + c * 8) = ya;
-        *reinterpret_cast<uint4*>(dst + HALF + c * 8) = yb;
+  }
+  const int rot_units = (p.H_q + p.H_kv) * RU;
+  const int n_rot = ntok * rot_units;
+  for (int base = threadIdx.x; base < n_rot; base += kBatch * blockDim.x) {
+    uint4 xa[kBatch], xb[kBatch];
+    uint16_t* dst[kBatch];
+    int cc[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int r = base + u * blockDim.x;
+      dst[u] = nullptr;
+      if (r >= n_rot) continue;
+      const int ti = r / rot_units, rr = r % rot_units;
+      const int a = prefill ? ti : blockIdx.x;
+      const int row = p.cache_rows[a];
+      if (row < 0 || row >= p.S) continue;
+      const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : static_cast<size_t>(a);
+      const int h = rr / RU, c = rr % RU;
+      const uint16_t* src;
+      if (h < p.H_q) {
+        src = p.q + (tok * p.H_q + h) * D;
+        dst[u] = p.q_out + (tok * p.H_q + h) * D;
       } else {
-        const int rr = r - (p.H_q + p.H_kv) * RU;
-        const int g = rr / VU, c = rr % VU;
-        const uint16_t* src = p.v + kv_base + static_cast<size_t>(g) * D + c * 8;
-        uint16_t* dst = p.v_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D + c * 8;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        const int g = h - p.H_q;
+        src = p.k + (tok * p.H_kv + g) * D;
+        dst[u] = p.k_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D;
       }
+      cc[u] = c;
+      xa[u] = *reinterpret_cast<const uint4*>(src + c * 8);
+      xb[u] = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
     }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (!dst[u]) continue;
+      uint4 ya, yb;
+      rotate8(xa[u], xb[u], cs + cs_slot(cc[u] * 8), ya, yb);
+      *reinterpret_cast<uint4*>(dst[u] + cc[u] * 8) = ya;
+      *reinterpret_cast<uint4*>(dst[u] + HALF + cc[u] * 8) = yb;
+    }
+  }
+  const int copy_units = p.H_kv * VU;
+  const int n_copy = ntok * copy_units;
+  for (int base = threadIdx.x; base < n_copy; base += kBatch * blockDim.x) {
+    uint4 x[kBatch];
+    uint16_t* dst[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int r = base + u * blockDim.x;
+      dst[u] = nullptr;
+      if (r >= n_copy) continue;
+      const int ti = r / copy_units, rr = r % copy_units;
+      const int a = prefill ? ti : blockIdx.x;
+      const int row = p.cache_rows[a];
+      if (row < 0 || row >= p.S) continue;
+      const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : static_cast<size_t>(a);
+      const int g = rr / VU, c = rr % VU;
+      dst[u] = p.v_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D + c * 8;
+      x[u] = *reinterpret_cast<const uint4*>(p.v + (tok * p.H_kv + g) * D + c * 8);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = x[u];
   }
 }
 
