@@ -91,7 +91,8 @@ typedef enum kvgqa_status {
   KVGQA_EALIAS = 5,      /* a written tensor overlaps another operand */
   KVGQA_EWORKSPACE = 6,  /* workspace too small or misaligned */
   KVGQA_ECUDA = 7,       /* a CUDA runtime call failed (message has the CUDA error) */
-  KVGQA_EUNSUPPORTED = 8 /* a legal shape this build has no kernel for (e.g. D = 96) */
+  KVGQA_EUNSUPPORTED = 8, /* a legal shape this build has no kernel for (e.g. D = 96) */
+  KVGQA_EFULL = 9         /* slot table: no free cache row */
 } kvgqa_status;
 
 /* Bits of the device status word (first 4 bytes of every workspace). */
@@ -276,6 +277,51 @@ kvgqa_status prefill_gqa_cached_rows_out_(const kvgqa_tensor* q, const kvgqa_ten
                                           double theta, float scale, const kvgqa_tensor* k_cache,
                                           const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
                                           const kvgqa_tensor* workspace, void* stream);
+
+/*
+ * Slot table and step metadata (host side, no kernels).
+ *
+ * microLLM-rocm ARCHITECTURE.md, section "Tensor ownership boundary": a
+ * continuous-batch scheduler owns the request-to-row map of the shared slot
+ * cache; it admits only at step boundaries, resets a row when its request
+ * ends (length, stop or cancel) and reuses the lowest free slot; CPU-origin
+ * token/position/row metadata of a step travel in one [3,A] host-to-device
+ * copy, split on the device into zero-copy views.
+ *
+ * kvgqa_slots_create    a table of num_slots rows of max_seq positions.
+ * kvgqa_slots_admit     lowest free row for `request`, whose row will hold
+ *                       prompt_len tokens (the prefill writes them); an
+ *                       admitted request keeps its row.  KVGQA_EFULL when no
+ *                       row is free.
+ * kvgqa_slots_release   free the request's row (reason 0 stop, 1 length,
+ *                       2 cancel); KVGQA_EINVAL for an unknown request.
+ * kvgqa_slots_step      one decode step for n admitted requests in the
+ *                       caller's order: writes token i, its position (the
+ *                       row's length) and its row into meta[0][i], meta[1][i],
+ *                       meta[2][i] of a host int32 [3][capacity] array, then
+ *                       advances every length; a row that becomes full is
+ *                       released (reason length) and flagged in finished[i]
+ *                       (may be NULL).  Unknown, repeated or full requests
+ *                       fail with KVGQA_EINVAL and change nothing.
+ * kvgqa_slots_query     rows in use, free rows, and releases per reason.
+ * kvgqa_metadata_upload one cudaMemcpyAsync of the whole host [3][capacity]
+ *                       int32 array (pinned memory for an asynchronous copy)
+ *                       into a device int32 tensor [3, capacity]; rows 1 and
+ *                       2 of that tensor, cut to the step's A entries, are the
+ *                       positions and cache_rows of the decode calls.
+ * The table is not thread-safe; one scheduler thread owns it.
+ */
+typedef struct kvgqa_slots kvgqa_slots;
+kvgqa_status kvgqa_slots_create(int32_t num_slots, int32_t max_seq, kvgqa_slots** out);
+kvgqa_status kvgqa_slots_destroy(kvgqa_slots* slots);
+kvgqa_status kvgqa_slots_admit(kvgqa_slots* slots, int64_t request, int32_t prompt_len, int32_t* row);
+kvgqa_status kvgqa_slots_release(kvgqa_slots* slots, int64_t request, int32_t reason);
+kvgqa_status kvgqa_slots_step(kvgqa_slots* slots, const int64_t* requests, const int32_t* tokens, int32_t n,
+                              int32_t* meta, int32_t capacity, uint8_t* finished);
+kvgqa_status kvgqa_slots_query(const kvgqa_slots* slots, int32_t* active, int32_t* free_rows,
+                               int64_t released[3]);
+kvgqa_status kvgqa_metadata_upload(const int32_t* host_meta, int32_t capacity, const kvgqa_tensor* device_meta,
+                                   void* stream);
 
 /* Opt-in: synchronise `stream`, return the status word of `workspace` in
  * *flags (KVGQA_FLAG_* bits; 0 = every device-side check passed) and clear it.

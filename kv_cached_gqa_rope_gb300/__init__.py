@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_PKG_DIR, "libkvgqa.so")
 
 KVGQA_BF16, KVGQA_I32, KVGQA_F32, KVGQA_U8 = 1, 2, 3, 4
 STATUS_NAMES = {0: "OK", 1: "EINVAL", 2: "EDTYPE", 3: "ELAYOUT", 4: "EDEVICE", 5: "EALIAS",
-                6: "EWORKSPACE", 7: "ECUDA", 8: "EUNSUPPORTED"}
+                6: "EWORKSPACE", 7: "ECUDA", 8: "EUNSUPPORTED", 9: "EFULL"}
 FLAG_POSITION_RANGE, FLAG_ROW_RANGE, FLAG_TIMEOUT = 0x1, 0x2, 0x4
 STATUS_BYTES = 256
 _DTYPES = {torch.bfloat16: KVGQA_BF16, torch.int32: KVGQA_I32, torch.float32: KVGQA_F32,
@@ -75,6 +75,18 @@ def _load():
     lib.decode_step_workspace_size.restype = st
     lib.decode_step_out_.argtypes = [P, P, P, P, P, ctypes.c_double, ctypes.c_float, P, P, P, P, ctypes.c_void_p]
     lib.decode_step_out_.restype = st
+    VP = ctypes.c_void_p
+    lib.kvgqa_slots_create.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(VP)]
+    lib.kvgqa_slots_destroy.argtypes = [VP]
+    lib.kvgqa_slots_admit.argtypes = [VP, ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+    lib.kvgqa_slots_release.argtypes = [VP, ctypes.c_int64, ctypes.c_int32]
+    lib.kvgqa_slots_step.argtypes = [VP, VP, VP, ctypes.c_int32, VP, ctypes.c_int32, VP]
+    lib.kvgqa_slots_query.argtypes = [VP, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                      ctypes.POINTER(ctypes.c_int64)]
+    lib.kvgqa_metadata_upload.argtypes = [VP, ctypes.c_int32, P, VP]
+    for name in ("kvgqa_slots_create", "kvgqa_slots_destroy", "kvgqa_slots_admit", "kvgqa_slots_release",
+                 "kvgqa_slots_step", "kvgqa_slots_query", "kvgqa_metadata_upload"):
+        getattr(lib, name).restype = st
     lib.kvgqa_read_status.argtypes = [P, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.kvgqa_read_status.restype = st
     return lib
@@ -87,7 +99,8 @@ EXPORTED_SYMBOLS = ("kvgqa_abi_version", "kvgqa_last_error", "rope_kv_store_work
                     "cached_gqa_attention_out_", "prefill_gqa_cached_rows_workspace_size",
                     "prefill_gqa_cached_rows_out_", "kvgqa_read_status",
                     "cached_gqa_attention_static_scratch_out_", "decode_step_workspace_size",
-                    "decode_step_out_")
+                    "decode_step_out_", "kvgqa_slots_create", "kvgqa_slots_destroy", "kvgqa_slots_admit",
+                    "kvgqa_slots_release", "kvgqa_slots_step", "kvgqa_slots_query", "kvgqa_metadata_upload")
 
 
 def library() -> ctypes.CDLL:
@@ -264,3 +277,82 @@ def new_workspace(nbytes: int, device=None) -> torch.Tensor:
     """A zero-filled workspace (status word clear), 256-byte aligned."""
     return torch.zeros(max(int(nbytes), STATUS_BYTES), dtype=torch.uint8,
                        device=device if device is not None else "cuda")
+
+
+# ---------------------------------------------------------------------- slots
+STOP, LENGTH, CANCEL = 0, 1, 2
+
+
+class SlotTable:
+    """The library's host slot table of the shared KV cache (which request owns
+    which cache row, and how many tokens that row holds).  Lowest free row on
+    admission, rows freed on stop / length / cancel, one decode step packs the
+    [3, capacity] token/position/row metadata (see include/kvgqa.h)."""
+
+    def __init__(self, num_slots: int, max_seq: int):
+        h = ctypes.c_void_p()
+        _check(_lib.kvgqa_slots_create(num_slots, max_seq, ctypes.byref(h)))
+        self._h = h
+        self.num_slots, self.max_seq = num_slots, max_seq
+
+    def close(self):
+        if self._h:
+            _lib.kvgqa_slots_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def admit(self, request: int, prompt_len: int) -> int:
+        row = ctypes.c_int32()
+        _check(_lib.kvgqa_slots_admit(self._h, int(request), int(prompt_len), ctypes.byref(row)))
+        return row.value
+
+    def release(self, request: int, reason: int = STOP) -> None:
+        _check(_lib.kvgqa_slots_release(self._h, int(request), int(reason)))
+
+    def step(self, requests, tokens, meta: torch.Tensor):
+        """Pack one decode step into the host int32 tensor `meta` [3, capacity];
+        returns (A, finished) where finished[i] tells whether request i's row
+        became full and was released."""
+        import numpy as np
+        if meta.dtype != torch.int32 or meta.dim() != 2 or meta.shape[0] != 3 or meta.device.type != "cpu" \
+                or not meta.is_contiguous():
+            raise ValueError("meta must be a contiguous host int32 tensor [3, capacity]")
+        req = np.ascontiguousarray(np.asarray(requests, dtype=np.int64))
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        if tok.shape != req.shape:
+            raise ValueError("one token per request")
+        fin = np.zeros(len(req), dtype=np.uint8)
+        _check(_lib.kvgqa_slots_step(self._h, req.ctypes.data, tok.ctypes.data, len(req), meta.data_ptr(),
+                                     meta.shape[1], fin.ctypes.data))
+        return len(req), fin.astype(bool)
+
+    def query(self):
+        active, free = ctypes.c_int32(), ctypes.c_int32()
+        rel = (ctypes.c_int64 * 3)()
+        _check(_lib.kvgqa_slots_query(self._h, ctypes.byref(active), ctypes.byref(free), rel))
+        return {"active": active.value, "free": free.value,
+                "released": {"stop": rel[0], "length": rel[1], "cancel": rel[2]}}
+
+
+class StepMetadata:
+    """Pinned host [3, capacity] int32 metadata and its device copy: one
+    host-to-device copy per step, then zero-copy device views of the first A
+    entries of each row (tokens, positions, cache_rows)."""
+
+    def __init__(self, capacity: int, device=None):
+        self.capacity = capacity
+        self.host = torch.zeros(3, capacity, dtype=torch.int32).pin_memory()
+        self.device = torch.zeros(3, capacity, dtype=torch.int32,
+                                  device=device if device is not None else "cuda")
+        self._desc = describe(self.device)
+
+    def upload(self, A: int, stream=None):
+        _check(_lib.kvgqa_metadata_upload(self.host.data_ptr(), self.capacity, _ref(self._desc), _stream(stream)))
+        d = self.device
+        return d[0, :A], d[1, :A], d[2, :A]
+

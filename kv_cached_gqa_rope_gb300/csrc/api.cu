@@ -18,6 +18,7 @@
 
 #include "kvgqa.h"
 #include "kvgqa_internal.h"
+#include "slots.h"
 
 namespace {
 
@@ -531,6 +532,79 @@ kvgqa_status prefill_gqa_cached_rows_out_(const kvgqa_tensor* q, const kvgqa_ten
     pp.D = (int)D; pp.S = (int)S; pp.max_seq = (int)max_seq;
     pp.scale_log2 = scale * 1.4426950408889634f;
     check_cuda(kvgqa::launch_prefill_attention(pp, st), "prefill attention launch");
+  });
+}
+
+struct kvgqa_slots {
+  kvgqa::SlotTable table;
+};
+
+kvgqa_status kvgqa_slots_create(int32_t num_slots, int32_t max_seq, kvgqa_slots** out) {
+  return guarded([&] {
+    if (!out) fail(KVGQA_EINVAL, "out: null");
+    if (num_slots <= 0 || max_seq <= 0) fail(KVGQA_EINVAL, "num_slots and max_seq must be positive");
+    *out = new kvgqa_slots{kvgqa::SlotTable(num_slots, max_seq)};
+  });
+}
+
+kvgqa_status kvgqa_slots_destroy(kvgqa_slots* slots) {
+  return guarded([&] { delete slots; });
+}
+
+kvgqa_status kvgqa_slots_admit(kvgqa_slots* slots, int64_t request, int32_t prompt_len, int32_t* row) {
+  return guarded([&] {
+    if (!slots || !row) fail(KVGQA_EINVAL, "null argument");
+    if (prompt_len < 0 || prompt_len > slots->table.max_seq())
+      fail(KVGQA_EINVAL, "prompt_len %d outside [0, max_seq=%d]", prompt_len, slots->table.max_seq());
+    const int r = slots->table.admit(request, prompt_len);
+    if (r < 0) fail(KVGQA_EFULL, "no free cache row (%d rows in use)", slots->table.active());
+    *row = r;
+  });
+}
+
+kvgqa_status kvgqa_slots_release(kvgqa_slots* slots, int64_t request, int32_t reason) {
+  return guarded([&] {
+    if (!slots) fail(KVGQA_EINVAL, "null argument");
+    if (reason < 0 || reason > 2) fail(KVGQA_EINVAL, "reason must be 0 (stop), 1 (length) or 2 (cancel)");
+    if (!slots->table.release(request, static_cast<kvgqa::SlotTable::Reason>(reason)))
+      fail(KVGQA_EINVAL, "request %lld holds no row", (long long)request);
+  });
+}
+
+kvgqa_status kvgqa_slots_step(kvgqa_slots* slots, const int64_t* requests, const int32_t* tokens, int32_t n,
+                              int32_t* meta, int32_t capacity, uint8_t* finished) {
+  return guarded([&] {
+    if (!slots || !meta || (n > 0 && !requests)) fail(KVGQA_EINVAL, "null argument");
+    if (n < 0 || n > capacity) fail(KVGQA_EINVAL, "n=%d must lie in [0, capacity=%d]", n, capacity);
+    const int bad = slots->table.step(requests, tokens, n, meta, capacity, finished);
+    if (bad >= 0)
+      fail(KVGQA_EINVAL, "request %lld (entry %d) is not admitted, is repeated, or its row is full",
+           (long long)requests[bad], bad);
+  });
+}
+
+kvgqa_status kvgqa_slots_query(const kvgqa_slots* slots, int32_t* active, int32_t* free_rows, int64_t released[3]) {
+  return guarded([&] {
+    if (!slots) fail(KVGQA_EINVAL, "null argument");
+    if (active) *active = slots->table.active();
+    if (free_rows) *free_rows = slots->table.num_slots() - slots->table.active();
+    if (released)
+      for (int i = 0; i < 3; ++i) released[i] = slots->table.released(static_cast<kvgqa::SlotTable::Reason>(i));
+  });
+}
+
+kvgqa_status kvgqa_metadata_upload(const int32_t* host_meta, int32_t capacity, const kvgqa_tensor* device_meta,
+                                   void* stream) {
+  return guarded([&] {
+    if (!host_meta) fail(KVGQA_EINVAL, "host_meta: null");
+    if (capacity <= 0) fail(KVGQA_EINVAL, "capacity must be positive");
+    View vm = check_tensor("device_meta", device_meta, 2, KVGQA_I32, 4);
+    require_shape(vm, {3, capacity});
+    const int dev = current_device();
+    check_device({&vm}, dev);
+    check_cuda(cudaMemcpyAsync(device_meta->data, host_meta, sizeof(int32_t) * 3 * static_cast<size_t>(capacity),
+                               cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)),
+               "metadata copy");
   });
 }
 
