@@ -242,3 +242,72 @@ def prefill_gqa_cached_rows(q, k, v, cache_rows, theta, scale, k_cache, v_cache,
             out[a, t, h] = prefill_attention_one(q_rot[a, t, h], kc[rows[a], g, :T],
                                                  vc[rows[a], g, :T], t, scale)
     return q_rot, out, kc, vc
+
+
+def prefill_varlen_gqa_cached_rows(q, k, v, offsets, lengths, cache_rows, theta, scale, k_cache, v_cache,
+                                   select=None):
+    """Prefill of A prompts of different lengths into rows that may already
+    hold a prefix (chunked prefill).
+
+    microLLM-rocm ARCHITECTURE.md, "Tensor ownership boundary" (prompts of
+    other lengths form separate equal-length groups there; here one call takes
+    them together) and "Attention layout boundary" (RoPE takes a nonnegative
+    position offset).  Prompt a has lengths[a] tokens (the first ones of the
+    padded [A, T] batch); token t sits at position p = offsets[a] + t of row
+    cache_rows[a].  Q and K are rotated at p, rotated K and raw V are stored at
+    (row, :, p, :), and query (a, t, h) attends causally over keys 0..p of its
+    row: the row's existing prefix [0, offsets[a]) and the prompt's tokens up
+    to itself.  Outputs for t >= lengths[a] are NaN; nothing else in the
+    caches changes.
+
+    Returns (q_rot [A, T, H_q, D] bits (rows past a prompt's length 0),
+    out float64 [A, T, H_q, D], k_cache', v_cache').  ``select`` optionally
+    lists the (a, t, h) outputs to compute.
+    """
+    q = np.asarray(q, dtype=np.uint16)
+    k = np.asarray(k, dtype=np.uint16)
+    v = np.asarray(v, dtype=np.uint16)
+    A, T, H_q, D = q.shape
+    S, H_kv, max_seq, _ = k_cache.shape
+    G = H_q // H_kv
+    rows = np.asarray(cache_rows, dtype=np.int64)
+    off = np.asarray(offsets, dtype=np.int64)
+    lens = np.asarray(lengths, dtype=np.int64)
+    if np.any((rows < 0) | (rows >= S)) or len(set(rows.tolist())) != len(rows):
+        raise ValueError("cache rows must be distinct and in range")
+    if np.any(lens < 0) or np.any(lens > T) or np.any(off < 0) or np.any(off + lens > max_seq):
+        raise ValueError("offsets/lengths out of range")
+    q_rot = np.zeros_like(q)
+    kc = np.array(k_cache, dtype=np.uint16, copy=True)
+    vc = np.array(v_cache, dtype=np.uint16, copy=True)
+    for a in range(A):
+        L, o = int(lens[a]), int(off[a])
+        pos = o + np.arange(L)
+        q_rot[a, :L] = rope_split_half_bf16(q[a, :L], pos[:, None], theta)
+        k_rot = rope_split_half_bf16(k[a, :L], pos[:, None], theta)
+        kc[rows[a], :, o:o + L, :] = np.transpose(k_rot, (1, 0, 2))
+        vc[rows[a], :, o:o + L, :] = np.transpose(v[a, :L], (1, 0, 2))
+    out = np.full((A, T, H_q, D), np.nan)
+    if select is None:
+        for a in range(A):
+            L, o = int(lens[a]), int(off[a])
+            if L == 0:
+                continue
+            n = o + L
+            mask = np.arange(n)[None, :] <= (o + np.arange(L))[:, None]   # key j visible to query t
+            for h in range(H_q):
+                g = h // G
+                Q = bf16_to_f64(q_rot[a, :L, h])
+                K = bf16_to_f64(kc[rows[a], g, :n])
+                V = bf16_to_f64(vc[rows[a], g, :n])
+                s = np.where(mask, (Q @ K.T) * scale, -np.inf)
+                out[a, :L, h] = softmax(s) @ V
+    else:
+        for a, t, h in select:
+            if t >= lens[a]:
+                continue
+            g = h // G
+            p = int(off[a]) + t
+            out[a, t, h] = cached_gqa_attention_one(bf16_to_f64(q_rot[a, t, h]), bf16_to_f64(kc[rows[a], g, :p + 1]),
+                                                    bf16_to_f64(vc[rows[a], g, :p + 1]), scale)
+    return q_rot, out, kc, vc

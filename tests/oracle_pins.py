@@ -306,6 +306,61 @@ def check_prefill_select_matches_full(o):
         assert np.allclose(part[a, t, h], full[a, t, h], rtol=0, atol=1e-14)
 
 
+def check_varlen_equal_lengths_is_prefill(o):
+    """Zero offsets and full lengths: the equal-length prefill."""
+    q, k, v, kc, vc = _prefill_case(seed=70)
+    rows = np.array([1, 3])
+    A, T = q.shape[:2]
+    qr1, out1, kc1, vc1 = o.prefill_gqa_cached_rows(q, k, v, rows, 16.0, 0.4, kc, vc)
+    qr2, out2, kc2, vc2 = o.prefill_varlen_gqa_cached_rows(q, k, v, np.zeros(A, int), np.full(A, T), rows, 16.0,
+                                                            0.4, kc, vc)
+    assert np.array_equal(qr1, qr2) and np.array_equal(kc1, kc2) and np.array_equal(vc1, vc2)
+    assert np.allclose(out1, out2, rtol=0, atol=1e-13)
+
+
+def check_varlen_length_one_is_decode(o):
+    """One token at offset p: the decode step at position p (store, then
+    attention over keys 0..p of the row)."""
+    A, T, H_q, H_kv, D, S, L = 3, 4, 4, 2, 8, 5, 12
+    q, k, v, _, _ = _prefill_case(A, T, H_q, H_kv, D, S, L, seed=80)
+    kc = random_bf16_bits((S, H_kv, L, D), seed=81)
+    vc = random_bf16_bits((S, H_kv, L, D), seed=82)
+    rows = np.array([4, 0, 2])
+    offs = np.array([0, 5, 11])
+    qr, out, kc2, vc2 = o.prefill_varlen_gqa_cached_rows(q, k, v, offs, np.ones(A, int), rows, 16.0, 0.4, kc, vc)
+    q_rot, kc3, vc3 = o.rope_kv_store(q[:, 0], k[:, 0], v[:, 0], offs, rows, 16.0, kc, vc)
+    ref = o.cached_gqa_attention(q_rot, kc3, vc3, offs, rows, 0.4)
+    assert np.array_equal(kc2, kc3) and np.array_equal(vc2, vc3) and np.array_equal(qr[:, 0], q_rot)
+    assert np.allclose(out[:, 0], ref, rtol=0, atol=1e-13)
+    assert np.all(np.isnan(out[:, 1:]))
+
+
+def check_varlen_chunks_compose(o):
+    """Prefilling L1 tokens and then the next L2 at offset L1 gives the same
+    cache and the same outputs as one prefill of L1 + L2 tokens; prompts of
+    different lengths in one call behave as separate calls."""
+    A, T, H_q, H_kv, D, S, L = 2, 7, 4, 2, 8, 4, 12
+    q, k, v, kc, vc = _prefill_case(A, T, H_q, H_kv, D, S, L, seed=90)
+    rows = np.array([2, 1])
+    _, out_full, kcf, vcf = o.prefill_gqa_cached_rows(q, k, v, rows, 16.0, 0.4, kc, vc)
+    L1 = np.array([3, 5])
+    _, out1, kc1, vc1 = o.prefill_varlen_gqa_cached_rows(q, k, v, np.zeros(A, int), L1, rows, 16.0, 0.4, kc, vc)
+    q2 = np.zeros_like(q); k2 = np.zeros_like(k); v2 = np.zeros_like(v)
+    for a in range(A):
+        n = T - L1[a]
+        q2[a, :n], k2[a, :n], v2[a, :n] = q[a, L1[a]:], k[a, L1[a]:], v[a, L1[a]:]
+    _, out2, kc2, vc2 = o.prefill_varlen_gqa_cached_rows(q2, k2, v2, L1, T - L1, rows, 16.0, 0.4, kc1, vc1)
+    assert np.array_equal(kc2, kcf) and np.array_equal(vc2, vcf)
+    for a in range(A):
+        assert np.allclose(out1[a, :L1[a]], out_full[a, :L1[a]], rtol=0, atol=1e-13)
+        assert np.allclose(out2[a, :T - L1[a]], out_full[a, L1[a]:], rtol=0, atol=1e-13)
+    # bytes past each prompt's tokens untouched
+    untouched = np.ones(kc.shape[:3], dtype=bool)
+    for a in range(A):
+        untouched[rows[a], :, :L1[a]] = False
+    assert np.array_equal(kc1[untouched], kc[untouched]) and np.array_equal(vc1[untouched], vc[untouched])
+
+
 ALL_CHECKS = [
     check_bf16_matches_torch_rounding, check_bf16_single_rounding, check_bf16_roundtrip,
     check_rope_frequencies, check_rope_pairing_and_direction, check_rope_identity_at_zero,
@@ -314,5 +369,6 @@ ALL_CHECKS = [
     check_equal_scores_give_mean, check_two_key_logistic, check_softmax_normalised,
     check_brute_force_tiny, check_gqa_equals_repeated_mha, check_prefix_is_inclusive_and_bounded,
     check_prefill_rows_and_first_position, check_prefill_causal, check_prefill_matches_decode,
-    check_prefill_select_matches_full,
+    check_prefill_select_matches_full, check_varlen_equal_lengths_is_prefill, check_varlen_length_one_is_decode,
+    check_varlen_chunks_compose,
 ]

@@ -132,10 +132,40 @@ def mutant_softmax_no_shift_sign(m):
     m.softmax = lambda s: np.exp(-s) / np.sum(np.exp(-s), axis=-1, keepdims=True)
 
 
+def mutant_varlen_mask_ignores_offset(m):
+    """The causal mask taken relative to the prompt (query t sees keys 0..t)
+    instead of the absolute position offset + t."""
+    orig = m.prefill_varlen_gqa_cached_rows
+
+    def varlen(q, k, v, offsets, lengths, cache_rows, theta, scale, k_cache, v_cache, select=None):
+        q_rot, out, kc, vc = orig(q, k, v, offsets, lengths, cache_rows, theta, scale, k_cache, v_cache, select)
+        A, T, H_q, D = q.shape
+        G = H_q // k_cache.shape[1]
+        for a in range(A):
+            for t in range(int(lengths[a])):
+                for h in range(H_q):
+                    r, g = int(cache_rows[a]), h // G
+                    out[a, t, h] = m.cached_gqa_attention_one(m.bf16_to_f64(q_rot[a, t, h]),
+                                                              m.bf16_to_f64(kc[r, g, : t + 1]),
+                                                              m.bf16_to_f64(vc[r, g, : t + 1]), scale)
+        return q_rot, out, kc, vc
+    m.prefill_varlen_gqa_cached_rows = varlen
+
+
+def mutant_varlen_rope_at_t(m):
+    """Tokens rotated at their index in the prompt, not at offset + index."""
+    orig = m.prefill_varlen_gqa_cached_rows
+
+    def varlen(q, k, v, offsets, lengths, *rest, **kw):
+        return orig(q, k, v, np.zeros_like(np.asarray(offsets)), lengths, *rest, **kw)
+    m.prefill_varlen_gqa_cached_rows = varlen
+
+
 MUTANTS = [mutant_rope_direction, mutant_rope_interleaved, mutant_rope_frequency,
            mutant_gqa_modulo, mutant_exclusive_prefix, mutant_scale_ignored,
            mutant_double_rounding, mutant_prefill_not_causal, mutant_store_row_index,
-           mutant_prefill_offset, mutant_softmax_no_shift_sign]
+           mutant_prefill_offset, mutant_softmax_no_shift_sign, mutant_varlen_mask_ignores_offset,
+           mutant_varlen_rope_at_t]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
