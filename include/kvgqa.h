@@ -1,7 +1,7 @@
 /*
  * kvgqa.h -- C ABI of the GB300 (sm_103a) cached GQA + RoPE decode/prefill path.
  *
- * One shared library, libkvgqa.so, exports the three operations of the
+ * One shared library, libkvgqa.so, exports the operations of the
  * positions-aware active-batch decode step over a shared slot KV cache and of
  * its dense case, the equal-length prefill into empty cache rows
  * (microLLM-rocm ARCHITECTURE.md, section "Tensor ownership boundary"):
@@ -12,6 +12,8 @@
  *                                 cached prefix (split-K + combine)
  *   prefill_gqa_cached_rows_out_  A prompts of T tokens: RoPE, store into the
  *                                 target empty rows, causal GQA attention
+ *   prefill_varlen_gqa_cached_rows_out_  prompts of different lengths at their
+ *                                 own offsets (chunked prefill), same steps
  *
  * Boundary conventions (same page, sections "Tensor ownership boundary" and
  * "Stable integration boundary"):
@@ -277,6 +279,45 @@ kvgqa_status prefill_gqa_cached_rows_out_(const kvgqa_tensor* q, const kvgqa_ten
                                           double theta, float scale, const kvgqa_tensor* k_cache,
                                           const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
                                           const kvgqa_tensor* workspace, void* stream);
+
+/*
+ * prefill_varlen_gqa_cached_rows_out_ -- prompts of different lengths, each
+ * at its own position offset, into rows that may already hold a prefix
+ * (chunked prefill).
+ *
+ * ARCHITECTURE.md, "Tensor ownership boundary", keeps prompts of different
+ * lengths in separate equal-length groups; this call runs them in one launch.
+ * Its RoPE takes a nonnegative position offset per prompt ("Attention layout
+ * boundary").  Prompt a holds len = lengths[a] tokens, padded to T in q/k/v,
+ * at positions off = offsets[a] .. off+len-1 of row r = cache_rows[a]:
+ *   k_cache[r, g, off+t, :] = RoPE(k[a, t, g, :], off+t),
+ *   v_cache[r, g, off+t, :] = v[a, t, g, :]            for t < len;
+ *   out[a, t, h, :] = GQA attention of RoPE(q[a,t,h,:], off+t) over cached
+ *   positions 0..off+t of row r (the prefix the row held, then the prompt's
+ *   own keys up to t), KV head floor(h/G), scores scaled by `scale`.
+ * Rows t >= len of out are not written.  offsets = 0, lengths = T is
+ * prefill_gqa_cached_rows_out_; len = 1 is one decode token at position off;
+ * prefilling a prompt in consecutive chunks equals prefilling it at once.
+ *
+ *   q [A,T,H_q,D], k/v [A,T,H_kv,D] bf16 (BTHD, T = the longest prompt or more)
+ *   offsets, lengths, cache_rows [A] int32 (read)
+ *   theta > 0, scale finite
+ *   k_cache/v_cache [S,H_kv,max_seq,D] bf16 with T <= max_seq (rows r written)
+ *   out [A,T,H_q,D] bf16 (rows t < lengths[a] written)
+ *   workspace >= prefill_gqa_cached_rows_workspace_size(...) bytes, 256-byte aligned
+ * Device-side checks: a prompt with len outside [0, T], off < 0 or
+ * off + len > max_seq sets KVGQA_FLAG_POSITION_RANGE, one whose row is outside
+ * [0, S) sets KVGQA_FLAG_ROW_RANGE; neither is read or written.  len = 0 is a
+ * no-op for that prompt.
+ * Preconditions: cache_rows distinct; positions 0..off-1 of each row hold the
+ * prefix the prompt continues.  Cells past off+len are never read.
+ */
+kvgqa_status prefill_varlen_gqa_cached_rows_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
+                                                 const kvgqa_tensor* v, const kvgqa_tensor* offsets,
+                                                 const kvgqa_tensor* lengths, const kvgqa_tensor* cache_rows,
+                                                 double theta, float scale, const kvgqa_tensor* k_cache,
+                                                 const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
+                                                 const kvgqa_tensor* workspace, void* stream);
 
 /*
  * Slot table and step metadata (host side, no kernels).

@@ -11,6 +11,8 @@ Functions keep the names of the C entry points:
     rope_kv_store_out_(q, k, v, positions, cache_rows, theta, q_out, k_cache, v_cache, workspace)
     cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_rows, scale, out, workspace)
     prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_cache, out, workspace)
+    prefill_varlen_gqa_cached_rows_out_(q, k, v, offsets, lengths, cache_rows, theta, scale,
+                                        k_cache, v_cache, out, workspace)
 
 plus the workspace-size queries and ``kvgqa_read_status``.  Shapes, layouts
 and the meaning of every argument are documented in ``include/kvgqa.h``.
@@ -69,6 +71,9 @@ def _load():
     lib.prefill_gqa_cached_rows_workspace_size.restype = st
     lib.prefill_gqa_cached_rows_out_.argtypes = [P, P, P, P, ctypes.c_double, ctypes.c_float, P, P, P, P, ctypes.c_void_p]
     lib.prefill_gqa_cached_rows_out_.restype = st
+    lib.prefill_varlen_gqa_cached_rows_out_.argtypes = [P, P, P, P, P, P, ctypes.c_double, ctypes.c_float,
+                                                        P, P, P, P, ctypes.c_void_p]
+    lib.prefill_varlen_gqa_cached_rows_out_.restype = st
     lib.cached_gqa_attention_static_scratch_out_.argtypes = [P, P, P, P, P, ctypes.c_float, P, ctypes.c_void_p]
     lib.cached_gqa_attention_static_scratch_out_.restype = st
     lib.decode_step_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
@@ -100,7 +105,8 @@ EXPORTED_SYMBOLS = ("kvgqa_abi_version", "kvgqa_last_error", "rope_kv_store_work
                     "prefill_gqa_cached_rows_out_", "kvgqa_read_status",
                     "cached_gqa_attention_static_scratch_out_", "decode_step_workspace_size",
                     "decode_step_out_", "kvgqa_slots_create", "kvgqa_slots_destroy", "kvgqa_slots_admit",
-                    "kvgqa_slots_release", "kvgqa_slots_step", "kvgqa_slots_query", "kvgqa_metadata_upload")
+                    "kvgqa_slots_release", "kvgqa_slots_step", "kvgqa_slots_query", "kvgqa_metadata_upload",
+                    "prefill_varlen_gqa_cached_rows_out_")
 
 
 def library() -> ctypes.CDLL:
@@ -214,6 +220,17 @@ def prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_c
     outs = [describe(t) for t in (k_cache, v_cache, out, workspace)]
     _check(_lib.prefill_gqa_cached_rows_out_(*map(_ref, ds), float(theta), float(scale),
                                              *map(_ref, outs), _stream(stream)))
+
+
+def prefill_varlen_gqa_cached_rows_out_(q, k, v, offsets, lengths, cache_rows, theta, scale, k_cache, v_cache,
+                                        out, workspace, stream=None) -> None:
+    """Prompts of lengths[a] tokens (padded to T) at positions offsets[a]..
+    of rows that may already hold a prefix; the workspace is the one of
+    prefill_gqa_cached_rows_workspace_size."""
+    ds = [describe(t) for t in (q, k, v, offsets, lengths, cache_rows)]
+    outs = [describe(t) for t in (k_cache, v_cache, out, workspace)]
+    _check(_lib.prefill_varlen_gqa_cached_rows_out_(*map(_ref, ds), float(theta), float(scale),
+                                                    *map(_ref, outs), _stream(stream)))
 
 
 class Prepared:

@@ -255,7 +255,7 @@ kvgqa_status rope_kv_store_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
     p.A = (int)A; p.T = 1; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.D = (int)D;
     p.S = (int)S; p.max_seq = (int)max_seq;
     fill_inv_freq(p.inv_freq, (int)D, theta);
-    check_cuda(kvgqa::launch_rope_kv_store(p, false, static_cast<cudaStream_t>(stream)),
+    check_cuda(kvgqa::launch_rope_kv_store(p, 0, static_cast<cudaStream_t>(stream)),
                "rope_kv_store launch");
   });
 }
@@ -471,67 +471,117 @@ kvgqa_status prefill_gqa_cached_rows_workspace_size(int64_t A, int64_t T, int64_
   });
 }
 
+}  // extern "C"
+
+namespace {
+
+// The equal-length prefill (offsets = lengths = nullptr) and the prefill of
+// prompts of different lengths at position offsets share this body.
+void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tensor* v, const kvgqa_tensor* offsets,
+                  const kvgqa_tensor* lengths, const kvgqa_tensor* cache_rows, double theta, float scale,
+                  const kvgqa_tensor* k_cache, const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
+                  const kvgqa_tensor* workspace, void* stream) {
+  if (!q || !k_cache) fail(KVGQA_EINVAL, "null descriptor");
+  if (q->ndim != 4 || k_cache->ndim != 4) fail(KVGQA_EINVAL, "q must be [A,T,H_q,D], caches [S,H_kv,max_seq,D]");
+  const bool varlen = offsets != nullptr || lengths != nullptr;
+  const int64_t A = q->shape[0], T = q->shape[1], H_q = q->shape[2], D = q->shape[3];
+  const int64_t S = k_cache->shape[0], H_kv = k_cache->shape[1], max_seq = k_cache->shape[2];
+  check_head_dim(D);
+  check_heads(H_q, H_kv);
+  check_theta(theta);
+  if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
+  if (T > max_seq) fail(KVGQA_EINVAL, "T=%lld exceeds max_seq=%lld", (long long)T, (long long)max_seq);
+  if (A * T > 0x7fffffffll) fail(KVGQA_EUNSUPPORTED, "A*T must stay below 2^31");
+  View vq = check_tensor("q", q, 4, KVGQA_BF16, 16);
+  View vk = check_tensor("k", k, 4, KVGQA_BF16, 16);
+  View vv = check_tensor("v", v, 4, KVGQA_BF16, 16);
+  View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
+  View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
+  View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+  View vo = check_tensor("out", out, 4, KVGQA_BF16, 16);
+  require_shape(vk, {A, T, H_kv, D});
+  require_shape(vv, {A, T, H_kv, D});
+  require_shape(vr, {A});
+  require_shape(vvc, {S, H_kv, max_seq, D});
+  require_shape(vo, {A, T, H_q, D});
+  View voff{}, vlen{};
+  if (varlen) {
+    voff = check_tensor("offsets", offsets, 1, KVGQA_I32, 4);
+    vlen = check_tensor("lengths", lengths, 1, KVGQA_I32, 4);
+    require_shape(voff, {A});
+    require_shape(vlen, {A});
+  }
+  const size_t need = KVGQA_STATUS_BYTES + static_cast<size_t>(A) * T * H_q * D * 2;
+  View vws = check_workspace(workspace, need);
+  if (varlen) {
+    check_no_alias({&vkc, &vvc, &vo, &vws}, {&vq, &vk, &vv, &vr, &voff, &vlen, &vkc, &vvc, &vo, &vws});
+  } else {
+    check_no_alias({&vkc, &vvc, &vo, &vws}, {&vq, &vk, &vv, &vr, &vkc, &vvc, &vo, &vws});
+  }
+  const int dev = current_device();
+  if (varlen) {
+    check_device({&vq, &vk, &vv, &vr, &voff, &vlen, &vkc, &vvc, &vo, &vws}, dev);
+  } else {
+    check_device({&vq, &vk, &vv, &vr, &vkc, &vvc, &vo, &vws}, dev);
+  }
+  if (A == 0 || T == 0) return;
+  kvgqa::RopeStoreParams rp{};
+  unsigned char* ws = static_cast<unsigned char*>(workspace->data);
+  uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + KVGQA_STATUS_BYTES);
+  rp.q = static_cast<const uint16_t*>(q->data);
+  rp.k = static_cast<const uint16_t*>(k->data);
+  rp.v = static_cast<const uint16_t*>(v->data);
+  rp.positions = nullptr;
+  rp.cache_rows = static_cast<const int32_t*>(cache_rows->data);
+  rp.offsets = varlen ? static_cast<const int32_t*>(offsets->data) : nullptr;
+  rp.lengths = varlen ? static_cast<const int32_t*>(lengths->data) : nullptr;
+  rp.q_out = q_rot;
+  rp.k_cache = static_cast<uint16_t*>(k_cache->data);
+  rp.v_cache = static_cast<uint16_t*>(v_cache->data);
+  rp.status = reinterpret_cast<int32_t*>(ws);
+  rp.A = (int)A; rp.T = (int)T; rp.H_q = (int)H_q; rp.H_kv = (int)H_kv; rp.D = (int)D;
+  rp.S = (int)S; rp.max_seq = (int)max_seq;
+  fill_inv_freq(rp.inv_freq, (int)D, theta);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  check_cuda(kvgqa::launch_rope_kv_store(rp, varlen ? 2 : 1, st), "prefill rope_kv_store launch");
+  kvgqa::PrefillParams pp{};
+  pp.q_rot = q_rot;
+  pp.k_cache = rp.k_cache;
+  pp.v_cache = rp.v_cache;
+  pp.cache_rows = rp.cache_rows;
+  pp.offsets = rp.offsets;
+  pp.lengths = rp.lengths;
+  pp.out = static_cast<uint16_t*>(out->data);
+  pp.status = rp.status;
+  pp.A = (int)A; pp.T = (int)T; pp.H_q = (int)H_q; pp.H_kv = (int)H_kv; pp.G = (int)(H_q / H_kv);
+  pp.D = (int)D; pp.S = (int)S; pp.max_seq = (int)max_seq;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  check_cuda(kvgqa::launch_prefill_attention(pp, st), "prefill attention launch");
+}
+
+}  // namespace
+
+extern "C" {
+
 kvgqa_status prefill_gqa_cached_rows_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
                                           const kvgqa_tensor* v, const kvgqa_tensor* cache_rows,
                                           double theta, float scale, const kvgqa_tensor* k_cache,
                                           const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
                                           const kvgqa_tensor* workspace, void* stream) {
   return guarded([&] {
-    if (!q || !k_cache) fail(KVGQA_EINVAL, "null descriptor");
-    if (q->ndim != 4 || k_cache->ndim != 4) fail(KVGQA_EINVAL, "q must be [A,T,H_q,D], caches [S,H_kv,max_seq,D]");
-    const int64_t A = q->shape[0], T = q->shape[1], H_q = q->shape[2], D = q->shape[3];
-    const int64_t S = k_cache->shape[0], H_kv = k_cache->shape[1], max_seq = k_cache->shape[2];
-    check_head_dim(D);
-    check_heads(H_q, H_kv);
-    check_theta(theta);
-    if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
-    if (T > max_seq) fail(KVGQA_EINVAL, "T=%lld exceeds max_seq=%lld", (long long)T, (long long)max_seq);
-    View vq = check_tensor("q", q, 4, KVGQA_BF16, 16);
-    View vk = check_tensor("k", k, 4, KVGQA_BF16, 16);
-    View vv = check_tensor("v", v, 4, KVGQA_BF16, 16);
-    View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
-    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
-    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
-    View vo = check_tensor("out", out, 4, KVGQA_BF16, 16);
-    require_shape(vk, {A, T, H_kv, D});
-    require_shape(vv, {A, T, H_kv, D});
-    require_shape(vr, {A});
-    require_shape(vvc, {S, H_kv, max_seq, D});
-    require_shape(vo, {A, T, H_q, D});
-    const size_t need = KVGQA_STATUS_BYTES + static_cast<size_t>(A) * T * H_q * D * 2;
-    View vws = check_workspace(workspace, need);
-    check_no_alias({&vkc, &vvc, &vo, &vws}, {&vq, &vk, &vv, &vr, &vkc, &vvc, &vo, &vws});
-    const int dev = current_device();
-    check_device({&vq, &vk, &vv, &vr, &vkc, &vvc, &vo, &vws}, dev);
-    if (A == 0 || T == 0) return;
-    kvgqa::RopeStoreParams rp{};
-    unsigned char* ws = static_cast<unsigned char*>(workspace->data);
-    uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + KVGQA_STATUS_BYTES);
-    rp.q = static_cast<const uint16_t*>(q->data);
-    rp.k = static_cast<const uint16_t*>(k->data);
-    rp.v = static_cast<const uint16_t*>(v->data);
-    rp.positions = nullptr;
-    rp.cache_rows = static_cast<const int32_t*>(cache_rows->data);
-    rp.q_out = q_rot;
-    rp.k_cache = static_cast<uint16_t*>(k_cache->data);
-    rp.v_cache = static_cast<uint16_t*>(v_cache->data);
-    rp.status = reinterpret_cast<int32_t*>(ws);
-    rp.A = (int)A; rp.T = (int)T; rp.H_q = (int)H_q; rp.H_kv = (int)H_kv; rp.D = (int)D;
-    rp.S = (int)S; rp.max_seq = (int)max_seq;
-    fill_inv_freq(rp.inv_freq, (int)D, theta);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    check_cuda(kvgqa::launch_rope_kv_store(rp, true, st), "prefill rope_kv_store launch");
-    kvgqa::PrefillParams pp{};
-    pp.q_rot = q_rot;
-    pp.k_cache = rp.k_cache;
-    pp.v_cache = rp.v_cache;
-    pp.cache_rows = rp.cache_rows;
-    pp.out = static_cast<uint16_t*>(out->data);
-    pp.status = rp.status;
-    pp.A = (int)A; pp.T = (int)T; pp.H_q = (int)H_q; pp.H_kv = (int)H_kv; pp.G = (int)(H_q / H_kv);
-    pp.D = (int)D; pp.S = (int)S; pp.max_seq = (int)max_seq;
-    pp.scale_log2 = scale * 1.4426950408889634f;
-    check_cuda(kvgqa::launch_prefill_attention(pp, st), "prefill attention launch");
+    prefill_body(q, k, v, nullptr, nullptr, cache_rows, theta, scale, k_cache, v_cache, out, workspace, stream);
+  });
+}
+
+kvgqa_status prefill_varlen_gqa_cached_rows_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
+                                                 const kvgqa_tensor* v, const kvgqa_tensor* offsets,
+                                                 const kvgqa_tensor* lengths, const kvgqa_tensor* cache_rows,
+                                                 double theta, float scale, const kvgqa_tensor* k_cache,
+                                                 const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
+                                                 const kvgqa_tensor* workspace, void* stream) {
+  return guarded([&] {
+    if (!offsets || !lengths) fail(KVGQA_EINVAL, "offsets/lengths: null descriptor");
+    prefill_body(q, k, v, offsets, lengths, cache_rows, theta, scale, k_cache, v_cache, out, workspace, stream);
   });
 }
 

@@ -22,6 +22,8 @@ struct RopeStoreParams {
   const uint16_t* v;
   const int32_t* positions;  // decode [A]; prefill: nullptr (positions are 0..T-1)
   const int32_t* cache_rows; // [A]
+  const int32_t* offsets;    // varlen prefill [A]: position of each prompt's first token
+  const int32_t* lengths;    // varlen prefill [A]: tokens of each prompt (<= T)
   uint16_t* q_out;           // rotated Q, same layout as q
   uint16_t* k_cache;         // [S,H_kv,max_seq,D]
   uint16_t* v_cache;
@@ -30,7 +32,10 @@ struct RopeStoreParams {
   double inv_freq[kMaxHeadDim / 2];  // theta^(-2i/D), computed on the host in double
 };
 
-cudaError_t launch_rope_kv_store(const RopeStoreParams& p, bool prefill, cudaStream_t stream);
+// mode 0: decode (one CTA per token at positions[a]); 1: equal-length prefill
+// (one CTA per position 0..T-1, all prompts); 2: varlen prefill (one CTA per
+// (prompt, token), token t of prompt a at offsets[a] + t, t < lengths[a]).
+cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_t stream);
 
 // ------------------------------------------------------------------ decode attention
 struct DecodeParams {
@@ -80,6 +85,8 @@ struct PrefillParams {
   const uint16_t* k_cache;    // [S,H_kv,max_seq,D]
   const uint16_t* v_cache;
   const int32_t* cache_rows;  // [A]
+  const int32_t* offsets;     // [A] or nullptr (all 0): position of each prompt's first token
+  const int32_t* lengths;     // [A] or nullptr (all T): tokens of each prompt
   uint16_t* out;              // [A,T,H_q,D]
   int32_t* status;
   int A, T, H_q, H_kv, G, D, S, max_seq;

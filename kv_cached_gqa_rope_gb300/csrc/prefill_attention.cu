@@ -123,49 +123,79 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // The work of the persistent grid: items (query tile qt, prompt a, head pair),
-// longest first (tile qt visits qt + 1 key tiles), dealt round-robin; every
-// role of a CTA walks the same sequence, key tile by key tile.
+// longest first (query tile qt of prompt a covers queries [qt*BM, qt*BM+BM)
+// at positions off_a + t and visits the key tiles up to its last query's
+// position), dealt round-robin; every role of a CTA walks the same sequence,
+// key tile by key tile.  Prompt a holds len_a tokens at positions
+// off_a .. off_a+len_a-1 of its row (the equal-length prefill: off 0, len T).
 struct TileWalk {
-  int i, stride, n_items, nqt, units, per_tok, H_q, H_kv, G, S;
-  bool pairs;                 // two heads of one KV group per item (G even)
-  const int32_t* rows;
+  const PrefillParams* p;     // the launch's parameters (read in place)
+  int i, stride;
   int qt, a, hA, hB, kv_row;  // current item (hB < 0: single head)
+  int off, len, nkt, kend;    // its prompt's offset and length, its key tiles, its last key + 1
   int j;                      // key tile within the item
   bool ok;                    // false past the last item
 
+  // Two heads of one KV group per item when G is even.
+  __device__ __forceinline__ bool pairs() const { return (p->G % 2) == 0; }
+  __device__ __forceinline__ int per_tok() const { return pairs() ? p->H_q / 2 : p->H_q; }
+  __device__ __forceinline__ int units() const { return p->A * per_tok(); }
+  __device__ __forceinline__ int n_items() const { return (p->T + BM - 1) / BM * units(); }
+  // Prompt a of item i (the same for every query tile).
+  __device__ __forceinline__ int prompt_of(int item) const { return item % units() / per_tok(); }
+
   __device__ bool load_item() {
-    while (i < n_items) {
-      qt = nqt - 1 - i / units;
-      const int rem = i % units;
-      a = rem / per_tok;
-      const int k = rem % per_tok;
-      hA = pairs ? 2 * k : k;
-      hB = pairs ? 2 * k + 1 : -1;
-      const int r = rows[a];
-      if (r >= 0 && r < S) {
-        kv_row = r * H_kv + hA / G;
+    const int nqt = (p->T + BM - 1) / BM, u = units(), pt = per_tok(), n = nqt * u;
+    while (i < n) {
+      qt = nqt - 1 - i / u;
+      const int rem = i % u;
+      a = rem / pt;
+      const int k = rem % pt;
+      hA = pairs() ? 2 * k : k;
+      hB = pairs() ? 2 * k + 1 : -1;
+      const int r = p->cache_rows[a];
+      const int o = p->offsets ? p->offsets[a] : 0;
+      const int L = p->lengths ? p->lengths[a] : p->T;
+      const bool meta_ok = L >= 0 && L <= p->T && o >= 0 && o <= p->max_seq - L;
+      if (r >= 0 && r < p->S && meta_ok && qt * BM < L) {
+        off = o;
+        len = L;
+        const int q_end = min(L, qt * BM + BM);
+        kend = o + q_end;
+        nkt = (kend + BN - 1) / BN;  // key tiles holding positions 0 .. kend - 1
+        kv_row = r * p->H_kv + hA / p->G;
         j = 0;
         return true;
       }
-      i += stride;  // prompts with an invalid row are skipped (and flagged by the producer)
+      // prompts with an invalid row or metadata are skipped (and flagged by
+      // the store kernel); query tiles past a prompt's length have no work
+      i += stride;
     }
     return false;
   }
-  __device__ void init(const PrefillParams& p, int first, int step) {
-    pairs = (p.G % 2) == 0;
-    per_tok = pairs ? p.H_q / 2 : p.H_q;
-    nqt = (p.T + BM - 1) / BM;
-    units = p.A * per_tok;
-    n_items = nqt * units;
-    H_q = p.H_q; H_kv = p.H_kv; G = p.G; S = p.S; rows = p.cache_rows;
+  __device__ void init(const PrefillParams* params, int first, int step) {
+    p = params;
     i = first;
     stride = step;
     ok = load_item();
   }
   __device__ __forceinline__ bool first_tile() const { return j == 0; }
-  __device__ __forceinline__ bool last_tile() const { return j == qt; }
+  __device__ __forceinline__ bool last_tile() const { return j == nkt - 1; }
+  // First cache position of the key tile: j * BN, except that with prompts at
+  // offsets a last tile reaching past kend is moved back to end at kend, so
+  // it reads no cell past the prompt (those may hold anything, and a zero
+  // weight times a NaN is still a NaN); its columns before j * BN were
+  // covered by tile j - 1 and are masked.  (The equal-length prefill's
+  // key map ends at T, so its positions past the prompt read as zeros.)
+  __device__ __forceinline__ int kstart() const {
+    return (p->offsets && j == nkt - 1 && (j + 1) * BN > kend) ? kend - BN : j * BN;
+  }
+  // Query row r of the tile sees key column c iff
+  // mask_lo() <= c <= mask_base() + r.
+  __device__ __forceinline__ int mask_base() const { return off + qt * BM - kstart(); }
+  __device__ __forceinline__ int mask_lo() const { return j * BN - kstart(); }
   __device__ void advance() {
-    if (j < qt) { ++j; return; }
+    if (j < nkt - 1) { ++j; return; }
     i += stride;
     ok = load_item();
   }
@@ -196,11 +226,11 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   TileWalk walk;
-  walk.init(p, blockIdx.x, gridDim.x);
+  walk.init(&p, blockIdx.x, gridDim.x);
   if (!walk.ok) {  // uniform: this CTA has no valid item
     if (threadIdx.x == 0) {
-      for (int i = blockIdx.x; i < walk.n_items; i += gridDim.x) {
-        const int r = p.cache_rows[(i % walk.units) / walk.per_tok];
+      for (int i = blockIdx.x; i < walk.n_items(); i += gridDim.x) {
+        const int r = p.cache_rows[walk.prompt_of(i)];
         if (r < 0 || r >= p.S) { atomicOr(p.status, KVGQA_FLAG_ROW_RANGE); break; }
       }
     }
@@ -245,8 +275,8 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     if (lane == 0) {
       const uint64_t pol_q = l2_evict_first_policy();
       const uint64_t pol_kv = l2_evict_last_policy();  // K/V tiles are re-read by the group's heads
-      for (int i = blockIdx.x; i < walk.n_items; i += gridDim.x) {
-        const int r = p.cache_rows[(i % walk.units) / walk.per_tok];
+      for (int i = blockIdx.x; i < walk.n_items(); i += gridDim.x) {
+        const int r = p.cache_rows[walk.prompt_of(i)];
         if (r < 0 || r >= p.S) { atomicOr(p.status, KVGQA_FLAG_ROW_RANGE); break; }
       }
       // Per item: Q_A, the first K tile, Q_B (the order the MMAs need them).
@@ -268,7 +298,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         unsigned char* st = smem + C::K_OFF + s * C::TILE;
         mbar_arrive_expect_tx(&k_full[s], BN * D * 2);
         for (int sub = 0; sub < C::NSUB; ++sub)
-          tma_load_3d(st + sub * SUB, &map_k, sub * 64, walk.j * BN, walk.kv_row, &k_full[s], pol_kv);
+          tma_load_3d(st + sub * SUB, &map_k, sub * 64, walk.kstart(), walk.kv_row, &k_full[s], pol_kv);
         ++it;
         if (fresh && walk.hB >= 0 && !load_q(1, qb)) break;
       }
@@ -291,7 +321,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         unsigned char* st = smem + C::V_OFF + s * C::TILE;
         mbar_arrive_expect_tx(&v_full[s], BN * D * 2);
         for (int sub = 0; sub < C::NSUB; ++sub)
-          tma_load_3d(st + sub * SUB, &map_v, sub * 64, walk.j * BN, walk.kv_row, &v_full[s], pol_kv);
+          tma_load_3d(st + sub * SUB, &map_v, sub * 64, walk.kstart(), walk.kv_row, &v_full[s], pol_kv);
         ++it;
       }
       if (*abort_flag) {
@@ -307,7 +337,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);
-      const bool pairs = walk.pairs;
+      const bool pairs = walk.pairs();
       const int nh = pairs ? 2 : 1;
       bool issued = false;
       int qn = 0;             // items whose Q tiles have been consumed
@@ -394,19 +424,23 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     float m_ref = -INFINITY, l = 0.f;
     for (int t = 0; walk.ok; ++t, walk.advance()) {
       if (x == 1 && walk.hB < 0) continue;  // single-head item: the B group has nothing to do
-      const bool first = walk.first_tile(), diag = walk.last_tile();
+      const bool first = walk.first_tile(), last = walk.last_tile();
+      const int mbase = walk.mask_base(), mlo = walk.mask_lo();
       if (!__all_sync(FULLMASK, mbar_wait_bounded(&s_full[x], t & 1, abort_flag, p.status))) break;
       tc_fence_after();
       // With head pairs the two groups take turns (A0 B0 A1 B1 ...): each runs
       // its softmax alone on the SM's issue slots while the tensor core
       // works for the other head.
-      if (walk.pairs && (x == 1 || t > 0)) {
+      if (walk.pairs() && (x == 1 || t > 0)) {
         const int k = x == 0 ? t - 1 : t;  // completion of the other group to wait for
         if (!__all_sync(FULLMASK, mbar_wait_bounded(&turn[1 - x], k & 1, abort_flag, p.status))) break;
       }
       // Scores enter the softmax as s * ce with ce > 0 (a non-positive scale is
       // folded into the scores first, a path no usual caller takes).  On the
-      // diagonal tile, keys after the query become -inf, so they weigh zero.
+      // tiles that reach past a query's position (the diagonal), keys after
+      // the query become -inf, so they weigh zero.  Every query sees key 0 in
+      // tile 0; a later tile may hold no key a row sees (with offsets), and
+      // then the row's maximum stays and its weights there are zero.
       uint32_t u[BN];
 #pragma unroll
       for (int q = 0; q < BN / 32; ++q) tmem_ld32(s_col + q * 32, *reinterpret_cast<uint32_t(*)[32]>(u + q * 32));
@@ -416,9 +450,14 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
 #pragma unroll
         for (int i = 0; i < BN; ++i) sv[i] *= c;
       }
-      if (diag) {
+      if (mlo > 0) {  // a moved last tile: a band
+        const int thr = mbase + r;
 #pragma unroll
-        for (int i = 0; i < BN; ++i) sv[i] = i <= r ? sv[i] : -INFINITY;
+        for (int i = 0; i < BN; ++i) sv[i] = (i >= mlo && i <= thr) ? sv[i] : -INFINITY;
+      } else if (mbase < BN - 1) {
+        const int thr = mbase + r;
+#pragma unroll
+        for (int i = 0; i < BN; ++i) sv[i] = i <= thr ? sv[i] : -INFINITY;
       }
       float mx[8];
 #pragma unroll
@@ -475,10 +514,10 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&p_full[x]);
-        if (walk.pairs) mbar_arrive(&turn[x]);
+        if (walk.pairs()) mbar_arrive(&turn[x]);
       }
 
-      if (diag) {
+      if (last) {
         // ---------------------------------------------------- item epilogue
         if (!__all_sync(FULLMASK, mbar_wait_bounded(&o_done[x], t & 1, abort_flag, p.status))) break;
         tc_fence_after();
@@ -489,9 +528,9 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
           uint32_t u[32];
-          tmem_ld32(o_col + q * 32, u);  // warp-wide: rows past T load too, only their store is skipped
+          tmem_ld32(o_col + q * 32, u);  // warp-wide: rows past the prompt load too, only their store is skipped
           tmem_wait_ld();
-          if (tq < p.T) {
+          if (tq < walk.len) {
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8) {
               uint4 o;
@@ -529,9 +568,11 @@ cudaError_t make_maps(const PrefillParams& p, PrefillMaps* m) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  // Keys: positions [0, T) of each (slot, kv head); positions >= T are
-  // outside the map and read as zeros.
-  cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(p.T), static_cast<cuuint64_t>(p.S) * p.H_kv};
+  // Keys: positions [0, T) of each (slot, kv head) for the equal-length
+  // prefill (positions >= T are outside the map and read as zeros), the whole
+  // row for prompts at offsets (keys past a query's position are masked).
+  const cuuint64_t key_extent = p.offsets ? static_cast<cuuint64_t>(p.max_seq) : static_cast<cuuint64_t>(p.T);
+  cuuint64_t dims[3] = {D, key_extent, static_cast<cuuint64_t>(p.S) * p.H_kv};
   cuuint64_t strides[2] = {D * 2, D * 2 * static_cast<cuuint64_t>(p.max_seq)};
   cuuint32_t box[3] = {64, BN, 1};
   cuuint32_t es[3] = {1, 1, 1};

@@ -55,7 +55,7 @@ __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const Co
 
 template <int D>
 __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_constant__ RopeStoreParams p,
-                                                            int prefill) {
+                                                            int mode) {
   constexpr int HALF = D / 2;
   constexpr int RU = D / 16;  // rotation units per head: 8 pairs each
   constexpr int VU = D / 8;   // copy units per head: 8 elements (16 bytes) each
@@ -63,18 +63,36 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
 
   pdl_wait();     // inputs and outputs may belong to the previous kernel
   pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
-  int pos, ntok;
-  if (prefill) {
+  const bool prefill = mode == 1;
+  int pos, ntok, a0 = 0;  // a0: the token's prompt (decode and varlen modes)
+  size_t tok0 = 0;        // its index in the token-major inputs
+  if (mode == 1) {
     pos = blockIdx.x;  // position t, shared by all A prompts
     ntok = p.A;
   } else {
-    pos = p.positions[blockIdx.x];
     ntok = 1;
-    const int row = p.cache_rows[blockIdx.x];
+    if (mode == 0) {
+      a0 = blockIdx.x;
+      tok0 = a0;
+      pos = p.positions[a0];
+    } else {
+      a0 = blockIdx.x / p.T;
+      const int t = blockIdx.x % p.T;
+      tok0 = blockIdx.x;
+      const int off = p.offsets[a0], len = p.lengths[a0];
+      const bool meta_ok = len >= 0 && len <= p.T && off >= 0 && off <= p.max_seq - len;
+      if (meta_ok && t >= len) return;  // past this prompt's tokens
+      if (!meta_ok) {
+        if (threadIdx.x == 0 && t == 0) atomicOr(p.status, KVGQA_FLAG_POSITION_RANGE);
+        return;
+      }
+      pos = off + t;
+    }
+    const int row = p.cache_rows[a0];
     const bool pos_ok = pos >= 0 && pos < p.max_seq;
     const bool row_ok = row >= 0 && row < p.S;
     if (!pos_ok || !row_ok) {
-      if (threadIdx.x == 0)
+      if (threadIdx.x == 0 && (mode == 0 || blockIdx.x % p.T == 0))
         atomicOr(p.status, (pos_ok ? 0 : KVGQA_FLAG_POSITION_RANGE) | (row_ok ? 0 : KVGQA_FLAG_ROW_RANGE));
       return;
     }
@@ -107,10 +125,10 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
       dst[u] = nullptr;
       if (r >= n_rot) continue;
       const int ti = r / rot_units, rr = r % rot_units;
-      const int a = prefill ? ti : blockIdx.x;
+      const int a = prefill ? ti : a0;
       const int row = p.cache_rows[a];
       if (row < 0 || row >= p.S) continue;
-      const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : static_cast<size_t>(a);
+      const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : tok0;
       const int h = rr / RU, c = rr % RU;
       const uint16_t* src;
       if (h < p.H_q) {
@@ -145,10 +163,10 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
       dst[u] = nullptr;
       if (r >= n_copy) continue;
       const int ti = r / copy_units, rr = r % copy_units;
-      const int a = prefill ? ti : blockIdx.x;
+      const int a = prefill ? ti : a0;
       const int row = p.cache_rows[a];
       if (row < 0 || row >= p.S) continue;
-      const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : static_cast<size_t>(a);
+      const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : tok0;
       const int g = rr / VU, c = rr % VU;
       dst[u] = p.v_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D + c * 8;
       x[u] = *reinterpret_cast<const uint4*>(p.v + (tok * p.H_kv + g) * D + c * 8);
@@ -161,8 +179,10 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
 
 }  // namespace
 
-cudaError_t launch_rope_kv_store(const RopeStoreParams& p, bool prefill, cudaStream_t stream) {
-  const unsigned grid = prefill ? static_cast<unsigned>(p.T) : static_cast<unsigned>(p.A);
+cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_t stream) {
+  const long long g = mode == 0 ? p.A : mode == 1 ? p.T : static_cast<long long>(p.A) * p.T;
+  if (g > 0x7fffffffll) return cudaErrorInvalidValue;
+  const unsigned grid = static_cast<unsigned>(g);
   if (grid == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -173,7 +193,6 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, bool prefill, cudaStr
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int mode = prefill ? 1 : 0;
   if (p.D == 128) return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<128>, p, mode);
   if (p.D == 64) return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<64>, p, mode);
   return cudaErrorInvalidValue;

@@ -249,6 +249,65 @@ def make_prefill_inputs(wl: PrefillWorkload, salt: int = 0) -> PrefillInputs:
     return PrefillInputs(wl, q, k, v, rows)
 
 
+NAN_BITS = 0x7FC0  # a quiet NaN in BF16
+
+
+@dataclass
+class VarlenInputs:
+    """Prompts of different lengths at their own offsets (chunked prefill).
+
+    Prompt a holds ``lengths[a]`` tokens, padded to T in q/k/v (the padding
+    is random too), at positions ``offsets[a]`` .. of row ``cache_rows[a]``,
+    whose cells ``[0, offsets[a])`` already hold a random prefix (earlier
+    chunks or decode steps)."""
+    wl: PrefillWorkload
+    q: torch.Tensor           # [A, T, H_q, D] bf16
+    k: torch.Tensor           # [A, T, H_kv, D] bf16
+    v: torch.Tensor           # [A, T, H_kv, D] bf16
+    offsets: torch.Tensor     # [A] int32
+    lengths: torch.Tensor     # [A] int32
+    cache_rows: torch.Tensor  # [A] int32
+    salt: int = 0
+
+    def build_cache(self, device="cpu", tail: str = "sentinel"):
+        """``[slots, H_kv, max_seq, D]`` caches: each target row's prefix
+        random, the cells from ``offsets[a]`` on ``tail`` ("sentinel" or
+        "nan"), every other slot random (other requests' live rows)."""
+        wl = self.wl
+        shape = (wl.slots, wl.H_kv, wl.max_seq, wl.D)
+        g = generator(wl.index, 100 + self.salt)
+        kc = randn_bf16(shape, g)
+        vc = randn_bf16(shape, g)
+        fill = {"sentinel": SENTINEL_BITS, "nan": NAN_BITS}[tail]
+        for a in range(self.offsets.shape[0]):
+            r, o = int(self.cache_rows[a]), min(max(int(self.offsets[a]), 0), wl.max_seq)
+            if 0 <= r < wl.slots:
+                kc[r, :, o:].view(torch.int16).fill_(fill)
+                vc[r, :, o:].view(torch.int16).fill_(fill)
+        return kc.to(device), vc.to(device)
+
+
+def make_varlen_inputs(wl: PrefillWorkload, offsets, lengths, salt: int = 0, rows=None) -> VarlenInputs:
+    g = generator(wl.index, salt)
+    perm = torch.randperm(wl.slots, generator=g)[: wl.A].to(torch.int32)
+    q = randn_bf16((wl.A, wl.T, wl.H_q, wl.D), g)
+    k = randn_bf16((wl.A, wl.T, wl.H_kv, wl.D), g)
+    v = randn_bf16((wl.A, wl.T, wl.H_kv, wl.D), g)
+    cache_rows = perm if rows is None else torch.tensor(rows, dtype=torch.int32)
+    return VarlenInputs(wl, q, k, v, torch.tensor(offsets, dtype=torch.int32),
+                        torch.tensor(lengths, dtype=torch.int32), cache_rows, salt)
+
+
+def random_offsets_lengths(wl: PrefillWorkload, salt: int = 0):
+    """A mix of chunk shapes for A prompts: lengths uniform in [1, T], offsets
+    uniform in [0, max_seq - length] (a prompt continuing a prefix of any
+    size, not aligned to any tile)."""
+    g = generator(wl.index, 200 + salt)
+    lengths = torch.randint(1, wl.T + 1, (wl.A,), generator=g)
+    offsets = torch.stack([torch.randint(0, wl.max_seq - int(n) + 1, (1,), generator=g)[0] for n in lengths])
+    return offsets.tolist(), lengths.tolist()
+
+
 def scaled_decode(wl: DecodeWorkload, **kw) -> DecodeWorkload:
     """A copy of a decode workload with some sizes replaced (test cases)."""
     d = dict(wl.__dict__)

@@ -18,7 +18,10 @@ numpy operations (a matrix product is the only library primitive used):
   inactive full-capacity rows stay untouched);
 * the equal-length prefill whose prefixes land in their target empty cache rows
   (same section: one [A, T] batch runs, then each prefix is mapped into its
-  target empty shared-cache row).
+  target empty shared-cache row), and its generalisation to prompts of
+  different lengths at nonnegative position offsets into rows that already
+  hold a prefix (chunked prefill; prompts of other lengths form separate
+  groups there, one call here).
 
 Storage is BF16 (16-bit patterns in numpy ``uint16`` arrays); arithmetic is
 float64; results that the path stores as BF16 are rounded once, directly from
@@ -31,7 +34,8 @@ Readings taken where the pages are silent (each is listed in the design doc):
   - q is rounded to BF16 after rotation, before attention;
   - the softmax scale multiplies the float score q.k (it is not folded into q);
   - query head h reads KV head floor(h / G), G = H_q / H_kv;
-  - prefill positions start at 0 (the target rows are empty).
+  - prefill positions start at 0 (the target rows are empty); a chunk's
+    positions start at its offset and see the row's prefix before it.
 
 Parity pins: every function here is checked by ``tests/test_oracle_pins.py``
 against closed forms, invariants and brute force; none is "parity unpinned".
@@ -43,7 +47,7 @@ import numpy as np
 __all__ = [
     "bf16_to_f64", "f64_to_bf16", "rope_inv_freq", "rope_split_half",
     "rope_split_half_bf16", "rope_kv_store", "cached_gqa_attention",
-    "cached_gqa_attention_one", "prefill_gqa_cached_rows",
+    "cached_gqa_attention_one", "prefill_gqa_cached_rows", "prefill_varlen_gqa_cached_rows",
     "prefill_attention_one", "ulp_distance_bf16",
 ]
 

@@ -1,6 +1,7 @@
 """Host-side contract of the C ABI, runnable without a GPU: the library loads,
 exports every function include/kvgqa.h declares, and rejects malformed calls
 with the documented status before touching CUDA."""
+import ctypes
 import os
 import re
 
@@ -201,6 +202,37 @@ def test_prefill_contract():
     a = prefill_args()
     a["k"] = torch.zeros(2, 8, 4, 64, dtype=torch.bfloat16)
     assert code_of(kv.prefill_gqa_cached_rows_out_, **a) == "EINVAL"
+
+
+def varlen_args(**kw):
+    a = prefill_args(**kw)
+    A = a["q"].shape[0]
+    a["offsets"] = torch.zeros(A, dtype=torch.int32)
+    a["lengths"] = torch.full((A,), a["q"].shape[1], dtype=torch.int32)
+    return a
+
+
+def test_prefill_varlen_contract():
+    a = varlen_args()
+    a["offsets"] = torch.zeros(3, dtype=torch.int32)      # not [A]
+    assert code_of(kv.prefill_varlen_gqa_cached_rows_out_, **a) == "EINVAL"
+    a = varlen_args()
+    a["lengths"] = torch.zeros(2, dtype=torch.float32)    # not int32
+    assert code_of(kv.prefill_varlen_gqa_cached_rows_out_, **a) == "EDTYPE"
+    a = varlen_args()
+    a["out"] = a["k_cache"].view(-1)[: 2 * 8 * 4 * 64].view(2, 8, 4, 64)
+    assert code_of(kv.prefill_varlen_gqa_cached_rows_out_, **a) == "EALIAS"
+    a = varlen_args(T=20)                                 # T > max_seq
+    a["workspace"] = aligned_bytes(256 + 2 * 20 * 4 * 64 * 2)
+    assert code_of(kv.prefill_varlen_gqa_cached_rows_out_, **a) == "EINVAL"
+    lib = kv.library()
+    # null offsets or lengths descriptors are rejected, not read as "equal length"
+    ds = [kv.describe(t) for t in (a["q"], a["k"], a["v"])]
+    null = ctypes.POINTER(kv.KvgqaTensor)()
+    st = lib.prefill_varlen_gqa_cached_rows_out_(*[ctypes.byref(d) for d in ds], null, null,
+                                                 ctypes.byref(kv.describe(a["cache_rows"])), 1e4, 0.125,
+                                                 null, null, null, null, None)
+    assert kv.STATUS_NAMES[st] == "EINVAL"
 
 
 def step_args(A=2, H_q=4, H_kv=2, D=64, S=4, L=32):
