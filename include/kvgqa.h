@@ -181,14 +181,15 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
                                        const kvgqa_tensor* out, const kvgqa_tensor* workspace,
                                        void* stream);
 
-/* Workspace of decode_step_out_: the same as cached_gqa_attention_out_'s. */
+/* Workspace of decode_step_out_ and decode_step_single_launch_out_: that of
+ * cached_gqa_attention_out_ (status block, counters, partials), then room for
+ * the rotated queries (A*H_q*D bf16, 256-byte aligned). */
 kvgqa_status decode_step_workspace_size(int64_t A, int64_t H_q, int64_t H_kv, int64_t D,
                                         int32_t device, size_t* bytes);
 
 /*
- * decode_step_out_ -- the whole decode step of one layer in one launch:
- * rope_kv_store_out_ followed by cached_gqa_attention_out_, without the
- * rotated queries ever leaving the chip.
+ * decode_step_out_ -- the whole decode step of one layer: rope_kv_store_out_
+ * followed by cached_gqa_attention_out_, in one call.
  *
  * microLLM-rocm ARCHITECTURE.md, section "Tensor ownership boundary":
  * positions and cache rows parameterise decode-only RoPE, the K/V store and
@@ -198,6 +199,10 @@ kvgqa_status decode_step_workspace_size(int64_t A, int64_t H_q, int64_t H_kv, in
  * out[a] is the attention of the rotated q[a] over keys 0..p of row r, as
  * cached_gqa_attention_out_ computes it (the rotated queries are rounded to
  * BF16 first, as there).  The results are bit-identical to the two calls.
+ * It is faster than them: knowing that the kernel before its attention is its
+ * own store kernel (which writes only the rotated queries, into the
+ * workspace, and the new cells), the attention streams every cache tile that
+ * holds no new cell while the store still runs.
  *
  *   q [A,H_q,D], k/v [A,H_kv,D] bf16, positions/cache_rows [A] int32  (read)
  *   theta > 0 and finite, scale finite
@@ -215,6 +220,20 @@ kvgqa_status decode_step_out_(const kvgqa_tensor* q, const kvgqa_tensor* k, cons
                               double theta, float scale, const kvgqa_tensor* k_cache,
                               const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
                               const kvgqa_tensor* workspace, void* stream);
+
+/*
+ * decode_step_single_launch_out_ -- decode_step_out_ in one kernel launch:
+ * the attention kernel rotates each segment's queries in shared memory and
+ * stores the new cells itself (the rotated queries never leave the chip).
+ * Same arguments, workspace and results (bit-identical); measured slower
+ * than decode_step_out_ on GB300, kept for launch-bound callers.
+ */
+kvgqa_status decode_step_single_launch_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
+                                            const kvgqa_tensor* v, const kvgqa_tensor* positions,
+                                            const kvgqa_tensor* cache_rows, double theta, float scale,
+                                            const kvgqa_tensor* k_cache, const kvgqa_tensor* v_cache,
+                                            const kvgqa_tensor* out, const kvgqa_tensor* workspace,
+                                            void* stream);
 
 /*
  * cached_gqa_attention_static_scratch_out_ -- the same attention as

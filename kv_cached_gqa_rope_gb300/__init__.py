@@ -80,6 +80,8 @@ def _load():
     lib.decode_step_workspace_size.restype = st
     lib.decode_step_out_.argtypes = [P, P, P, P, P, ctypes.c_double, ctypes.c_float, P, P, P, P, ctypes.c_void_p]
     lib.decode_step_out_.restype = st
+    lib.decode_step_single_launch_out_.argtypes = lib.decode_step_out_.argtypes
+    lib.decode_step_single_launch_out_.restype = st
     VP = ctypes.c_void_p
     lib.kvgqa_slots_create.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(VP)]
     lib.kvgqa_slots_destroy.argtypes = [VP]
@@ -106,7 +108,7 @@ EXPORTED_SYMBOLS = ("kvgqa_abi_version", "kvgqa_last_error", "rope_kv_store_work
                     "cached_gqa_attention_static_scratch_out_", "decode_step_workspace_size",
                     "decode_step_out_", "kvgqa_slots_create", "kvgqa_slots_destroy", "kvgqa_slots_admit",
                     "kvgqa_slots_release", "kvgqa_slots_step", "kvgqa_slots_query", "kvgqa_metadata_upload",
-                    "prefill_varlen_gqa_cached_rows_out_")
+                    "prefill_varlen_gqa_cached_rows_out_", "decode_step_single_launch_out_")
 
 
 def library() -> ctypes.CDLL:
@@ -197,11 +199,21 @@ def cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_rows, sc
 
 def decode_step_out_(q, k, v, positions, cache_rows, theta, scale, k_cache, v_cache, out, workspace,
                      stream=None) -> None:
-    """The whole decode step in one launch: the store of rope_kv_store_out_
-    and the attention of cached_gqa_attention_out_ (no q_out)."""
+    """The whole decode step: the store of rope_kv_store_out_ and the
+    attention of cached_gqa_attention_out_ (no q_out), the attention starting
+    to stream the cache while the store runs."""
     ds = [describe(t) for t in (q, k, v, positions, cache_rows)]
     outs = [describe(t) for t in (k_cache, v_cache, out, workspace)]
     _check(_lib.decode_step_out_(*map(_ref, ds), float(theta), float(scale), *map(_ref, outs), _stream(stream)))
+
+
+def decode_step_single_launch_out_(q, k, v, positions, cache_rows, theta, scale, k_cache, v_cache, out, workspace,
+                                   stream=None) -> None:
+    """decode_step_out_ in one kernel launch (same results, bit for bit)."""
+    ds = [describe(t) for t in (q, k, v, positions, cache_rows)]
+    outs = [describe(t) for t in (k_cache, v_cache, out, workspace)]
+    _check(_lib.decode_step_single_launch_out_(*map(_ref, ds), float(theta), float(scale), *map(_ref, outs),
+                                               _stream(stream)))
 
 
 def cached_gqa_attention_static_scratch_out_(q_rot, k_cache, v_cache, positions, cache_rows, scale, out,
@@ -265,12 +277,12 @@ def prepare_cached_gqa_attention_out_(q_rot, k_cache, v_cache, positions, cache_
 
 
 def prepare_decode_step_out_(q, k, v, positions, cache_rows, theta, scale, k_cache, v_cache, out, workspace,
-                             stream=None) -> Prepared:
+                             stream=None, single_launch=False) -> Prepared:
     ds = [describe(t) for t in (q, k, v, positions, cache_rows, k_cache, v_cache, out, workspace)]
     args = (*map(_ref, ds[:5]), ctypes.c_double(theta), ctypes.c_float(scale), *map(_ref, ds[5:]),
             ctypes.c_void_p(_stream(stream)))
-    return Prepared(_lib.decode_step_out_, args,
-                    (ds, q, k, v, positions, cache_rows, k_cache, v_cache, out, workspace))
+    fn = _lib.decode_step_single_launch_out_ if single_launch else _lib.decode_step_out_
+    return Prepared(fn, args, (ds, q, k, v, positions, cache_rows, k_cache, v_cache, out, workspace))
 
 
 def prepare_prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_cache, v_cache, out, workspace,

@@ -331,16 +331,38 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
   });
 }
 
+namespace {
+// Workspace of the whole decode step: the attention call's (status block,
+// counters, partials), then the rotated queries [A, H_q, D] bf16.
+size_t step_q_offset(const kvgqa::DecodeLayout& lay) {
+  return (KVGQA_STATUS_BYTES + lay.counter_bytes + lay.partial_bytes + 255) / 256 * 256;
+}
+}  // namespace
+
 kvgqa_status decode_step_workspace_size(int64_t A, int64_t H_q, int64_t H_kv, int64_t D, int32_t device,
                                         size_t* bytes) {
-  return cached_gqa_attention_workspace_size(A, H_q, H_kv, D, device, bytes);
+  return guarded([&] {
+    if (!bytes) fail(KVGQA_EINVAL, "bytes: null");
+    if (A < 0) fail(KVGQA_EINVAL, "A < 0");
+    check_head_dim(D);
+    check_heads(H_q, H_kv);
+    const int G = (int)(H_q / H_kv);
+    if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
+    kvgqa::DecodeLayout lay;
+    check_cuda(kvgqa::decode_layout(device, (int)D, kvgqa::decode_group_pad(G), A, H_kv, &lay),
+               "decode kernel set-up");
+    *bytes = step_q_offset(lay) + static_cast<size_t>(A) * H_q * D * 2;
+  });
 }
 
-kvgqa_status decode_step_out_(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tensor* v,
-                              const kvgqa_tensor* positions, const kvgqa_tensor* cache_rows, double theta,
-                              float scale, const kvgqa_tensor* k_cache, const kvgqa_tensor* v_cache,
-                              const kvgqa_tensor* out, const kvgqa_tensor* workspace, void* stream) {
-  return guarded([&] {
+namespace {
+// The whole decode step.  Two launches (default): the store kernel, then the
+// attention with an early start.  Single launch: the attention kernel in its
+// fused form rotates the queries and stores the new cells itself.
+void decode_step_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tensor* v,
+                      const kvgqa_tensor* positions, const kvgqa_tensor* cache_rows, double theta, float scale,
+                      const kvgqa_tensor* k_cache, const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
+                      const kvgqa_tensor* workspace, void* stream, bool single_launch) {
     if (!q || !k_cache) fail(KVGQA_EINVAL, "null descriptor");
     if (q->ndim != 3 || k_cache->ndim != 4) fail(KVGQA_EINVAL, "q must be [A,H_q,D], caches [S,H_kv,max_seq,D]");
     const int64_t A = q->shape[0], H_q = q->shape[1], D = q->shape[2];
@@ -373,30 +395,87 @@ kvgqa_status decode_step_out_(const kvgqa_tensor* q, const kvgqa_tensor* k, cons
     kvgqa::DecodeLayout lay;
     check_cuda(kvgqa::decode_layout(dev, (int)D, kvgqa::decode_group_pad(G), A, H_kv, &lay),
                "decode kernel set-up");
-    View vws = check_workspace(workspace, KVGQA_STATUS_BYTES + lay.counter_bytes + lay.partial_bytes);
+    const size_t q_off = step_q_offset(lay);
+    View vws = check_workspace(workspace, q_off + static_cast<size_t>(A) * H_q * D * 2);
     check_device({&vq, &vk, &vv, &vp, &vr, &vkc, &vvc, &vo, &vws}, dev);
     if (A == 0) return;
-    kvgqa::DecodeParams p{};
-    p.q = static_cast<const uint16_t*>(q->data);
-    p.k_cache = static_cast<const uint16_t*>(k_cache->data);
-    p.v_cache = static_cast<const uint16_t*>(v_cache->data);
-    p.positions = static_cast<const int32_t*>(positions->data);
-    p.cache_rows = static_cast<const int32_t*>(cache_rows->data);
-    p.out = static_cast<uint16_t*>(out->data);
     unsigned char* ws = static_cast<unsigned char*>(workspace->data);
-    p.status = reinterpret_cast<int32_t*>(ws);
+    uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + q_off);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (single_launch) {
+      kvgqa::DecodeParams p{};
+      p.q = static_cast<const uint16_t*>(q->data);
+      p.k_cache = static_cast<const uint16_t*>(k_cache->data);
+      p.v_cache = static_cast<const uint16_t*>(v_cache->data);
+      p.positions = static_cast<const int32_t*>(positions->data);
+      p.cache_rows = static_cast<const int32_t*>(cache_rows->data);
+      p.out = static_cast<uint16_t*>(out->data);
+      p.status = reinterpret_cast<int32_t*>(ws);
+      p.counters = reinterpret_cast<int32_t*>(ws + KVGQA_STATUS_BYTES);
+      p.partials = reinterpret_cast<float*>(ws + KVGQA_STATUS_BYTES + lay.counter_bytes);
+      p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
+      p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
+      p.scale_log2 = scale * 1.4426950408889634f;
+      p.fused = 1;
+      p.k_new = static_cast<const uint16_t*>(k->data);
+      p.v_new = static_cast<const uint16_t*>(v->data);
+      p.k_cache_w = static_cast<uint16_t*>(k_cache->data);
+      p.v_cache_w = static_cast<uint16_t*>(v_cache->data);
+      fill_inv_freq(p.inv_freq, (int)D, theta);
+      check_cuda(kvgqa::launch_cached_gqa_attention(p, st), "decode_step launch");
+      return;
+    }
+    // 1. the store kernel: rotated queries into the workspace, new cells
+    kvgqa::RopeStoreParams rp{};
+    rp.q = static_cast<const uint16_t*>(q->data);
+    rp.k = static_cast<const uint16_t*>(k->data);
+    rp.v = static_cast<const uint16_t*>(v->data);
+    rp.positions = static_cast<const int32_t*>(positions->data);
+    rp.cache_rows = static_cast<const int32_t*>(cache_rows->data);
+    rp.q_out = q_rot;
+    rp.k_cache = static_cast<uint16_t*>(k_cache->data);
+    rp.v_cache = static_cast<uint16_t*>(v_cache->data);
+    rp.status = reinterpret_cast<int32_t*>(ws);
+    rp.A = (int)A; rp.T = 1; rp.H_q = (int)H_q; rp.H_kv = (int)H_kv; rp.D = (int)D;
+    rp.S = (int)S; rp.max_seq = (int)max_seq;
+    fill_inv_freq(rp.inv_freq, (int)D, theta);
+    check_cuda(kvgqa::launch_rope_kv_store(rp, 0, st), "decode_step store launch");
+    // 2. the attention, started while the store kernel runs: it streams the
+    // cache tiles without a new cell before waiting for it
+    kvgqa::DecodeParams p{};
+    p.q = q_rot;
+    p.k_cache = rp.k_cache;
+    p.v_cache = rp.v_cache;
+    p.positions = rp.positions;
+    p.cache_rows = rp.cache_rows;
+    p.out = static_cast<uint16_t*>(out->data);
+    p.status = rp.status;
     p.counters = reinterpret_cast<int32_t*>(ws + KVGQA_STATUS_BYTES);
     p.partials = reinterpret_cast<float*>(ws + KVGQA_STATUS_BYTES + lay.counter_bytes);
     p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
     p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.fused = 1;
-    p.k_new = static_cast<const uint16_t*>(k->data);
-    p.v_new = static_cast<const uint16_t*>(v->data);
-    p.k_cache_w = static_cast<uint16_t*>(k_cache->data);
-    p.v_cache_w = static_cast<uint16_t*>(v_cache->data);
-    fill_inv_freq(p.inv_freq, (int)D, theta);
-    check_cuda(kvgqa::launch_cached_gqa_attention(p, static_cast<cudaStream_t>(stream)), "decode_step launch");
+    p.early = 1;
+    check_cuda(kvgqa::launch_cached_gqa_attention(p, st), "decode_step attention launch");
+}
+}  // namespace
+
+kvgqa_status decode_step_out_(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tensor* v,
+                              const kvgqa_tensor* positions, const kvgqa_tensor* cache_rows, double theta,
+                              float scale, const kvgqa_tensor* k_cache, const kvgqa_tensor* v_cache,
+                              const kvgqa_tensor* out, const kvgqa_tensor* workspace, void* stream) {
+  return guarded([&] {
+    decode_step_body(q, k, v, positions, cache_rows, theta, scale, k_cache, v_cache, out, workspace, stream, false);
+  });
+}
+
+kvgqa_status decode_step_single_launch_out_(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tensor* v,
+                                            const kvgqa_tensor* positions, const kvgqa_tensor* cache_rows,
+                                            double theta, float scale, const kvgqa_tensor* k_cache,
+                                            const kvgqa_tensor* v_cache, const kvgqa_tensor* out,
+                                            const kvgqa_tensor* workspace, void* stream) {
+  return guarded([&] {
+    decode_step_body(q, k, v, positions, cache_rows, theta, scale, k_cache, v_cache, out, workspace, stream, true);
   });
 }
 

@@ -286,10 +286,11 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* ptr, int v) {
   return old;
 }
 
-template <int D, int GP, bool FUSED>
+template <int D, int GP, bool FUSED, bool EARLY>
 __global__ void __launch_bounds__(threads_of(FUSED), 1)
 flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap map_k,
                            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_q) {
+  static_assert(!(FUSED && EARLY), "the fused step has no store kernel before it");
   using C = Cfg<D, FUSED>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -333,7 +334,16 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     *abort_flag = 0;
     fence_mbar_init();
   }
-  pdl_wait();     // everything below may read what the previous kernel wrote
+  if (threadIdx.x == 32 * 4) {  // the producer's descriptors, fetched while the CTA sets up
+    tma_prefetch_map(&map_k);
+    tma_prefetch_map(&map_v);
+    tma_prefetch_map(&map_q);
+  }
+  // Everything past pdl_wait() may read what the previous kernel wrote.  With
+  // an early start only the producer waits, before the first query tile or
+  // tile with a new cell it loads: the positions and rows read here are inputs
+  // of the whole step, which its store kernel does not write.
+  if constexpr (!EARLY) pdl_wait();
   pdl_trigger();  // the next kernel in the stream may launch and set itself up
   build_prefix(p, prefix, nkeys, blockIdx.x == 0);  // ends with __syncthreads
 
@@ -363,6 +373,43 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       if constexpr (!FUSED) {
         // each tile brings its K and V rows and the segment's rotated query tile
         int it = 0;
+        // Early start: the K/V rows of the first tiles (at most one per stage,
+        // up to the first that holds a new cell) are loaded before waiting for
+        // the store kernel, their query tiles right after it.
+        if constexpr (EARLY) {
+          Cursor c = cur;
+          int qrow[C::NS];
+          int n_early = 0;
+#pragma unroll
+          for (int i = 0; i < C::NS; ++i) {
+            qrow[i] = 0;
+            if (n_early == i && c.more() && !(c.last() && c.x_end == c.n)) {
+              const int nb = (c.nt() + BOX_ROWS - 1) / BOX_ROWS;
+              unsigned char* st = smem + i * C::STAGE;
+              const int kv_row = p.cache_rows[c.a] * p.H_kv + c.g;
+              mbar_arrive_expect_tx(&kv_full[i], static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + QSUB));
+              for (int sub = 0; sub < C::NSUB; ++sub)
+                for (int b = 0; b < nb; ++b) {
+                  tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, c.k0() + b * BOX_ROWS,
+                              kv_row, &kv_full[i], pol_kv);
+                  tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, c.k0() + b * BOX_ROWS,
+                              kv_row, &kv_full[i], pol_kv);
+                }
+              qrow[i] = c.a * p.H_q + c.g * p.G;
+              c.advance();
+              ++n_early;
+            }
+          }
+          pdl_wait();
+#pragma unroll
+          for (int i = 0; i < C::NS; ++i)
+            if (i < n_early)
+              for (int sub = 0; sub < C::NSUB; ++sub)
+                tma_load_3d(smem + i * C::STAGE + C::Q_OFF + sub * QSUB, &map_q, sub * 64, qrow[i], 0, &kv_full[i],
+                            pol_q);
+          cur = c;
+          it = n_early;
+        }
         for (; cur.more(); cur.advance(), ++it) {
           const int s = it % C::NS;
           if (it >= C::NS && !mbar_wait_bounded(&kv_empty[s], ((it / C::NS) - 1) & 1, abort_flag, p.status)) break;
@@ -805,10 +852,13 @@ struct Kernels {
     static int ctas[64];
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::call_once(flags[device], [&]() {
-      errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP, false>,
+      errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP, false, false>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, false>::SMEM);
       if (errs[device] == cudaSuccess)
-        errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP, true>,
+        errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP, false, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, false>::SMEM);
+      if (errs[device] == cudaSuccess)
+        errs[device] = cudaFuncSetAttribute(flash_decode_splitk_kernel<D, GP, true, false>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, true>::SMEM);
       int sms = 0;
       if (errs[device] == cudaSuccess)
@@ -818,7 +868,7 @@ struct Kernels {
     *num_ctas = ctas[device];
     return errs[device];
   }
-  template <bool FUSED>
+  template <bool FUSED, bool EARLY>
   static cudaError_t launch_mode(const DecodeParams& p, const DecodeMaps& m, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -830,10 +880,11 @@ struct Kernels {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP, FUSED>, p, m.kc, m.vc, m.q);
+    return cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP, FUSED, EARLY>, p, m.kc, m.vc, m.q);
   }
   static cudaError_t launch(const DecodeParams& p, const DecodeMaps& m, cudaStream_t stream) {
-    return p.fused ? launch_mode<true>(p, m, stream) : launch_mode<false>(p, m, stream);
+    if (p.fused) return launch_mode<true, false>(p, m, stream);
+    return p.early ? launch_mode<false, true>(p, m, stream) : launch_mode<false, false>(p, m, stream);
   }
 };
 

@@ -32,9 +32,10 @@ struct RopeStoreParams {
   double inv_freq[kMaxHeadDim / 2];  // theta^(-2i/D), computed on the host in double
 };
 
-// mode 0: decode (one CTA per token at positions[a]); 1: equal-length prefill
-// (one CTA per position 0..T-1, all prompts); 2: varlen prefill (one CTA per
-// (prompt, token), token t of prompt a at offsets[a] + t, t < lengths[a]).
+// mode 0: decode (token a at positions[a]); 1: equal-length prefill (one CTA
+// per position 0..T-1, all prompts); 2: varlen prefill (token t of prompt a at
+// offsets[a] + t, t < lengths[a]).  Modes 0 and 2 give each token four CTAs,
+// each with a quarter of the frequencies (H_kv * D / 8 must divide by 4).
 cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_t stream);
 
 // ------------------------------------------------------------------ decode attention
@@ -51,6 +52,11 @@ struct DecodeParams {
   int A, H_q, H_kv, G, D, S, max_seq;
   int num_ctas;               // grid size of the split-K kernel
   float scale_log2;           // scale * log2(e)
+  // Early start (whole-step call only, where the previous kernel in the
+  // stream is that call's own store kernel, which writes only the rotated
+  // queries and each active row's new cell): cache tiles without a new cell
+  // are loaded before the store kernel ends.
+  int early;
   // Fused decode step only (fused != 0): the kernel rotates q itself and
   // stores the rotated new K and raw new V into each row's cell at positions[a].
   int fused;

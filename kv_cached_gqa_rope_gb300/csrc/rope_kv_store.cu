@@ -8,14 +8,20 @@
 // and a positive base.  The same kernel serves the prefill into empty rows,
 // where token (a, t) sits at position t of row cache_rows[a].
 //
-// One CTA owns one position.  It evaluates the D/2 angles pos * theta^(-2i/D)
-// once, in FP64, and keeps cos/sin as FP32 hi+lo pairs in shared memory; every
-// token at that position (one in decode, A in prefill) then streams its heads
-// through 16-byte vector loads and stores.  The rotation is evaluated with
-// FP32 error-free products so that the BF16 result is within one rounding of
-// the exact value even where x cos - y sin cancels.
+// Equal-length prefill: one CTA owns one position.  It evaluates the D/2
+// angles pos * theta^(-2i/D) once, in FP64, and keeps cos/sin as FP32 hi+lo
+// pairs in shared memory; the A tokens at that position then stream their
+// heads through 16-byte vector loads and stores.  Decode and the prefill of
+// prompts at offsets (one position per token): kTokenSplit CTAs share a token,
+// each owning a quarter of the frequencies of every head (and a quarter of its
+// V bytes), so that the FP64 angle work of a token is spread over four SMs;
+// each CTA issues its loads before it evaluates its angles.  The rotation is
+// evaluated with FP32 error-free products so that the BF16 result is within
+// one rounding of the exact value even where x cos - y sin cancels.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "kvgqa_internal.h"
 #include "ptx.cuh"
@@ -54,8 +60,7 @@ __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const Co
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_constant__ RopeStoreParams p,
-                                                            int mode) {
+__global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_constant__ RopeStoreParams p) {
   constexpr int HALF = D / 2;
   constexpr int RU = D / 16;  // rotation units per head: 8 pairs each
   constexpr int VU = D / 8;   // copy units per head: 8 elements (16 bytes) each
@@ -63,40 +68,8 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
 
   pdl_wait();     // inputs and outputs may belong to the previous kernel
   pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
-  const bool prefill = mode == 1;
-  int pos, ntok, a0 = 0;  // a0: the token's prompt (decode and varlen modes)
-  size_t tok0 = 0;        // its index in the token-major inputs
-  if (mode == 1) {
-    pos = blockIdx.x;  // position t, shared by all A prompts
-    ntok = p.A;
-  } else {
-    ntok = 1;
-    if (mode == 0) {
-      a0 = blockIdx.x;
-      tok0 = a0;
-      pos = p.positions[a0];
-    } else {
-      a0 = blockIdx.x / p.T;
-      const int t = blockIdx.x % p.T;
-      tok0 = blockIdx.x;
-      const int off = p.offsets[a0], len = p.lengths[a0];
-      const bool meta_ok = len >= 0 && len <= p.T && off >= 0 && off <= p.max_seq - len;
-      if (meta_ok && t >= len) return;  // past this prompt's tokens
-      if (!meta_ok) {
-        if (threadIdx.x == 0 && t == 0) atomicOr(p.status, KVGQA_FLAG_POSITION_RANGE);
-        return;
-      }
-      pos = off + t;
-    }
-    const int row = p.cache_rows[a0];
-    const bool pos_ok = pos >= 0 && pos < p.max_seq;
-    const bool row_ok = row >= 0 && row < p.S;
-    if (!pos_ok || !row_ok) {
-      if (threadIdx.x == 0 && (mode == 0 || blockIdx.x % p.T == 0))
-        atomicOr(p.status, (pos_ok ? 0 : KVGQA_FLAG_POSITION_RANGE) | (row_ok ? 0 : KVGQA_FLAG_ROW_RANGE));
-      return;
-    }
-  }
+  const int pos = blockIdx.x;  // position t, shared by all A prompts
+  const int ntok = p.A;
 
   for (int i = threadIdx.x; i < HALF; i += blockDim.x) cs[cs_slot(i)] = rope_cos_sin(pos, p.inv_freq[i]);
   __syncthreads();
@@ -107,7 +80,7 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
   // overlap (one at a time, the loop is bound by load latency, not bandwidth).
   // Prefill tokens whose cache row is out of range are skipped and flagged.
   constexpr int kBatch = 4;
-  if (prefill && blockIdx.x == 0) {
+  if (blockIdx.x == 0) {
     for (int a = threadIdx.x; a < ntok; a += blockDim.x) {
       const int row = p.cache_rows[a];
       if (row < 0 || row >= p.S) atomicOr(p.status, KVGQA_FLAG_ROW_RANGE);
@@ -125,10 +98,10 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
       dst[u] = nullptr;
       if (r >= n_rot) continue;
       const int ti = r / rot_units, rr = r % rot_units;
-      const int a = prefill ? ti : a0;
+      const int a = ti;
       const int row = p.cache_rows[a];
       if (row < 0 || row >= p.S) continue;
-      const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : tok0;
+      const size_t tok = static_cast<size_t>(a) * p.T + pos;
       const int h = rr / RU, c = rr % RU;
       const uint16_t* src;
       if (h < p.H_q) {
@@ -163,10 +136,10 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
       dst[u] = nullptr;
       if (r >= n_copy) continue;
       const int ti = r / copy_units, rr = r % copy_units;
-      const int a = prefill ? ti : a0;
+      const int a = ti;
       const int row = p.cache_rows[a];
       if (row < 0 || row >= p.S) continue;
-      const size_t tok = prefill ? static_cast<size_t>(a) * p.T + pos : tok0;
+      const size_t tok = static_cast<size_t>(a) * p.T + pos;
       const int g = rr / VU, c = rr % VU;
       dst[u] = p.v_cache + ((static_cast<size_t>(row) * p.H_kv + g) * p.max_seq + pos) * D + c * 8;
       x[u] = *reinterpret_cast<const uint4*>(p.v + (tok * p.H_kv + g) * D + c * 8);
@@ -177,24 +150,163 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
   }
 }
 
+constexpr int kTokenSplit = 4;     // CTAs per token (decode, prompts at offsets)
+constexpr int kTokenThreads = 128;
+
+// One token at its own position: decode (token a at positions[a], varlen = 0)
+// or the prefill of prompts at offsets (token t of prompt a at offsets[a] + t,
+// t < lengths[a], varlen = 1).  CTA part s of the token rotates the pairs of
+// frequencies [s*F, s*F + F) of every Q and K head, F = D/2 / kTokenSplit, and
+// copies part s of its V bytes.
+template <int D>
+__global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(const __grid_constant__ RopeStoreParams p,
+                                                                          int varlen) {
+  constexpr int HALF = D / 2;
+  constexpr int F = HALF / kTokenSplit;  // frequencies of this CTA
+  constexpr int UF = F / 8;              // rotation units (8 pairs) per head
+  constexpr int VU = D / 8;              // V copy units (16 bytes) per head
+  constexpr int kBatch = 2;
+  static_assert(F % 8 == 0, "a CTA's frequencies are whole 16-byte units");
+  __shared__ CosSin cs[F + F / 8];
+
+  pdl_wait();     // inputs and outputs may belong to the previous kernel
+  pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
+  const int tk = blockIdx.x / kTokenSplit, part = blockIdx.x % kTokenSplit;
+  const size_t tok = tk;  // index in the token-major inputs
+  const int rot_items = (p.H_q + p.H_kv) * UF;
+  const int copy_per_part = p.H_kv * VU / kTokenSplit;
+  const int n_items = rot_items + copy_per_part;
+
+  // Item j < rot_items: unit part*UF + j%UF of head j/UF (Q heads, then K
+  // heads); otherwise V copy unit part*copy_per_part + (j - rot_items).  The
+  // loads of the first round do not depend on the position or the row, so
+  // they are issued before the metadata and the angles are known.
+  auto load = [&](int j, uint4& xa, uint4& xb) {
+    if (j < rot_items) {
+      const int h = j / UF, c = part * UF + j % UF;
+      const uint16_t* src = h < p.H_q ? p.q + (tok * p.H_q + h) * D : p.k + (tok * p.H_kv + (h - p.H_q)) * D;
+      xa = *reinterpret_cast<const uint4*>(src + c * 8);
+      xb = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
+    } else {
+      const int u = part * copy_per_part + (j - rot_items);
+      xa = *reinterpret_cast<const uint4*>(p.v + (tok * p.H_kv + u / VU) * D + (u % VU) * 8);
+    }
+  };
+  uint4 xa[kBatch], xb[kBatch];
+#pragma unroll
+  for (int b = 0; b < kBatch; ++b) {
+    const int j = threadIdx.x + b * kTokenThreads;
+    if (j < n_items) load(j, xa[b], xb[b]);
+  }
+
+  int a, pos;
+  if (!varlen) {
+    a = tk;
+    pos = p.positions[a];
+  } else {
+    a = tk / p.T;
+    const int t = tk % p.T;
+    const int off = p.offsets[a], len = p.lengths[a];
+    const bool meta_ok = len >= 0 && len <= p.T && off >= 0 && off <= p.max_seq - len;
+    if (meta_ok && t >= len) return;  // past this prompt's tokens
+    if (!meta_ok) {
+      if (threadIdx.x == 0 && t == 0 && part == 0) atomicOr(p.status, KVGQA_FLAG_POSITION_RANGE);
+      return;
+    }
+    pos = off + t;
+  }
+  const int row = p.cache_rows[a];
+  const bool pos_ok = pos >= 0 && pos < p.max_seq;
+  const bool row_ok = row >= 0 && row < p.S;
+  if (!pos_ok || !row_ok) {
+    if (threadIdx.x == 0 && part == 0 && (!varlen || tk % p.T == 0))
+      atomicOr(p.status, (pos_ok ? 0 : KVGQA_FLAG_POSITION_RANGE) | (row_ok ? 0 : KVGQA_FLAG_ROW_RANGE));
+    return;
+  }
+
+  for (int i = threadIdx.x; i < F; i += kTokenThreads) cs[cs_slot(i)] = rope_cos_sin(pos, p.inv_freq[part * F + i]);
+  __syncthreads();
+
+  auto store = [&](int j, const uint4& va, const uint4& vb) {
+    if (j < rot_items) {
+      const int h = j / UF, cl = j % UF, c = part * UF + cl;
+      uint16_t* dst = h < p.H_q ? p.q_out + (tok * p.H_q + h) * D
+                                : p.k_cache + ((static_cast<size_t>(row) * p.H_kv + (h - p.H_q)) * p.max_seq + pos) * D;
+      uint4 ya, yb;
+      rotate8(va, vb, cs + cs_slot(cl * 8), ya, yb);
+      *reinterpret_cast<uint4*>(dst + c * 8) = ya;
+      *reinterpret_cast<uint4*>(dst + HALF + c * 8) = yb;
+    } else {
+      const int u = part * copy_per_part + (j - rot_items);
+      *reinterpret_cast<uint4*>(p.v_cache + ((static_cast<size_t>(row) * p.H_kv + u / VU) * p.max_seq + pos) * D +
+                                (u % VU) * 8) = va;
+    }
+  };
+#pragma unroll
+  for (int b = 0; b < kBatch; ++b) {
+    const int j = threadIdx.x + b * kTokenThreads;
+    if (j < n_items) store(j, xa[b], xb[b]);
+  }
+  // more heads than one round covers: the rest, loads first in each round
+  for (int base = threadIdx.x + kBatch * kTokenThreads; base < n_items; base += kBatch * kTokenThreads) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int j = base + b * kTokenThreads;
+      if (j < n_items) load(j, xa[b], xb[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int j = base + b * kTokenThreads;
+      if (j < n_items) store(j, xa[b], xb[b]);
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_t stream) {
-  const long long g = mode == 0 ? p.A : mode == 1 ? p.T : static_cast<long long>(p.A) * p.T;
+  const long long g = mode == 1 ? p.T : (mode == 0 ? p.A : static_cast<long long>(p.A) * p.T) * kTokenSplit;
   if (g > 0x7fffffffll) return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(g);
   if (grid == 0) return cudaSuccess;
+  if ((p.H_kv * (p.D / 8)) % kTokenSplit) return cudaErrorInvalidValue;  // V bytes split in whole units
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(mode == 1 ? 256 : kTokenThreads);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.D == 128) return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<128>, p, mode);
-  if (p.D == 64) return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<64>, p, mode);
+  // The attention kernel that follows (programmatic launch) needs most of an
+  // SM's shared memory; with the store kernel's CTAs in the shared-memory-
+  // heavy split it can start on their SMs while they run.
+  static std::once_flag carveout_once[64];
+  static cudaError_t carveout_err[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(carveout_once[dev], [dev] {
+    const void* fns[4] = {reinterpret_cast<const void*>(rope_kv_store_kernel<128>),
+                          reinterpret_cast<const void*>(rope_kv_store_kernel<64>),
+                          reinterpret_cast<const void*>(rope_kv_store_token_kernel<128>),
+                          reinterpret_cast<const void*>(rope_kv_store_token_kernel<64>)};
+    carveout_err[dev] = cudaSuccess;
+    for (const void* f : fns)
+      if (carveout_err[dev] == cudaSuccess)
+        carveout_err[dev] = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                 cudaSharedmemCarveoutMaxShared);
+  });
+  if (carveout_err[dev] != cudaSuccess) return carveout_err[dev];
+  const int varlen = mode == 2;
+  if (p.D == 128)
+    return mode == 1 ? cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<128>, p)
+                     : cudaLaunchKernelEx(&cfg, rope_kv_store_token_kernel<128>, p, varlen);
+  if (p.D == 64)
+    return mode == 1 ? cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<64>, p)
+                     : cudaLaunchKernelEx(&cfg, rope_kv_store_token_kernel<64>, p, varlen);
   return cudaErrorInvalidValue;
 }
 

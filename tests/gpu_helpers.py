@@ -118,12 +118,14 @@ def oracle_attention(inp: W.DecodeInputs, rows, heads=None, q_rot_bits=None, ext
     return oracle.cached_gqa_attention(q, kc_b, vc_b, pos, np.arange(len(rows)), wl.scale, heads=heads)
 
 
-def fused_step(run: DecodeRun, out=None, ws=None):
-    """decode_step_out_ on the buffers of `run` (its own workspace by default)."""
+def whole_step(run: DecodeRun, out=None, ws=None, single_launch=False):
+    """decode_step_out_ (or its single-launch form) on the buffers of `run`
+    (its own workspace by default)."""
     kv, wl = run.kv, run.inp.wl
     if ws is None:
         if not hasattr(run, "ws_step"):
             run.ws_step = kv.new_workspace(kv.decode_step_workspace_size(wl.A, wl.H_q, wl.H_kv, wl.D))
         ws = run.ws_step
-    kv.decode_step_out_(run.q, run.k, run.v, run.positions, run.cache_rows, wl.theta, wl.scale,
-                        run.k_cache, run.v_cache, run.out if out is None else out, ws)
+    fn = kv.decode_step_single_launch_out_ if single_launch else kv.decode_step_out_
+    fn(run.q, run.k, run.v, run.positions, run.cache_rows, wl.theta, wl.scale,
+       run.k_cache, run.v_cache, run.out if out is None else out, ws)
