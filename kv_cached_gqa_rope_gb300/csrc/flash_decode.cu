@@ -375,39 +375,36 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         int it = 0;
         // Early start: the K/V rows of the first tiles (at most one per stage,
         // up to the first that holds a new cell) are loaded before waiting for
-        // the store kernel, their query tiles right after it.
+        // the store kernel, their query tiles right after it.  The loops stay
+        // rolled: unrolled, this once-per-CTA code measured about 4 us slower
+        // over the whole kernel on GB300.
         if constexpr (EARLY) {
-          Cursor c = cur;
           int qrow[C::NS];
           int n_early = 0;
-#pragma unroll
-          for (int i = 0; i < C::NS; ++i) {
-            qrow[i] = 0;
-            if (n_early == i && c.more() && !(c.last() && c.x_end == c.n)) {
-              const int nb = (c.nt() + BOX_ROWS - 1) / BOX_ROWS;
-              unsigned char* st = smem + i * C::STAGE;
-              const int kv_row = p.cache_rows[c.a] * p.H_kv + c.g;
-              mbar_arrive_expect_tx(&kv_full[i], static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + QSUB));
-              for (int sub = 0; sub < C::NSUB; ++sub)
-                for (int b = 0; b < nb; ++b) {
-                  tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, c.k0() + b * BOX_ROWS,
-                              kv_row, &kv_full[i], pol_kv);
-                  tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, c.k0() + b * BOX_ROWS,
-                              kv_row, &kv_full[i], pol_kv);
-                }
-              qrow[i] = c.a * p.H_q + c.g * p.G;
-              c.advance();
-              ++n_early;
-            }
+#pragma unroll 1
+          for (; n_early < C::NS && cur.more() && !(cur.last() && cur.x_end == cur.n); cur.advance(), ++n_early) {
+            const int nb = (cur.nt() + BOX_ROWS - 1) / BOX_ROWS;
+            unsigned char* st = smem + n_early * C::STAGE;
+            const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
+            mbar_arrive_expect_tx(&kv_full[n_early], static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + QSUB));
+#pragma unroll 1
+            for (int sub = 0; sub < C::NSUB; ++sub)
+#pragma unroll 1
+              for (int b = 0; b < nb; ++b) {
+                tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
+                            kv_row, &kv_full[n_early], pol_kv);
+                tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
+                            kv_row, &kv_full[n_early], pol_kv);
+              }
+            qrow[n_early] = cur.a * p.H_q + cur.g * p.G;
           }
           pdl_wait();
-#pragma unroll
-          for (int i = 0; i < C::NS; ++i)
-            if (i < n_early)
-              for (int sub = 0; sub < C::NSUB; ++sub)
-                tma_load_3d(smem + i * C::STAGE + C::Q_OFF + sub * QSUB, &map_q, sub * 64, qrow[i], 0, &kv_full[i],
-                            pol_q);
-          cur = c;
+#pragma unroll 1
+          for (int i = 0; i < n_early; ++i)
+#pragma unroll 1
+            for (int sub = 0; sub < C::NSUB; ++sub)
+              tma_load_3d(smem + i * C::STAGE + C::Q_OFF + sub * QSUB, &map_q, sub * 64, qrow[i], 0, &kv_full[i],
+                          pol_q);
           it = n_early;
         }
         for (; cur.more(); cur.advance(), ++it) {

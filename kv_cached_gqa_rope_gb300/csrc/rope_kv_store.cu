@@ -279,9 +279,11 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // The attention kernel that follows (programmatic launch) needs most of an
-  // SM's shared memory; with the store kernel's CTAs in the shared-memory-
-  // heavy split it can start on their SMs while they run.
+  // The decode attention kernel that follows (programmatic launch) needs most
+  // of an SM's shared memory; with the per-token store CTAs in the
+  // shared-memory-heavy split it can start on their SMs while they run.  (The
+  // prefill attention kernel cannot share an SM with store CTAs anyway: it
+  // takes the whole register file.)
   static std::once_flag carveout_once[64];
   static cudaError_t carveout_err[64];
   int dev = 0;
@@ -289,9 +291,7 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::call_once(carveout_once[dev], [dev] {
-    const void* fns[4] = {reinterpret_cast<const void*>(rope_kv_store_kernel<128>),
-                          reinterpret_cast<const void*>(rope_kv_store_kernel<64>),
-                          reinterpret_cast<const void*>(rope_kv_store_token_kernel<128>),
+    const void* fns[2] = {reinterpret_cast<const void*>(rope_kv_store_token_kernel<128>),
                           reinterpret_cast<const void*>(rope_kv_store_token_kernel<64>)};
     carveout_err[dev] = cudaSuccess;
     for (const void* f : fns)
