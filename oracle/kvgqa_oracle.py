@@ -23,9 +23,11 @@ numpy operations (a matrix product is the only library primitive used):
   hold a prefix (chunked prefill; prompts of other lengths form separate
   groups there, one call here).
 
-Storage is BF16 (16-bit patterns in numpy ``uint16`` arrays); arithmetic is
-float64; results that the path stores as BF16 are rounded once, directly from
-float64, to nearest-even.
+Storage is BF16 (16-bit patterns in numpy ``uint16`` arrays), or IEEE
+binary16 where a function is given ``fmt="f16"`` (the FP16 cached rows the
+pages' typed softmax also serves); arithmetic is float64; results that the
+path stores are rounded once, directly from float64, to nearest-even in the
+storage format.
 
 Readings taken where the pages are silent (each is listed in the design doc):
   - pair i of a head is (x[i], x[i + D/2]) and rotates by angle pos * theta^(-2i/D),
@@ -48,7 +50,7 @@ __all__ = [
     "bf16_to_f64", "f64_to_bf16", "rope_inv_freq", "rope_split_half",
     "rope_split_half_bf16", "rope_kv_store", "cached_gqa_attention",
     "cached_gqa_attention_one", "prefill_gqa_cached_rows", "prefill_varlen_gqa_cached_rows",
-    "prefill_attention_one", "ulp_distance_bf16",
+    "prefill_attention_one", "ulp_distance_bf16", "f16_to_f64", "f64_to_f16", "widen", "codec",
 ]
 
 
@@ -82,9 +84,46 @@ def f64_to_bf16(x) -> np.ndarray:
     return bits.astype(np.uint16)
 
 
+def f16_to_f64(bits) -> np.ndarray:
+    """IEEE binary16 bit patterns -> float64 (exact: every half value is a
+    double; the widening is numpy's, which preserves the value)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def f64_to_f16(x) -> np.ndarray:
+    """Round float64 values to IEEE binary16, nearest-even, in one step.
+
+    Binary16 keeps 11 significant bits, normal numbers from 2^-14, subnormal
+    spacing 2^-24, largest finite 65504.  As for BF16: scale so that the last
+    kept bit has weight 1, round with ``np.rint`` (ties to even), scale back.
+    A result above 65504 (from 65520 up) is out of range and becomes infinity.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    _, e = np.frexp(ax)                       # ax = m * 2^e, m in [0.5, 1)
+    quantum = np.maximum(e - 11, -24)
+    y = np.ldexp(np.rint(np.ldexp(ax, -quantum)), quantum)
+    y = np.where(y > 65504.0, np.inf, y)
+    with np.errstate(over="ignore", invalid="ignore"):
+        bits = y.astype(np.float16).view(np.uint16)   # exact: y is a binary16 value or inf
+    bits = np.where(np.isnan(x), np.uint16(0x7E00), bits)
+    bits = np.where(np.signbit(x), bits | np.uint16(0x8000), bits)
+    return bits.astype(np.uint16)
+
+
+def codec(fmt: str):
+    """(widen, round) of a storage format: "bf16" or "f16"."""
+    return {"bf16": (bf16_to_f64, f64_to_bf16), "f16": (f16_to_f64, f64_to_f16)}[fmt]
+
+
+def widen(bits, fmt: str = "bf16") -> np.ndarray:
+    return codec(fmt)[0](bits)
+
+
 def ulp_distance_bf16(a_bits, b_bits) -> np.ndarray:
     """Distance between BF16 patterns counted in representable values
-    (ordered-integer difference; +0 and -0 are the same point)."""
+    (ordered-integer difference; +0 and -0 are the same point).  The same
+    ordering holds for binary16 patterns, so it serves both formats."""
     def ordered(b):
         b = np.asarray(b, dtype=np.uint16).astype(np.int64)
         mag = b & 0x7FFF
@@ -122,13 +161,15 @@ def rope_split_half(x, positions, theta: float) -> np.ndarray:
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
-def rope_split_half_bf16(x_bits, positions, theta: float) -> np.ndarray:
-    """BF16 in, BF16 out: widen, rotate in float64, round once."""
-    return f64_to_bf16(rope_split_half(bf16_to_f64(x_bits), positions, theta))
+def rope_split_half_bf16(x_bits, positions, theta: float, fmt: str = "bf16") -> np.ndarray:
+    """Stored format in, stored format out (BF16 unless ``fmt`` says "f16"):
+    widen, rotate in float64, round once."""
+    to64, round16 = codec(fmt)
+    return round16(rope_split_half(to64(x_bits), positions, theta))
 
 
 # ---------------------------------------------------------------- decode store
-def rope_kv_store(q, k, v, positions, cache_rows, theta, k_cache, v_cache):
+def rope_kv_store(q, k, v, positions, cache_rows, theta, k_cache, v_cache, fmt="bf16"):
     """Decode RoPE + K/V store for A active tokens.
 
     q [A, H_q, D], k/v [A, H_kv, D] (BF16 bits); positions, cache_rows [A];
@@ -145,8 +186,8 @@ def rope_kv_store(q, k, v, positions, cache_rows, theta, k_cache, v_cache):
         raise ValueError("position or cache row out of range")
     if len(set(rows.tolist())) != len(rows):
         raise ValueError("cache rows of one step must be distinct")
-    q_rot = rope_split_half_bf16(q, positions[:, None], theta)
-    k_rot = rope_split_half_bf16(k, positions[:, None], theta)
+    q_rot = rope_split_half_bf16(q, positions[:, None], theta, fmt)
+    k_rot = rope_split_half_bf16(k, positions[:, None], theta, fmt)
     kc = np.array(k_cache, dtype=np.uint16, copy=True)
     vc = np.array(v_cache, dtype=np.uint16, copy=True)
     for a in range(len(rows)):
@@ -170,7 +211,7 @@ def cached_gqa_attention_one(q_vec, keys, values, scale: float) -> np.ndarray:
 
 
 def cached_gqa_attention(q_rot, k_cache, v_cache, positions, cache_rows,
-                         scale: float, heads=None) -> np.ndarray:
+                         scale: float, heads=None, fmt="bf16") -> np.ndarray:
     """Cached GQA attention of the decode step, float64 result.
 
     Token a, query head h attends to keys 0..positions[a] (inclusive) of KV head
@@ -185,21 +226,21 @@ def cached_gqa_attention(q_rot, k_cache, v_cache, positions, cache_rows,
     pairs = [(a, h) for a in range(A) for h in range(H_q)] if heads is None else heads
     for a, h in pairs:
         r, p, g = int(cache_rows[a]), int(positions[a]), h // G
-        keys = bf16_to_f64(k_cache[r, g, : p + 1])
-        vals = bf16_to_f64(v_cache[r, g, : p + 1])
-        out[a, h] = cached_gqa_attention_one(bf16_to_f64(q_rot[a, h]), keys, vals, scale)
+        keys = widen(k_cache[r, g, : p + 1], fmt)
+        vals = widen(v_cache[r, g, : p + 1], fmt)
+        out[a, h] = cached_gqa_attention_one(widen(q_rot[a, h], fmt), keys, vals, scale)
     return out
 
 
 # ---------------------------------------------------------------- prefill
-def prefill_attention_one(q_rot_bits, k_rows, v_rows, t: int, scale: float) -> np.ndarray:
+def prefill_attention_one(q_rot_bits, k_rows, v_rows, t: int, scale: float, fmt="bf16") -> np.ndarray:
     """Causal attention of prompt position t over cached positions 0..t."""
-    return cached_gqa_attention_one(bf16_to_f64(q_rot_bits), bf16_to_f64(k_rows[: t + 1]),
-                                    bf16_to_f64(v_rows[: t + 1]), scale)
+    return cached_gqa_attention_one(widen(q_rot_bits, fmt), widen(k_rows[: t + 1], fmt),
+                                    widen(v_rows[: t + 1], fmt), scale)
 
 
 def prefill_gqa_cached_rows(q, k, v, cache_rows, theta, scale, k_cache, v_cache,
-                            select=None):
+                            select=None, fmt="bf16"):
     """Equal-length prefill of A prompts into empty cache rows.
 
     q [A, T, H_q, D], k/v [A, T, H_kv, D] (BF16 bits, token-major BTHD), positions
@@ -221,8 +262,8 @@ def prefill_gqa_cached_rows(q, k, v, cache_rows, theta, scale, k_cache, v_cache,
     if np.any((rows < 0) | (rows >= S)) or len(set(rows.tolist())) != len(rows):
         raise ValueError("cache rows must be distinct and in range")
     pos = np.arange(T)
-    q_rot = rope_split_half_bf16(q, pos[None, :, None], theta)
-    k_rot = rope_split_half_bf16(k, pos[None, :, None], theta)
+    q_rot = rope_split_half_bf16(q, pos[None, :, None], theta, fmt)
+    k_rot = rope_split_half_bf16(k, pos[None, :, None], theta, fmt)
     kc = np.array(k_cache, dtype=np.uint16, copy=True)
     vc = np.array(v_cache, dtype=np.uint16, copy=True)
     for a in range(A):
@@ -234,9 +275,9 @@ def prefill_gqa_cached_rows(q, k, v, cache_rows, theta, scale, k_cache, v_cache,
         for a in range(A):
             for h in range(H_q):
                 g = h // G
-                Q = bf16_to_f64(q_rot[a, :, h])
-                K = bf16_to_f64(kc[rows[a], g, :T])
-                V = bf16_to_f64(vc[rows[a], g, :T])
+                Q = widen(q_rot[a, :, h], fmt)
+                K = widen(kc[rows[a], g, :T], fmt)
+                V = widen(vc[rows[a], g, :T], fmt)
                 s = (Q @ K.T) * scale
                 s = np.where(mask, s, -np.inf)
                 out[a, :, h] = softmax(s) @ V
@@ -244,12 +285,12 @@ def prefill_gqa_cached_rows(q, k, v, cache_rows, theta, scale, k_cache, v_cache,
         for a, t, h in select:
             g = h // G
             out[a, t, h] = prefill_attention_one(q_rot[a, t, h], kc[rows[a], g, :T],
-                                                 vc[rows[a], g, :T], t, scale)
+                                                 vc[rows[a], g, :T], t, scale, fmt)
     return q_rot, out, kc, vc
 
 
 def prefill_varlen_gqa_cached_rows(q, k, v, offsets, lengths, cache_rows, theta, scale, k_cache, v_cache,
-                                   select=None):
+                                   select=None, fmt="bf16"):
     """Prefill of A prompts of different lengths into rows that may already
     hold a prefix (chunked prefill).
 
@@ -287,8 +328,8 @@ def prefill_varlen_gqa_cached_rows(q, k, v, offsets, lengths, cache_rows, theta,
     for a in range(A):
         L, o = int(lens[a]), int(off[a])
         pos = o + np.arange(L)
-        q_rot[a, :L] = rope_split_half_bf16(q[a, :L], pos[:, None], theta)
-        k_rot = rope_split_half_bf16(k[a, :L], pos[:, None], theta)
+        q_rot[a, :L] = rope_split_half_bf16(q[a, :L], pos[:, None], theta, fmt)
+        k_rot = rope_split_half_bf16(k[a, :L], pos[:, None], theta, fmt)
         kc[rows[a], :, o:o + L, :] = np.transpose(k_rot, (1, 0, 2))
         vc[rows[a], :, o:o + L, :] = np.transpose(v[a, :L], (1, 0, 2))
     out = np.full((A, T, H_q, D), np.nan)
@@ -301,9 +342,9 @@ def prefill_varlen_gqa_cached_rows(q, k, v, offsets, lengths, cache_rows, theta,
             mask = np.arange(n)[None, :] <= (o + np.arange(L))[:, None]   # key j visible to query t
             for h in range(H_q):
                 g = h // G
-                Q = bf16_to_f64(q_rot[a, :L, h])
-                K = bf16_to_f64(kc[rows[a], g, :n])
-                V = bf16_to_f64(vc[rows[a], g, :n])
+                Q = widen(q_rot[a, :L, h], fmt)
+                K = widen(kc[rows[a], g, :n], fmt)
+                V = widen(vc[rows[a], g, :n], fmt)
                 s = np.where(mask, (Q @ K.T) * scale, -np.inf)
                 out[a, :L, h] = softmax(s) @ V
     else:
@@ -312,6 +353,6 @@ def prefill_varlen_gqa_cached_rows(q, k, v, offsets, lengths, cache_rows, theta,
                 continue
             g = h // G
             p = int(off[a]) + t
-            out[a, t, h] = cached_gqa_attention_one(bf16_to_f64(q_rot[a, t, h]), bf16_to_f64(kc[rows[a], g, :p + 1]),
-                                                    bf16_to_f64(vc[rows[a], g, :p + 1]), scale)
+            out[a, t, h] = cached_gqa_attention_one(widen(q_rot[a, t, h], fmt), widen(kc[rows[a], g, :p + 1], fmt),
+                                                    widen(vc[rows[a], g, :p + 1], fmt), scale)
     return q_rot, out, kc, vc

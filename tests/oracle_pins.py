@@ -67,6 +67,82 @@ def check_bf16_roundtrip(o):
     assert o.bf16_to_f64(np.array([0x7F7F], dtype=np.uint16))[0] == float.fromhex("0x1.fep127")
 
 
+# ------------------------------------------------------------------ binary16 codec
+def check_f16_matches_torch_rounding(o):
+    """For FP32-representable inputs, direct FP64 -> binary16 nearest-even must
+    equal torch's FP32 -> FP16 conversion (a library routine), across normal,
+    subnormal, overflowing and tie inputs."""
+    r = rng(11)
+    mags = np.ldexp(r.uniform(1, 2, 150000), r.integers(-30, 18, 150000))
+    signs = np.where(r.integers(0, 2, 150000) == 1, -1.0, 1.0)
+    x = (signs * mags).astype(np.float32)
+    # ties: 12 significant bits with the last set, at normal and subnormal scales
+    m = (r.integers(2048, 4096, 20000) | 1).astype(np.float64)
+    ties = np.concatenate([np.ldexp(m, r.integers(-20, 5, 20000)), np.ldexp(m, -36)]).astype(np.float32)
+    edge = np.array([65504, 65519.99, 65520, 65536, 2.0**-24, 2.0**-25, 3 * 2.0**-26, 2.0**-14,
+                     2.0**-14 - 2.0**-25, 0.0, -0.0, np.inf, -np.inf], dtype=np.float32)
+    f32 = np.concatenate([x, ties, edge])
+    ref = torch.from_numpy(f32.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    got = o.f64_to_f16(f32.astype(np.float64))
+    assert np.array_equal(got, ref), int(np.sum(got != ref))
+
+
+def check_f16_single_rounding(o):
+    """Hand-derived: 1 + 2^-11 is a tie (-> even, 1.0); 1 + 3*2^-11 is a tie
+    (-> 1 + 2^-9); 1 + 2^-11 + 2^-40 lies above the tie and rounds up to
+    1 + 2^-10, which a detour through FP32 (that drops 2^-40) would miss;
+    65520 overflows to infinity, 65519.99 does not; 2^-25 is a tie between 0
+    and the smallest subnormal (-> 0); 3*2^-26 rounds up to 2^-24."""
+    vals = np.array([1 + 2.0**-11, 1 + 3 * 2.0**-11, 1 + 2.0**-11 + 2.0**-40, -(1 + 2.0**-11 + 2.0**-40),
+                     65520.0, 65519.99, 2.0**-25, 3 * 2.0**-26])
+    want = np.array([0x3C00, 0x3C02, 0x3C01, 0xBC01, 0x7C00, 0x7BFF, 0x0000, 0x0001], dtype=np.uint16)
+    assert np.array_equal(o.f64_to_f16(vals), want), o.f64_to_f16(vals)
+
+
+def check_f16_roundtrip(o):
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = o.f16_to_f64(allbits)
+    ok = ~np.isnan(f)
+    assert np.array_equal(o.f64_to_f16(f[ok]), allbits[ok])
+    assert o.f16_to_f64(np.array([0x3C00], dtype=np.uint16))[0] == 1.0
+    assert o.f16_to_f64(np.array([0x7BFF], dtype=np.uint16))[0] == 65504.0
+    assert o.f16_to_f64(np.array([0x0001], dtype=np.uint16))[0] == 2.0**-24
+
+
+def check_f16_storage_paths(o):
+    """With fmt="f16" the store writes binary16 patterns of the rotated K
+    (a unit vector turned by a known angle, so the exact values are cos/sin
+    rounded once to binary16) and attention reads the cache as binary16:
+    one key returns V exactly, and it equals the BF16 path's result on data
+    that both formats hold exactly (small integers)."""
+    D, pos, theta = 8, 3, 16.0
+    k = np.zeros((1, 1, D))
+    k[0, 0, 0] = 1.0
+    kb = o.f64_to_f16(k)
+    q = o.f64_to_f16(np.zeros((1, 1, D)))
+    kc = np.zeros((1, 1, 8, D), dtype=np.uint16)
+    vc = np.zeros_like(kc)
+    v = o.f64_to_f16(np.arange(D, dtype=np.float64).reshape(1, 1, D))
+    _, kc2, vc2 = o.rope_kv_store(q, kb, v, np.array([pos]), np.array([0]), theta, kc, vc, fmt="f16")
+    phi = pos * 1.0   # frequency of pair 0 is 1
+    want = o.f64_to_f16(np.array([math.cos(phi), 0, 0, 0, math.sin(phi), 0, 0, 0]))
+    assert np.array_equal(kc2[0, 0, pos], want)
+    assert np.array_equal(vc2[0, 0, pos], v[0, 0])
+    out = o.cached_gqa_attention(o.f64_to_f16(np.ones((1, 1, D))), kc2, vc2, np.array([0]), np.array([0]),
+                                 0.5, fmt="f16")
+    assert np.array_equal(out[0, 0], o.f16_to_f64(vc2[0, 0, 0]))
+    ints = np.array([[1.0, -2.0, 3.0, 4.0], [0.5, 2.0, -1.0, 8.0]])
+    a16 = o.f64_to_f16(ints)
+    a_bf = o.f64_to_bf16(ints)
+    assert np.array_equal(o.f16_to_f64(a16), o.bf16_to_f64(a_bf))
+    kcx = a16[None, None]                              # [1 slot, 1 kv head, 2 positions, 4]
+    kcb = a_bf[None, None]
+    qx = np.array([[[1.0, 0.5, -1.0, 2.0]]])
+    r16 = o.cached_gqa_attention(o.f64_to_f16(qx), kcx, kcx, np.array([1]), np.array([0]), 0.25, fmt="f16")
+    rbf = o.cached_gqa_attention(o.f64_to_bf16(qx), kcb, kcb, np.array([1]), np.array([0]), 0.25)
+    assert np.allclose(r16, rbf, rtol=0, atol=1e-12)
+
+
 # ------------------------------------------------------------------ RoPE
 def check_rope_frequencies(o):
     """theta = 16, D = 8 gives frequencies 16^(-2i/8) = 2^-i exactly; theta =
@@ -363,6 +439,7 @@ def check_varlen_chunks_compose(o):
 
 ALL_CHECKS = [
     check_bf16_matches_torch_rounding, check_bf16_single_rounding, check_bf16_roundtrip,
+    check_f16_matches_torch_rounding, check_f16_single_rounding, check_f16_roundtrip, check_f16_storage_paths,
     check_rope_frequencies, check_rope_pairing_and_direction, check_rope_identity_at_zero,
     check_rope_norm_and_composition, check_rope_matches_complex_rotation,
     check_store_slot_mapping_and_untouched, check_single_key_returns_v,

@@ -161,11 +161,32 @@ def mutant_varlen_rope_at_t(m):
     m.prefill_varlen_gqa_cached_rows = varlen
 
 
+def mutant_f16_double_rounding(m):
+    m.f64_to_f16 = lambda x: np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float16).view(np.uint16)
+
+
+def mutant_f16_no_subnormals(m):
+    def f(x):
+        x = np.asarray(x, dtype=np.float64)
+        _, e = np.frexp(np.abs(x))
+        q = e - 11                                  # subnormal spacing forgotten
+        y = np.ldexp(np.rint(np.ldexp(np.abs(x), -q)), q)
+        y = np.where(y > 65504.0, np.inf, y)
+        b = y.astype(np.float16).view(np.uint16)
+        return np.where(np.signbit(x), b | np.uint16(0x8000), b).astype(np.uint16)
+    m.f64_to_f16 = f
+
+
+def mutant_f16_read_as_bf16(m):
+    m.f16_to_f64 = m.bf16_to_f64
+
+
 MUTANTS = [mutant_rope_direction, mutant_rope_interleaved, mutant_rope_frequency,
            mutant_gqa_modulo, mutant_exclusive_prefix, mutant_scale_ignored,
            mutant_double_rounding, mutant_prefill_not_causal, mutant_store_row_index,
            mutant_prefill_offset, mutant_softmax_no_shift_sign, mutant_varlen_mask_ignores_offset,
-           mutant_varlen_rope_at_t]
+           mutant_varlen_rope_at_t, mutant_f16_double_rounding, mutant_f16_no_subnormals,
+           mutant_f16_read_as_bf16]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
