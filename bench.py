@@ -59,6 +59,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp16", action="store_true", help="skip the FP16-storage measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="run just the timed decode steps or just the prefill calls (for profiler captures)")
@@ -326,6 +327,39 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device status flags {flags} after the timed region")
     fused_avg_ms = max_over_ranks(float(np.mean(fused_ms)), world)
 
+    # ---- FP16 storage: the same step and attention call on the same workload
+    # held as IEEE binary16 (the caches converted; unused cells 65504)
+    fp16 = None
+    if not args.no_fp16:
+        q16, k16, v16, kc16, vc16 = (W.to_f16(t) for t in (q, k, v, kc, vc))
+        q_rot16, out16 = torch.empty_like(q16), torch.empty_like(q16)
+        ws16 = [kv.new_workspace(n, dev) for n in (
+            kv.rope_kv_store_workspace_size(), kv.cached_gqa_attention_workspace_size(wl.A, wl.H_q, wl.H_kv, wl.D),
+            kv.decode_step_workspace_size(wl.A, wl.H_q, wl.H_kv, wl.D))]
+        store16 = kv.prepare_rope_kv_store_out_(q16, k16, v16, pos, rows, wl.theta, q_rot16, kc16, vc16, ws16[0], stream)
+        attend16 = kv.prepare_cached_gqa_attention_out_(q_rot16, kc16, vc16, pos, rows, wl.scale, out16, ws16[1], stream)
+        step16 = kv.prepare_decode_step_out_(q16, k16, v16, pos, rows, wl.theta, wl.scale, kc16, vc16, out16, ws16[2],
+                                             stream)
+        for _ in range(3):
+            store16(); attend16(); step16()
+        torch.cuda.synchronize()
+
+        def step16_body(e):
+            e[0].record(stream); step16(); e[1].record(stream)
+
+        def attn16_body(e):
+            store16(); e[0].record(stream); attend16(); e[1].record(stream)
+
+        s16 = max_over_ranks(float(np.mean(timed(step16_body, host_us["step"]))), world)
+        a16 = max_over_ranks(float(np.mean(timed(attn16_body, host_us["store"] + host_us["attention"]))), world) / 1e3
+        if any(kv.kvgqa_read_status(w) for w in ws16):
+            raise RuntimeError("device status flags set in the FP16 decode")
+        fp16 = {"decode": {"step": "decode_step_out_", "step_ms": round(s16, 5),
+                           "tokens_per_s": round(wl.A * world / (s16 / 1e3), 1),
+                           "attention_ms": round(a16 * 1e3, 5), "kv_gbs": round(attn_bytes / a16 / 1e9, 1),
+                           "hbm_frac": round(attn_bytes / a16 / 1e9 / hbm_peak, 4)}}
+        del q16, k16, v16, kc16, vc16, q_rot16, out16, ws16, store16, attend16, step16
+
     # ---- end to end: pinned host inputs -> device -> the step call -> host output
     h_q, h_k, h_v = inp.q.pin_memory(), inp.k.pin_memory(), inp.v.pin_memory()
     h_pos, h_rows = inp.positions.pin_memory(), inp.cache_rows.pin_memory()
@@ -362,6 +396,9 @@ def run_ours(args, rank, world, local):
     prefill = None
     if not args.no_prefill:
         prefill = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
+        if fp16 is not None:
+            fp16["prefill"] = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src,
+                                          f16=True)
     clocks = sampler.stop() if sampler else None
 
     if rank != 0:
@@ -397,17 +434,21 @@ def run_ours(args, rank, world, local):
     }
     if prefill is not None:
         line["prefill"] = prefill
+    if fp16 is not None:
+        line["fp16"] = fp16
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
 
 
-def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src):
+def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src, f16=False):
     pw = W.PREFILL
     pin = W.make_prefill_inputs(pw)
     q, k, v, rows = pin.q.to(dev), pin.k.to(dev), pin.v.to(dev), pin.cache_rows.to(dev)
     kc, vc = pin.build_cache(dev)
-    out = torch.empty(pw.A, pw.T, pw.H_q, pw.D, dtype=torch.bfloat16, device=dev)
+    if f16:  # the same workload held as IEEE binary16
+        q, k, v, kc, vc = (W.to_f16(t) for t in (q, k, v, kc, vc))
+    out = torch.empty(pw.A, pw.T, pw.H_q, pw.D, dtype=q.dtype, device=dev)
     ws = kv.new_workspace(kv.prefill_gqa_cached_rows_workspace_size(pw.A, pw.T, pw.H_q, pw.H_kv, pw.D), dev)
 
     call = kv.prepare_prefill_gqa_cached_rows_out_(q, k, v, rows, pw.theta, pw.scale, kc, vc, out, ws, stream)
@@ -437,7 +478,8 @@ def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_
         raise RuntimeError("device status flags set in prefill")
     return {"workload": pw.name, "ms_per_call": round(avg, 5), "causal_flops": flops,
             "tflops": round(tflops, 1), "frac_of_bf16_peak": round(tflops / bf16_peak, 4),
-            "peak": bf16_peak, "peak_source": f"{peak_src} burst bf16_tflops",
+            "peak": bf16_peak,
+            "peak_source": f"{peak_src} burst bf16_tflops" + (" (FP16 dense rate = BF16 rate, nominal ratio 1)" if f16 else ""),
             "note": "whole call: RoPE + store of all prompts, then causal attention", "gpu_launches": 2 * K}
 
 

@@ -34,8 +34,12 @@
  *    which kvgqa_read_status() returns on request.  The default path never
  *    synchronises the stream.
  *
- * Data types: Q, K, V, the caches and the outputs are BF16; positions and cache
- * rows are int32; softmax and accumulation run in FP32.
+ * Data types: Q, K, V, the caches and the outputs are BF16, or all IEEE
+ * binary16 (FP16 cached rows; one storage type per call, taken from its first
+ * 16-bit tensor, every other 16-bit operand must match or the call returns
+ * KVGQA_EDTYPE); "bf16" below stands for that storage type.  Results are
+ * rounded once, to nearest even, in it.  Positions and cache rows are int32;
+ * softmax and accumulation run in FP32.
  *
  * Layouts (row-major, contiguous, element strides):
  *   decode  q, q_out, out   [A, H_q, D]          k, v  [A, H_kv, D]
@@ -65,7 +69,8 @@ typedef enum kvgqa_dtype {
   KVGQA_BF16 = 1,
   KVGQA_I32 = 2,
   KVGQA_F32 = 3,
-  KVGQA_U8 = 4
+  KVGQA_U8 = 4,
+  KVGQA_F16 = 5    /* IEEE binary16 */
 } kvgqa_dtype;
 
 /* Non-owning tensor descriptor.  `data` is a device pointer on `device` (it may

@@ -27,13 +27,13 @@ import torch
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG_DIR, "libkvgqa.so")
 
-KVGQA_BF16, KVGQA_I32, KVGQA_F32, KVGQA_U8 = 1, 2, 3, 4
+KVGQA_BF16, KVGQA_I32, KVGQA_F32, KVGQA_U8, KVGQA_F16 = 1, 2, 3, 4, 5
 STATUS_NAMES = {0: "OK", 1: "EINVAL", 2: "EDTYPE", 3: "ELAYOUT", 4: "EDEVICE", 5: "EALIAS",
                 6: "EWORKSPACE", 7: "ECUDA", 8: "EUNSUPPORTED", 9: "EFULL"}
 FLAG_POSITION_RANGE, FLAG_ROW_RANGE, FLAG_TIMEOUT = 0x1, 0x2, 0x4
 STATUS_BYTES = 256
 _DTYPES = {torch.bfloat16: KVGQA_BF16, torch.int32: KVGQA_I32, torch.float32: KVGQA_F32,
-           torch.uint8: KVGQA_U8}
+           torch.uint8: KVGQA_U8, torch.float16: KVGQA_F16}
 
 
 class KvgqaTensor(ctypes.Structure):

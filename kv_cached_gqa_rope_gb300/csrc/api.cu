@@ -45,6 +45,7 @@ void check_cuda(cudaError_t e, const char* what) {
 int64_t elem_size(int32_t dtype) {
   switch (dtype) {
     case KVGQA_BF16: return 2;
+    case KVGQA_F16: return 2;
     case KVGQA_I32: return 4;
     case KVGQA_F32: return 4;
     case KVGQA_U8: return 1;
@@ -55,6 +56,7 @@ int64_t elem_size(int32_t dtype) {
 const char* dtype_name(int32_t dtype) {
   switch (dtype) {
     case KVGQA_BF16: return "bf16";
+    case KVGQA_F16: return "f16";
     case KVGQA_I32: return "int32";
     case KVGQA_F32: return "float32";
     case KVGQA_U8: return "uint8";
@@ -103,6 +105,15 @@ View check_tensor(const char* name, const kvgqa_tensor* t, int ndim, int32_t dty
   v.lo = reinterpret_cast<uintptr_t>(t->data);
   v.hi = v.lo + static_cast<uintptr_t>(bytes);
   return v;
+}
+
+// Storage type of a call (BF16 or IEEE binary16), taken from its first 16-bit
+// tensor; every other 16-bit tensor of the call must have the same type.
+int32_t storage_type(const kvgqa_tensor* t, const char* name) {
+  if (!t) fail(KVGQA_EINVAL, "%s: null descriptor", name);
+  if (t->dtype != KVGQA_BF16 && t->dtype != KVGQA_F16)
+    fail(KVGQA_EDTYPE, "%s: expected bf16 or f16, got %s", name, dtype_name(t->dtype));
+  return t->dtype;
 }
 
 // The device checks: the declared device is the current one, and CUDA knows
@@ -221,14 +232,15 @@ kvgqa_status rope_kv_store_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
     check_head_dim(D);
     check_heads(H_q, H_kv);
     check_theta(theta);
-    View vq = check_tensor("q", q, 3, KVGQA_BF16, 16);
-    View vk = check_tensor("k", k, 3, KVGQA_BF16, 16);
-    View vv = check_tensor("v", v, 3, KVGQA_BF16, 16);
+    const int32_t elem = storage_type(q, "q");
+    View vq = check_tensor("q", q, 3, elem, 16);
+    View vk = check_tensor("k", k, 3, elem, 16);
+    View vv = check_tensor("v", v, 3, elem, 16);
     View vp = check_tensor("positions", positions, 1, KVGQA_I32, 4);
     View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
-    View vqo = check_tensor("q_out", q_out, 3, KVGQA_BF16, 16);
-    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
-    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+    View vqo = check_tensor("q_out", q_out, 3, elem, 16);
+    View vkc = check_tensor("k_cache", k_cache, 4, elem, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, elem, 16);
     View vws = check_workspace(workspace, KVGQA_STATUS_BYTES);
     require_shape(vk, {A, H_kv, D});
     require_shape(vv, {A, H_kv, D});
@@ -254,6 +266,7 @@ kvgqa_status rope_kv_store_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
     p.status = static_cast<int32_t*>(workspace->data);
     p.A = (int)A; p.T = 1; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.D = (int)D;
     p.S = (int)S; p.max_seq = (int)max_seq;
+    p.f16 = elem == KVGQA_F16;
     fill_inv_freq(p.inv_freq, (int)D, theta);
     check_cuda(kvgqa::launch_rope_kv_store(p, 0, static_cast<cudaStream_t>(stream)),
                "rope_kv_store launch");
@@ -293,12 +306,13 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
     if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
     if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
-    View vq = check_tensor("q_rot", q_rot, 3, KVGQA_BF16, 16);
-    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
-    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+    const int32_t elem = storage_type(q_rot, "q_rot");
+    View vq = check_tensor("q_rot", q_rot, 3, elem, 16);
+    View vkc = check_tensor("k_cache", k_cache, 4, elem, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, elem, 16);
     View vp = check_tensor("positions", positions, 1, KVGQA_I32, 4);
     View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
-    View vo = check_tensor("out", out, 3, KVGQA_BF16, 16);
+    View vo = check_tensor("out", out, 3, elem, 16);
     require_shape(vvc, {S, H_kv, max_seq, D});
     require_shape(vp, {A});
     require_shape(vr, {A});
@@ -325,6 +339,7 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
     p.partials = reinterpret_cast<float*>(ws + KVGQA_STATUS_BYTES + lay.counter_bytes);
     p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
     p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
+    p.f16 = elem == KVGQA_F16;
     p.scale_log2 = scale * 1.4426950408889634f;
     check_cuda(kvgqa::launch_cached_gqa_attention(p, static_cast<cudaStream_t>(stream)),
                "cached_gqa_attention launch");
@@ -375,14 +390,15 @@ void decode_step_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_
     if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
     if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
-    View vq = check_tensor("q", q, 3, KVGQA_BF16, 16);
-    View vk = check_tensor("k", k, 3, KVGQA_BF16, 16);
-    View vv = check_tensor("v", v, 3, KVGQA_BF16, 16);
+    const int32_t elem = storage_type(q, "q");
+    View vq = check_tensor("q", q, 3, elem, 16);
+    View vk = check_tensor("k", k, 3, elem, 16);
+    View vv = check_tensor("v", v, 3, elem, 16);
     View vp = check_tensor("positions", positions, 1, KVGQA_I32, 4);
     View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
-    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
-    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
-    View vo = check_tensor("out", out, 3, KVGQA_BF16, 16);
+    View vkc = check_tensor("k_cache", k_cache, 4, elem, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, elem, 16);
+    View vo = check_tensor("out", out, 3, elem, 16);
     require_shape(vk, {A, H_kv, D});
     require_shape(vv, {A, H_kv, D});
     require_shape(vp, {A});
@@ -415,6 +431,7 @@ void decode_step_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_
       p.partials = reinterpret_cast<float*>(ws + KVGQA_STATUS_BYTES + lay.counter_bytes);
       p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
       p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
+      p.f16 = elem == KVGQA_F16;
       p.scale_log2 = scale * 1.4426950408889634f;
       p.fused = 1;
       p.k_new = static_cast<const uint16_t*>(k->data);
@@ -438,6 +455,7 @@ void decode_step_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_
     rp.status = reinterpret_cast<int32_t*>(ws);
     rp.A = (int)A; rp.T = 1; rp.H_q = (int)H_q; rp.H_kv = (int)H_kv; rp.D = (int)D;
     rp.S = (int)S; rp.max_seq = (int)max_seq;
+    rp.f16 = elem == KVGQA_F16;
     fill_inv_freq(rp.inv_freq, (int)D, theta);
     check_cuda(kvgqa::launch_rope_kv_store(rp, 0, st), "decode_step store launch");
     // 2. the attention, started while the store kernel runs: it streams the
@@ -454,6 +472,7 @@ void decode_step_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_
     p.partials = reinterpret_cast<float*>(ws + KVGQA_STATUS_BYTES + lay.counter_bytes);
     p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
     p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
+    p.f16 = elem == KVGQA_F16;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.early = 1;
     check_cuda(kvgqa::launch_cached_gqa_attention(p, st), "decode_step attention launch");
@@ -497,12 +516,13 @@ kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
     if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
     if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
-    View vq = check_tensor("q_rot", q_rot, 3, KVGQA_BF16, 16);
-    View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
-    View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
+    const int32_t elem = storage_type(q_rot, "q_rot");
+    View vq = check_tensor("q_rot", q_rot, 3, elem, 16);
+    View vkc = check_tensor("k_cache", k_cache, 4, elem, 16);
+    View vvc = check_tensor("v_cache", v_cache, 4, elem, 16);
     View vp = check_tensor("positions", positions, 1, KVGQA_I32, 4);
     View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
-    View vo = check_tensor("out", out, 3, KVGQA_BF16, 16);
+    View vo = check_tensor("out", out, 3, elem, 16);
     require_shape(vvc, {S, H_kv, max_seq, D});
     require_shape(vp, {A});
     require_shape(vr, {A});
@@ -533,6 +553,7 @@ kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
     p.partials = reinterpret_cast<float*>(sc + KVGQA_STATUS_BYTES + lay.counter_bytes);
     p.A = (int)A; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.G = G; p.D = (int)D;
     p.S = (int)S; p.max_seq = (int)max_seq; p.num_ctas = lay.num_ctas;
+    p.f16 = elem == KVGQA_F16;
     p.scale_log2 = scale * 1.4426950408889634f;
     check_cuda(kvgqa::launch_cached_gqa_attention(p, static_cast<cudaStream_t>(stream)),
                "cached_gqa_attention launch");
@@ -571,13 +592,14 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
   if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
   if (T > max_seq) fail(KVGQA_EINVAL, "T=%lld exceeds max_seq=%lld", (long long)T, (long long)max_seq);
   if (A * T > 0x7fffffffll) fail(KVGQA_EUNSUPPORTED, "A*T must stay below 2^31");
-  View vq = check_tensor("q", q, 4, KVGQA_BF16, 16);
-  View vk = check_tensor("k", k, 4, KVGQA_BF16, 16);
-  View vv = check_tensor("v", v, 4, KVGQA_BF16, 16);
+  const int32_t elem = storage_type(q, "q");
+  View vq = check_tensor("q", q, 4, elem, 16);
+  View vk = check_tensor("k", k, 4, elem, 16);
+  View vv = check_tensor("v", v, 4, elem, 16);
   View vr = check_tensor("cache_rows", cache_rows, 1, KVGQA_I32, 4);
-  View vkc = check_tensor("k_cache", k_cache, 4, KVGQA_BF16, 16);
-  View vvc = check_tensor("v_cache", v_cache, 4, KVGQA_BF16, 16);
-  View vo = check_tensor("out", out, 4, KVGQA_BF16, 16);
+  View vkc = check_tensor("k_cache", k_cache, 4, elem, 16);
+  View vvc = check_tensor("v_cache", v_cache, 4, elem, 16);
+  View vo = check_tensor("out", out, 4, elem, 16);
   require_shape(vk, {A, T, H_kv, D});
   require_shape(vv, {A, T, H_kv, D});
   require_shape(vr, {A});
@@ -620,6 +642,7 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
   rp.status = reinterpret_cast<int32_t*>(ws);
   rp.A = (int)A; rp.T = (int)T; rp.H_q = (int)H_q; rp.H_kv = (int)H_kv; rp.D = (int)D;
   rp.S = (int)S; rp.max_seq = (int)max_seq;
+  rp.f16 = elem == KVGQA_F16;
   fill_inv_freq(rp.inv_freq, (int)D, theta);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   check_cuda(kvgqa::launch_rope_kv_store(rp, varlen ? 2 : 1, st), "prefill rope_kv_store launch");
@@ -634,6 +657,7 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
   pp.status = rp.status;
   pp.A = (int)A; pp.T = (int)T; pp.H_q = (int)H_q; pp.H_kv = (int)H_kv; pp.G = (int)(H_q / H_kv);
   pp.D = (int)D; pp.S = (int)S; pp.max_seq = (int)max_seq;
+  pp.f16 = elem == KVGQA_F16;
   pp.scale_log2 = scale * 1.4426950408889634f;
   check_cuda(kvgqa::launch_prefill_attention(pp, st), "prefill attention launch");
 }

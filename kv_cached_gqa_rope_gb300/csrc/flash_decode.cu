@@ -17,12 +17,12 @@
 // then padding that stands for the cost of its tail tile and its end.  CTA b
 // of the persistent grid (one CTA per SM) takes the virtual range
 // [b*W, (b+1)*W), W = ceil(V_tot / grid), and processes the real keys in it.
-// A segment whose real keys lie inside one CTA is finished there (BF16 out
+// A segment whose real keys lie inside one CTA is finished there (output in the storage type
 // written); a segment cut by a CTA boundary leaves FP32 partials (m, l, o):
 // the CTA where it starts writes slot 1, each later CTA slot 0.  The combine
 // (K3) runs in whichever of those CTAs finishes last: each counts its partial
 // in a per-segment counter, and the one that completes the count merges the
-// segment's partials, writes the BF16 output and resets the counter to zero.
+// segment's partials, writes the output (storage type) and resets the counter to zero.
 //
 // Inside a CTA, per tile of up to 128 keys of one segment:
 //   warp 4     TMA producer: K and V tiles (128B swizzle, 32-row boxes, so a
@@ -35,12 +35,16 @@
 //              TMEM accumulator;
 //   warps 0-3  one thread per key: S^T row from TMEM, FP32 online softmax per
 //              head (warp shuffles + a 4-warp exchange for the tile maximum
-//              and sum), P^T as BF16 into 128B-swizzled shared memory; the O^T
+//              and sum), P^T in the storage type into 128B-swizzled shared memory; the O^T
 //              rescale (TMEM load/scale/store, one lane per d) happens only when
 //              a head's maximum grew by more than 2^8; at a segment end each
 //              lane d writes O^T[d][h] / l[h] (or the partial).
 // The tensor cores do the two contractions, so the CUDA cores only run the
 // softmax: the kernel is bound by the HBM stream of K and V.
+#ifndef KVGQA_DECODE_F16
+#define KVGQA_DECODE_F16 0  // 1: the IEEE binary16 build of these kernels
+#endif
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,6 +53,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "elem.cuh"
 #include "kvgqa_internal.h"
 #include "rope_math.cuh"
 #include "tcgen05.cuh"
@@ -56,11 +61,17 @@
 namespace kvgqa {
 namespace {
 
+// Storage type of this translation unit's kernels (flash_decode_f16.cu
+// compiles the same kernels for IEEE binary16).
+constexpr bool kF16 = KVGQA_DECODE_F16 != 0;
+using E = Elem<kF16>;
+constexpr CUtensorMapDataType kTmaElem = kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
 constexpr int BN = 128;                 // keys per tile (= TMEM lanes = softmax threads)
 constexpr int NQ = 16;                  // MMA N: query heads of a group, padded
 constexpr int BOX_ROWS = 32;            // rows per TMA box of a K or V tile
-constexpr int SUB = BN * 128;           // one [128 rows x 64 bf16] swizzled sub-tile
-constexpr int QSUB = NQ * 128;          // one [16 rows x 64 bf16] swizzled sub-tile
+constexpr int SUB = BN * 128;           // one [128 rows x 64 16-bit values] swizzled sub-tile
+constexpr int QSUB = NQ * 128;          // one [16 rows x 64 16-bit values] swizzled sub-tile
 // 4 softmax warps + producer + MMA, plus the query/cell prep warp of the fused step
 __host__ __device__ constexpr int threads_of(bool fused) { return fused ? 224 : 192; }
 constexpr int TMEM_COLS = 64;           // S^T x2 (16 cols each) + O^T (16 cols)
@@ -228,13 +239,8 @@ struct Cursor {
   }
 };
 
-__device__ __forceinline__ uint16_t bf16_bits(float v) {
-  const __nv_bfloat16 b = __float2bfloat16_rn(v);
-  return *reinterpret_cast<const uint16_t*>(&b);
-}
-
 // K3, the combine: merge the partials of CTAs b0..b1 for segment (a, g) and
-// write the BF16 output of its G query heads.  One thread per d (d < D) of
+// write the output of its G query heads.  One thread per d (d < D) of
 // the 128 softmax threads.  Partials of other CTAs are read past L1, in
 // batches of kMaxParts partials whose loads (all heads) are issued before any
 // is used: one L2 round trip per batch instead of one per partial and head.
@@ -276,7 +282,7 @@ __device__ void combine_segment(const DecodeParams& p, int a, int g, int b0, int
   }
 #pragma unroll
   for (int h = 0; h < GP; ++h)
-    if (h < p.G) p.out[(static_cast<size_t>(a) * p.H_q + g * p.G + h) * D + d] = bf16_bits(acc[h] / lsum[h]);
+    if (h < p.G) p.out[(static_cast<size_t>(a) * p.H_q + g * p.G + h) * D + d] = E::from_f32(acc[h] / lsum[h]);
 }
 
 // Atomic add with release and acquire semantics at GPU scope.
@@ -485,8 +491,8 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   } else if (warp == 5) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16_f32(BN, NQ, 0, 0);
-      constexpr uint32_t IDESC_O = idesc_bf16_f32(BN, NQ, 0, 1);
+      constexpr uint32_t IDESC_S = idesc_f16kind_f32(E::kMmaFormat, BN, NQ, 0, 0);
+      constexpr uint32_t IDESC_O = idesc_f16kind_f32(E::kMmaFormat, BN, NQ, 0, 1);
       constexpr uint32_t V_LBO = D == 128 ? SUB : 0;  // D = 64: the second M half repeats the first
       const uint32_t p_addr = sbase + C::P_OFF;
       bool issued = false;
@@ -616,9 +622,9 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             const int j = lane + 32 * u;
             uint16_t* c1 = cell(qb + (j >> 6) * QSUB, h, j);
             uint16_t* c2 = cell(qb + ((j + HALF) >> 6) * QSUB, h, j + HALF);
-            const float x1 = bf16_bits_to_f32(*c1), x2 = bf16_bits_to_f32(*c2);
-            *c1 = bf16_rn_bits(rot_first(x1, x2, cs[u]));
-            *c2 = bf16_rn_bits(rot_second(x1, x2, cs[u]));
+            const float x1 = E::to_f32(*c1), x2 = E::to_f32(*c2);
+            *c1 = E::from_f32(rot_first(x1, x2, cs[u]));
+            *c2 = E::from_f32(rot_second(x1, x2, cs[u]));
           }
         }
         fence_proxy_async_smem();  // the query tile is read by the tensor cores
@@ -628,9 +634,9 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
           uint16_t kr[2 * NU];
 #pragma unroll
           for (int u = 0; u < NU; ++u) {
-            const float x1 = bf16_bits_to_f32(kn[2 * u]), x2 = bf16_bits_to_f32(kn[2 * u + 1]);
-            kr[2 * u] = bf16_rn_bits(rot_first(x1, x2, cs[u]));
-            kr[2 * u + 1] = bf16_rn_bits(rot_second(x1, x2, cs[u]));
+            const float x1 = E::to_f32(kn[2 * u]), x2 = E::to_f32(kn[2 * u + 1]);
+            kr[2 * u] = E::from_f32(rot_first(x1, x2, cs[u]));
+            kr[2 * u + 1] = E::from_f32(rot_second(x1, x2, cs[u]));
           }
           const size_t cell_off = ((static_cast<size_t>(p.cache_rows[cur.a]) * p.H_kv + cur.g) * p.max_seq + pos) * D;
 #pragma unroll
@@ -724,7 +730,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         tmem_st16(tmem + lane_base + 2 * NQ, o);
         tmem_wait_st();
       }
-      // P^T[h][r] as BF16 (K-major B operand: 16 rows of 128 keys, two 64-key
+      // P^T[h][r] in the storage type (K-major B operand: 16 rows of 128 keys, two 64-key
       // swizzled sub-tiles); padded heads and invalid keys are zero.
       const int sub = r >> 6, chunk = (r & 63) >> 3, e = r & 7;
       unsigned char* pt = pt0 + (it & 1) * 2 * QSUB;
@@ -733,8 +739,8 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         uint16_t b = 0;
         if (h < GP) {
           const float pv = x[h] == -INFINITY ? 0.f : exp2f(x[h] - m_ref[h]);
-          b = bf16_bits(pv);
-          float ps = __uint_as_float(static_cast<uint32_t>(b) << 16);
+          b = E::from_f32(pv);
+          float ps = E::to_f32(b);
 #pragma unroll
           for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(FULL, ps, off);
           if (lane == 0) red_sum[warp * NQ + h] = ps;
@@ -772,7 +778,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             uint16_t* dst = p.out + (static_cast<size_t>(cur.a) * p.H_q + cur.g * p.G) * D + d;
 #pragma unroll
             for (int h = 0; h < GP; ++h)
-              if (h < p.G) dst[h * D] = bf16_bits(__uint_as_float(o[h]) / l[h]);
+              if (h < p.G) dst[h * D] = E::from_f32(__uint_as_float(o[h]) / l[h]);
           } else {
             float* slotp = p.partials + static_cast<size_t>(blockIdx.x * 2 + cur.slot()) * slot_floats(GP, D);
 #pragma unroll
@@ -823,7 +829,7 @@ cudaError_t make_decode_maps(const DecodeParams& p, DecodeMaps* m) {
   cuuint32_t box[3] = {64, BOX_ROWS, 1};
   cuuint32_t es[3] = {1, 1, 1};
   for (int t = 0; t < 2; ++t) {
-    if (enc(t == 0 ? &m->kc : &m->vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    if (enc(t == 0 ? &m->kc : &m->vc, kTmaElem, 3,
             const_cast<uint16_t*>(t == 0 ? p.k_cache : p.v_cache), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -834,7 +840,7 @@ cudaError_t make_decode_maps(const DecodeParams& p, DecodeMaps* m) {
   cuuint64_t qdims[3] = {D, static_cast<cuuint64_t>(p.A) * p.H_q, 1};
   cuuint64_t qstrides[2] = {D * 2, D * 2 * static_cast<cuuint64_t>(p.A) * p.H_q};
   cuuint32_t qbox[3] = {64, NQ, 1};
-  if (enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.q), qdims, qstrides, qbox, es,
+  if (enc(&m->q, kTmaElem, 3, const_cast<uint16_t*>(p.q), qdims, qstrides, qbox, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -909,6 +915,21 @@ cudaError_t dispatch(int D, int GP, F&& f) {
 
 }  // namespace
 
+#if KVGQA_DECODE_F16
+cudaError_t launch_cached_gqa_attention_f16(const DecodeParams& p, cudaStream_t stream) {
+  DecodeMaps m;
+  cudaError_t e = make_decode_maps(p, &m);
+  if (e != cudaSuccess) return e;
+  const int GP = decode_group_pad(p.G);
+  int device = 0, n = 0;
+  e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  return dispatch(p.D, GP, [&](auto k) {
+    const cudaError_t pe = decltype(k)::prepare(device, &n);
+    return pe != cudaSuccess ? pe : decltype(k)::launch(p, m, stream);
+  });
+}
+#else
 int decode_group_pad(int G) {
   int gp = 1;
   while (gp < G) gp <<= 1;
@@ -944,11 +965,13 @@ cudaError_t static_scratch_address(int device, void** ptr) {
 
 cudaError_t launch_cached_gqa_attention(const DecodeParams& p, cudaStream_t stream) {
   if (p.A == 0) return cudaSuccess;
+  if (p.f16) return launch_cached_gqa_attention_f16(p, stream);
   DecodeMaps m;
   const cudaError_t e = make_decode_maps(p, &m);
   if (e != cudaSuccess) return e;
   const int GP = decode_group_pad(p.G);
   return dispatch(p.D, GP, [&](auto k) { return decltype(k)::launch(p, m, stream); });
 }
+#endif  // KVGQA_DECODE_F16
 
 }  // namespace kvgqa

@@ -29,6 +29,7 @@ struct RopeStoreParams {
   uint16_t* v_cache;
   int32_t* status;
   int A, T, H_q, H_kv, D, S, max_seq;
+  int f16;                   // storage: 0 BF16, 1 IEEE binary16
   double inv_freq[kMaxHeadDim / 2];  // theta^(-2i/D), computed on the host in double
 };
 
@@ -51,6 +52,7 @@ struct DecodeParams {
   int32_t* status;
   int A, H_q, H_kv, G, D, S, max_seq;
   int num_ctas;               // grid size of the split-K kernel
+  int f16;                    // storage: 0 BF16, 1 IEEE binary16
   float scale_log2;           // scale * log2(e)
   // Early start (whole-step call only, where the previous kernel in the
   // stream is that call's own store kernel, which writes only the rotated
@@ -78,6 +80,8 @@ struct DecodeLayout {
 };
 cudaError_t decode_layout(int device, int D, int GP, int64_t A, int64_t H_kv, DecodeLayout* out);
 cudaError_t launch_cached_gqa_attention(const DecodeParams& p, cudaStream_t stream);
+// The same for IEEE binary16 storage (called by the above when p.f16 is set).
+cudaError_t launch_cached_gqa_attention_f16(const DecodeParams& p, cudaStream_t stream);
 
 // Size of the library's own device scratch array (status block + partials)
 // used by the entry point for callers that cannot allocate, and its device
@@ -97,6 +101,7 @@ struct PrefillParams {
   int32_t* status;
   int A, T, H_q, H_kv, G, D, S, max_seq;
   float scale_log2;
+  int f16;                    // storage: 0 BF16, 1 IEEE binary16
 };
 
 cudaError_t launch_prefill_attention(const PrefillParams& p, cudaStream_t stream);

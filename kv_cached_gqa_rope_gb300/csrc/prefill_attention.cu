@@ -19,10 +19,10 @@
 //               O_x += P_x V with P_x read from TMEM (x = A, B);
 //   warps 0-3   softmax of head A, warps 4-7 softmax of head B, one thread
 //               per query row: S row from TMEM, scale and diagonal causal mask,
-//               FP32 online softmax, P as BF16 pairs written back over the S
+//               FP32 online softmax, P as BF16 (FP16 storage: FP16) pairs written back over the S
 //               columns, O rescaled in TMEM only when the row maximum grew by
 //               more than 2^8 (otherwise the old base is kept; O / l stays
-//               exact); at the item end O / l is rounded to BF16 and stored.
+//               exact); at the item end O / l is rounded to the storage type and stored.
 // The two softmax groups alternate with the tensor core: while one works on
 // its head's scores, the MMAs of the other head run.  MMAs issued by one
 // thread complete in order and a commit covers every earlier MMA, so S_x of
@@ -39,6 +39,7 @@
 #include <mutex>
 
 #include "kvgqa_internal.h"
+#include "elem.cuh"
 #include "tcgen05.cuh"
 
 namespace kvgqa {
@@ -46,7 +47,7 @@ namespace {
 
 constexpr int BM = 128;        // query rows per tile
 constexpr int BN = 128;        // keys per tile
-constexpr int SUB = 16384;     // one [128 rows x 64 bf16] swizzled sub-tile
+constexpr int SUB = 16384;     // one [128 rows x 64 16-bit values] swizzled sub-tile
 constexpr int NWARPS = 12;     // 2 x 4 softmax + Q/K producer + V producer + MMA + spare
 constexpr int THREADS = NWARPS * 32;
 constexpr int W_QK = 8, W_V = 9, W_MMA = 10;
@@ -85,10 +86,6 @@ struct PrefillMaps {
   CUtensorMap v;
 };
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 template <int N>
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
@@ -115,7 +112,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // 2^x on the special-function unit (flushes results below 2^-126 to zero,
-// which no BF16 probability needs).
+// which no 16-bit probability needs).
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -201,11 +198,12 @@ struct TileWalk {
   }
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
   using C = PCfg<D>;
+  using E = Elem<F16>;  // storage type of Q, K, V, P and the output
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
@@ -335,8 +333,8 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     // The whole warp runs the issue loop (uniform control flow); one elected
     // lane issues each group of MMAs and its commits.
     {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);
+      constexpr uint32_t IDESC_QK = idesc_f16kind_f32(E::kMmaFormat, BM, BN, 0);
+      constexpr uint32_t IDESC_PV = idesc_f16kind_f32(E::kMmaFormat, BM, D, 1);
       const bool pairs = walk.pairs();
       const int nh = pairs ? 2 : 1;
       bool issued = false;
@@ -489,7 +487,8 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
           tmem_st32(o_col + q * 32, u);
         }
       }
-      // P as BF16 pairs over the first 64 columns of S_x (the A operand of P.V).
+      // P as pairs of the storage type over the first 64 columns of S_x (the A
+      // operand of P.V, which must have V's type).
       float2 ls = make_float2(0.f, 0.f);
       const float2 c2 = make_float2(ce, ce), nm2 = make_float2(-m_ref, -m_ref);
 #pragma unroll
@@ -501,7 +500,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
           const float2 xx = ffma2(make_float2(sv[i0], sv[i0 + 1]), c2, nm2);
           const float2 pr = make_float2(ex2(xx.x), ex2(xx.y));
           ls = fadd2(ls, pr);
-          w[e] = pack2(pr.x, pr.y);
+          w[e] = E::pack2(pr.x, pr.y);
         }
         tmem_st32(s_col + half * 32, w);
       }
@@ -534,10 +533,10 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8) {
               uint4 o;
-              o.x = pack2(__uint_as_float(u[q8 * 8 + 0]) * inv, __uint_as_float(u[q8 * 8 + 1]) * inv);
-              o.y = pack2(__uint_as_float(u[q8 * 8 + 2]) * inv, __uint_as_float(u[q8 * 8 + 3]) * inv);
-              o.z = pack2(__uint_as_float(u[q8 * 8 + 4]) * inv, __uint_as_float(u[q8 * 8 + 5]) * inv);
-              o.w = pack2(__uint_as_float(u[q8 * 8 + 6]) * inv, __uint_as_float(u[q8 * 8 + 7]) * inv);
+              o.x = E::pack2(__uint_as_float(u[q8 * 8 + 0]) * inv, __uint_as_float(u[q8 * 8 + 1]) * inv);
+              o.y = E::pack2(__uint_as_float(u[q8 * 8 + 2]) * inv, __uint_as_float(u[q8 * 8 + 3]) * inv);
+              o.z = E::pack2(__uint_as_float(u[q8 * 8 + 4]) * inv, __uint_as_float(u[q8 * 8 + 5]) * inv);
+              o.w = E::pack2(__uint_as_float(u[q8 * 8 + 6]) * inv, __uint_as_float(u[q8 * 8 + 7]) * inv);
               *reinterpret_cast<uint4*>(dst + q * 32 + q8 * 8) = o;
             }
           }
@@ -557,13 +556,14 @@ cudaError_t make_maps(const PrefillParams& p, PrefillMaps* m) {
   auto enc = tma_encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t D = p.D;
+  const CUtensorMapDataType elem_type = p.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   {
     cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(p.H_q), static_cast<cuuint64_t>(p.T),
                           static_cast<cuuint64_t>(p.A)};
     cuuint64_t strides[3] = {D * 2, D * 2 * p.H_q, D * 2 * p.H_q * p.T};
     cuuint32_t box[4] = {64, 1, BM, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    if (enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(p.q_rot), dims, strides, box, es,
+    if (enc(&m->q, elem_type, 4, const_cast<uint16_t*>(p.q_rot), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -576,18 +576,18 @@ cudaError_t make_maps(const PrefillParams& p, PrefillMaps* m) {
   cuuint64_t strides[2] = {D * 2, D * 2 * static_cast<cuuint64_t>(p.max_seq)};
   cuuint32_t box[3] = {64, BN, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  if (enc(&m->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.k_cache), dims, strides, box, es,
+  if (enc(&m->k, elem_type, 3, const_cast<uint16_t*>(p.k_cache), dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  if (enc(&m->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.v_cache), dims, strides, box, es,
+  if (enc(&m->v, elem_type, 3, const_cast<uint16_t*>(p.v_cache), dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   return cudaSuccess;
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t stream) {
   static std::once_flag flags[64];
   static cudaError_t errs[64];
@@ -596,12 +596,12 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t 
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::call_once(flags[dev], [&] {
-    errs[dev] = cudaFuncSetAttribute(prefill_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    errs[dev] = cudaFuncSetAttribute(prefill_attention_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      PCfg<D>::SMEM);
     // The in-kernel register split needs the launch to hand out kLaunchRegs
     // per thread; with fewer, setmaxnreg.inc could never be satisfied.
     cudaFuncAttributes attr;
-    if (errs[dev] == cudaSuccess) errs[dev] = cudaFuncGetAttributes(&attr, prefill_attention_kernel<D>);
+    if (errs[dev] == cudaSuccess) errs[dev] = cudaFuncGetAttributes(&attr, prefill_attention_kernel<D, F16>);
     if (errs[dev] == cudaSuccess && attr.numRegs < kLaunchRegs) errs[dev] = cudaErrorInvalidConfiguration;
   });
   if (errs[dev] != cudaSuccess) return errs[dev];
@@ -614,7 +614,7 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t 
   const int per_tok = p.G % 2 == 0 ? p.H_q / 2 : p.H_q;  // head pairs when the group size is even
   const long long items = static_cast<long long>((p.T + BM - 1) / BM) * p.A * per_tok;
   const unsigned grid = static_cast<unsigned>(items < sms[dev] ? items : sms[dev]);  // one CTA per SM
-  prefill_attention_kernel<D><<<grid, THREADS, PCfg<D>::SMEM, stream>>>(p, m.q, m.k, m.v);
+  prefill_attention_kernel<D, F16><<<grid, THREADS, PCfg<D>::SMEM, stream>>>(p, m.q, m.k, m.v);
   return cudaGetLastError();
 }
 
@@ -639,8 +639,8 @@ cudaError_t launch_prefill_attention(const PrefillParams& p, cudaStream_t stream
   PrefillMaps m;
   cudaError_t e = make_maps(p, &m);
   if (e != cudaSuccess) return e;
-  if (p.D == 128) return launch_d<128>(p, m, stream);
-  if (p.D == 64) return launch_d<64>(p, m, stream);
+  if (p.D == 128) return p.f16 ? launch_d<128, true>(p, m, stream) : launch_d<128, false>(p, m, stream);
+  if (p.D == 64) return p.f16 ? launch_d<64, true>(p, m, stream) : launch_d<64, false>(p, m, stream);
   return cudaErrorInvalidValue;
 }
 

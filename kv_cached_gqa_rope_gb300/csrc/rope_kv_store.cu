@@ -22,9 +22,11 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "kvgqa_internal.h"
 #include "ptx.cuh"
+#include "elem.cuh"
 #include "rope_math.cuh"
 
 namespace kvgqa {
@@ -35,31 +37,29 @@ namespace {
 // entries puts those lanes on different shared-memory banks.
 __device__ __forceinline__ int cs_slot(int i) { return i + (i >> 3); }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// Rotate the 8 pairs (a[i], b[i]) held in two 16-byte chunks.
+// Rotate the 8 pairs (a[i], b[i]) held in two 16-byte chunks of the storage
+// type; each result is rounded once (nearest even) back to it.
+template <bool F16>
 __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const CosSin* cs,
                                         uint4& ya, uint4& yb) {
+  using E = Elem<F16>;
   // cs points at the padded slot of pair 8c; the eight pairs follow contiguously
   const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
   const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
   uint32_t oa[4], ob[4];
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    const float2 x1 = bf16x2_to_f2(aw[w]);
-    const float2 x2 = bf16x2_to_f2(bw[w]);
+    const float2 x1 = E::pair_to_f2(aw[w]);
+    const float2 x2 = E::pair_to_f2(bw[w]);
     const CosSin c0 = cs[2 * w], c1 = cs[2 * w + 1];
-    oa[w] = pack_bf16x2(rot_first(x1.x, x2.x, c0), rot_first(x1.y, x2.y, c1));
-    ob[w] = pack_bf16x2(rot_second(x1.x, x2.x, c0), rot_second(x1.y, x2.y, c1));
+    oa[w] = E::pack2(rot_first(x1.x, x2.x, c0), rot_first(x1.y, x2.y, c1));
+    ob[w] = E::pack2(rot_second(x1.x, x2.x, c0), rot_second(x1.y, x2.y, c1));
   }
   ya = make_uint4(oa[0], oa[1], oa[2], oa[3]);
   yb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_constant__ RopeStoreParams p) {
   constexpr int HALF = D / 2;
   constexpr int RU = D / 16;  // rotation units per head: 8 pairs each
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
     for (int u = 0; u < kBatch; ++u) {
       if (!dst[u]) continue;
       uint4 ya, yb;
-      rotate8(xa[u], xb[u], cs + cs_slot(cc[u] * 8), ya, yb);
+      rotate8<F16>(xa[u], xb[u], cs + cs_slot(cc[u] * 8), ya, yb);
       *reinterpret_cast<uint4*>(dst[u] + cc[u] * 8) = ya;
       *reinterpret_cast<uint4*>(dst[u] + HALF + cc[u] * 8) = yb;
     }
@@ -158,7 +158,7 @@ constexpr int kTokenThreads = 128;
 // t < lengths[a], varlen = 1).  CTA part s of the token rotates the pairs of
 // frequencies [s*F, s*F + F) of every Q and K head, F = D/2 / kTokenSplit, and
 // copies part s of its V bytes.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(const __grid_constant__ RopeStoreParams p,
                                                                           int varlen) {
   constexpr int HALF = D / 2;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(cons
       uint16_t* dst = h < p.H_q ? p.q_out + (tok * p.H_q + h) * D
                                 : p.k_cache + ((static_cast<size_t>(row) * p.H_kv + (h - p.H_q)) * p.max_seq + pos) * D;
       uint4 ya, yb;
-      rotate8(va, vb, cs + cs_slot(cl * 8), ya, yb);
+      rotate8<F16>(va, vb, cs + cs_slot(cl * 8), ya, yb);
       *reinterpret_cast<uint4*>(dst + c * 8) = ya;
       *reinterpret_cast<uint4*>(dst + HALF + c * 8) = yb;
     } else {
@@ -291,8 +291,10 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::call_once(carveout_once[dev], [dev] {
-    const void* fns[2] = {reinterpret_cast<const void*>(rope_kv_store_token_kernel<128>),
-                          reinterpret_cast<const void*>(rope_kv_store_token_kernel<64>)};
+    const void* fns[4] = {reinterpret_cast<const void*>(rope_kv_store_token_kernel<128, false>),
+                          reinterpret_cast<const void*>(rope_kv_store_token_kernel<64, false>),
+                          reinterpret_cast<const void*>(rope_kv_store_token_kernel<128, true>),
+                          reinterpret_cast<const void*>(rope_kv_store_token_kernel<64, true>)};
     carveout_err[dev] = cudaSuccess;
     for (const void* f : fns)
       if (carveout_err[dev] == cudaSuccess)
@@ -301,12 +303,16 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
   });
   if (carveout_err[dev] != cudaSuccess) return carveout_err[dev];
   const int varlen = mode == 2;
-  if (p.D == 128)
-    return mode == 1 ? cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<128>, p)
-                     : cudaLaunchKernelEx(&cfg, rope_kv_store_token_kernel<128>, p, varlen);
-  if (p.D == 64)
-    return mode == 1 ? cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<64>, p)
-                     : cudaLaunchKernelEx(&cfg, rope_kv_store_token_kernel<64>, p, varlen);
+  auto go = [&](auto d, auto f16) {
+    constexpr int kD = decltype(d)::value;
+    constexpr bool kF16 = decltype(f16)::value;
+    return mode == 1 ? cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<kD, kF16>, p)
+                     : cudaLaunchKernelEx(&cfg, rope_kv_store_token_kernel<kD, kF16>, p, varlen);
+  };
+  using T = std::true_type;
+  using F = std::false_type;
+  if (p.D == 128) return p.f16 ? go(std::integral_constant<int, 128>{}, T{}) : go(std::integral_constant<int, 128>{}, F{});
+  if (p.D == 64) return p.f16 ? go(std::integral_constant<int, 64>{}, T{}) : go(std::integral_constant<int, 64>{}, F{});
   return cudaErrorInvalidValue;
 }
 

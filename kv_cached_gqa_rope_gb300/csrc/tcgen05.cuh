@@ -63,16 +63,22 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Instruction descriptor of kind::f16: BF16 A and B, FP32 accumulator,
-// M x N tile; each operand K-major (0) or MN-major (1).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major, int a_mn_major = 0) {
+// Instruction descriptor of kind::f16: A and B both of one format
+// (ab_format 1 = BF16, 0 = FP16), FP32 accumulator, M x N tile; each operand
+// K-major (0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(uint32_t ab_format, int M, int N, int b_mn_major,
+                                                         int a_mn_major = 0) {
   return (1u << 4)                              // D format: F32
-         | (1u << 7)                            // A format: BF16
-         | (1u << 10)                           // B format: BF16
+         | (ab_format << 7)                     // A format
+         | (ab_format << 10)                    // B format
          | (static_cast<uint32_t>(a_mn_major) << 15)
          | (static_cast<uint32_t>(b_mn_major) << 16)
          | (static_cast<uint32_t>(N >> 3) << 17)
          | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major, int a_mn_major = 0) {
+  return idesc_f16kind_f32(1u, M, N, b_mn_major, a_mn_major);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout a TMA load

@@ -321,6 +321,25 @@ def scaled_prefill(wl: PrefillWorkload, **kw) -> PrefillWorkload:
     return PrefillWorkload(**d)
 
 
+F16_SENTINEL_BITS = 0x7BFF  # 65504, the largest finite binary16 value
+
+
+def to_f16(t: torch.Tensor) -> torch.Tensor:
+    """The FP16-storage form of a BF16 workload tensor: every value converted
+    (BF16 draws of N(0, 1) are binary16 values, except the rare ones below
+    2^-14, which round), and unused-cell sentinels mapped to the largest
+    finite binary16 value (0x7F7F itself would overflow to infinity)."""
+    bits = t.view(torch.int16)
+    out = t.to(torch.float16)
+    out.view(torch.int16)[bits == SENTINEL_BITS] = F16_SENTINEL_BITS
+    return out
+
+
+def bits16(t: torch.Tensor):
+    """16-bit tensor (BF16 or FP16) -> numpy uint16 array of its patterns."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
+
+
 def bf16_bits(t: torch.Tensor):
     """BF16 tensor -> numpy uint16 array of its bit patterns (a view copy)."""
     return t.contiguous().view(torch.int16).numpy().view("uint16")

@@ -24,8 +24,9 @@ numpy operations (a matrix product is the only library primitive used):
   groups there, one call here).
 
 Storage is BF16 (16-bit patterns in numpy ``uint16`` arrays), or IEEE
-binary16 where a function is given ``fmt="f16"`` (the FP16 cached rows the
-pages' typed softmax also serves); arithmetic is float64; results that the
+binary16 where a function is given ``fmt="f16"`` (the FP16 cached rows that
+microLLM-rocm operator-development.md, section "Public interfaces", has its
+typed softmax serve beside BF16); arithmetic is float64; results that the
 path stores are rounded once, directly from float64, to nearest-even in the
 storage format.
 

@@ -77,7 +77,15 @@ def test_store_dtype_rejected():
     assert code_of(call_store, positions=torch.zeros(2, dtype=torch.float32)) == "EDTYPE"
     assert code_of(call_store, cache_rows=torch.zeros(2, dtype=torch.uint8)) == "EDTYPE"
     with pytest.raises(TypeError):          # no C dtype for it at all
-        call_store(q=torch.zeros(2, 4, 64, dtype=torch.float16))
+        call_store(q=torch.zeros(2, 4, 64, dtype=torch.float64))
+    # FP16 storage is accepted only when every 16-bit operand is FP16
+    assert code_of(call_store, q=torch.zeros(2, 4, 64, dtype=torch.float16)) == "EDTYPE"
+    f16 = dict(q=torch.zeros(2, 4, 64, dtype=torch.float16), k=torch.zeros(2, 2, 64, dtype=torch.float16),
+               v=torch.zeros(2, 2, 64, dtype=torch.float16), q_out=torch.zeros(2, 4, 64, dtype=torch.float16),
+               k_cache=torch.zeros(4, 2, 16, 64, dtype=torch.float16))
+    assert code_of(call_store, **f16) == "EDTYPE"                     # v_cache still bf16
+    f16["v_cache"] = torch.zeros(4, 2, 16, 64, dtype=torch.float16)
+    assert code_of(call_store, **f16) in ("ECUDA", "EDEVICE", "OK")    # past the dtype checks
 
 
 def test_store_layout_rejected():
