@@ -98,6 +98,13 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def whole_job_rate(units_per_rank: float, seconds: float, world: int) -> float:
+    """Whole-job throughput of N replicas: every rank processes the same
+    units, so the job's rate is all ranks' units over the slowest rank's
+    time (taken across ranks)."""
+    return units_per_rank * world / max_over_ranks(seconds, world)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -324,9 +331,9 @@ def run_ours(args, rank, world, local):
     else:
         step_ms = timed(two_call_body, host_us["store"] + host_us["attention"])
     barrier(world)
-    total_ms = max_over_ranks(float(sum(step_ms)), world)
+    tokens_per_s = whole_job_rate(wl.A * K, float(sum(step_ms)) / 1e3, world)
+    total_ms = wl.A * K * world / tokens_per_s * 1e3  # the slowest rank's K steps
     attn_bytes, step_bytes, fused_bytes = decode_bytes(wl, inp.positions.numpy())
-    tokens_per_s = wl.A * K * world / (total_ms / 1e3)
     # (2) the attention call alone: the dominant kernel, for the roofline
     attn_ms = timed(attention_body, host_us["store"] + host_us["attention"])
     attn_avg_s = max_over_ranks(float(np.mean(attn_ms)), world) / 1e3
@@ -419,8 +426,7 @@ def run_ours(args, rank, world, local):
         t0 = time.perf_counter()
         e2e_step()
         e2e_total += time.perf_counter() - t0
-    e2e_total = max_over_ranks(e2e_total, world)
-    e2e_value = wl.A * K * world / e2e_total
+    e2e_value = whole_job_rate(wl.A * K, e2e_total, world)
 
     # ---- prefill: 16 prompts x 1024 tokens into empty rows
     prefill = None
