@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp16", action="store_true", help="skip the FP16-storage measurements")
+    ap.add_argument("--no-decode-workloads", action="store_true",
+                    help="skip the attention call on the divergent-length and long-context decode workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="run just the timed decode steps or just the prefill calls (for profiler captures)")
@@ -428,6 +430,12 @@ def run_ours(args, rank, world, local):
         e2e_total += time.perf_counter() - t0
     e2e_value = whole_job_rate(wl.A * K, e2e_total, world)
 
+    # ---- the attention call on the other decode workloads of the same path
+    decode_workloads = None
+    if not args.no_decode_workloads:
+        decode_workloads = [run_attention_workload(args, kv, w_, dev, stream, flush, world, hbm_peak)
+                            for w_ in (W.DIVERGENT_DECODE, W.LONG_DECODE)]
+
     # ---- prefill: 16 prompts x 1024 tokens into empty rows
     prefill = None
     if not args.no_prefill:
@@ -468,6 +476,8 @@ def run_ours(args, rank, world, local):
         "host_us_per_call": host_us,
         "clocks": clocks,
     }
+    if decode_workloads is not None:
+        line["decode_workloads"] = decode_workloads
     if prefill is not None:
         line["prefill"] = prefill
     if fp16 is not None:
@@ -475,6 +485,44 @@ def run_ours(args, rank, world, local):
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
+
+
+def run_attention_workload(args, kv, wl, dev, stream, flush, world, hbm_peak):
+    """The attention call (cached_gqa_attention_out_) on another decode
+    workload, timed like the roofline number: the store call outside the
+    events, the attention call inside, L2 flushed before each step."""
+    inp = W.make_decode_inputs(wl)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    pos, rows = inp.positions.to(dev), inp.cache_rows.to(dev)
+    kc, vc = inp.build_cache(dev)
+    q_rot, out = torch.empty_like(q), torch.empty_like(q)
+    ws1 = kv.new_workspace(kv.rope_kv_store_workspace_size(), dev)
+    ws2 = kv.new_workspace(kv.cached_gqa_attention_workspace_size(wl.A, wl.H_q, wl.H_kv, wl.D), dev)
+    store = kv.prepare_rope_kv_store_out_(q, k, v, pos, rows, wl.theta, q_rot, kc, vc, ws1, stream)
+    attend = kv.prepare_cached_gqa_attention_out_(q_rot, kc, vc, pos, rows, wl.scale, out, ws2, stream)
+    for _ in range(max(args.warmup, 3)):
+        store()
+        attend()
+    K = max(10, min(args.steps, 100))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    hold_gpu(K * 80.0)
+    for i in range(K):
+        flush()
+        store()
+        ev[i][0].record(stream)
+        attend()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if kv.kvgqa_read_status(ws1) or kv.kvgqa_read_status(ws2):
+        raise RuntimeError(f"device status flags set ({wl.name})")
+    avg_s = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world) / 1e3
+    attn_bytes = decode_bytes(wl, inp.positions.numpy())[0]
+    gbs = attn_bytes / avg_s / 1e9
+    return {"workload": wl.name, "attention_ms": round(avg_s * 1e3, 5), "attention_bytes": attn_bytes,
+            "kv_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+            "tokens_per_s": round(wl.A * world / avg_s, 1)}
 
 
 def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src, f16=False):

@@ -140,6 +140,37 @@ def test_edge_positions_and_groups(D, H_q, H_kv):
     assert run.status() == (0, 0)
 
 
+@pytest.mark.parametrize("step", [False, True], ids=["two_calls", "decode_step"])
+def test_max_active_rows(step):
+    """The largest batch the decode kernels take (1024 active rows, every
+    slot of a 1024-slot cache active, positions spread over the whole row),
+    checked in full against the oracle; the whole-step call must give the
+    same bytes as the two calls."""
+    wl = W.DecodeWorkload(name="max_rows", index=16, slots=1024, max_seq=160, A=1024, H_q=8, H_kv=2, D=64,
+                          theta=10000.0, positions="uniform", pos_lo=0, pos_hi=160)
+    inp = W.make_decode_inputs(wl)
+    run = DecodeRun(inp, cache_guard=4096)
+    q_rot_o, k_rot_o = check_store(inp, run)
+    run.attention(q_rot=run.q_out)
+    torch.cuda.synchronize()
+    ref = oracle_attention(inp, list(range(wl.A)), q_rot_bits=q_rot_o, extra_cell=(k_rot_o, W.bf16_bits(inp.v)))
+    assert_attention_close(run.out.cpu(), ref, "1024 active rows")
+    assert run.guards_intact()
+    assert run.status() == (0, 0)
+    if step:
+        import kv_cached_gqa_rope_gb300 as kv
+        kc, vc = inp.build_cache("cuda")
+        out2 = torch.empty_like(run.out)
+        ws = kv.new_workspace(kv.decode_step_workspace_size(wl.A, wl.H_q, wl.H_kv, wl.D), "cuda")
+        kv.decode_step_out_(run.q, run.k, run.v, run.positions, run.cache_rows, wl.theta, wl.scale, kc, vc,
+                            out2, ws)
+        torch.cuda.synchronize()
+        assert kv.kvgqa_read_status(ws) == 0
+        assert torch.equal(out2.view(torch.int16), run.out.view(torch.int16))
+        assert torch.equal(kc.view(torch.int16), run.k_cache.view(torch.int16))
+        assert torch.equal(vc.view(torch.int16), run.v_cache.view(torch.int16))
+
+
 def test_single_key_returns_v_exactly():
     """Position 0: the only key is the token itself, so out == V bit for bit."""
     wl = W.DecodeWorkload(name="pos0", index=12, slots=8, max_seq=64, A=5, H_q=32, H_kv=8, D=128,
