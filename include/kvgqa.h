@@ -393,6 +393,17 @@ kvgqa_status kvgqa_metadata_upload(const int32_t* host_meta, int32_t capacity, c
  * This is the only call that waits for the device. */
 kvgqa_status kvgqa_read_status(const kvgqa_tensor* workspace, void* stream, int32_t* flags);
 
+/* Diagnostic: check on the device that the library's waits end.  Launches on
+ * `stream` one CTA that holds tensor memory and waits, with the bounded wait
+ * every kernel here uses, on an mbarrier nothing ever arrives on.  After the
+ * bound (2 s) the wait gives up and sets KVGQA_FLAG_TIMEOUT in the status word
+ * of `workspace`; the CTA frees its tensor memory and returns, and the
+ * context stays usable (the same path a kernel takes when a copy or MMA it
+ * waits for never completes).  No counterpart in the pages: a test hook.
+ *   workspace  >= 256 bytes, 256-byte aligned, device memory (status word set)
+ * Read the result with kvgqa_read_status(). */
+kvgqa_status kvgqa_check_bounded_wait(const kvgqa_tensor* workspace, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -96,6 +96,8 @@ def _load():
         getattr(lib, name).restype = st
     lib.kvgqa_read_status.argtypes = [P, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.kvgqa_read_status.restype = st
+    lib.kvgqa_check_bounded_wait.argtypes = [P, ctypes.c_void_p]
+    lib.kvgqa_check_bounded_wait.restype = st
     return lib
 
 
@@ -108,7 +110,8 @@ EXPORTED_SYMBOLS = ("kvgqa_abi_version", "kvgqa_last_error", "rope_kv_store_work
                     "cached_gqa_attention_static_scratch_out_", "decode_step_workspace_size",
                     "decode_step_out_", "kvgqa_slots_create", "kvgqa_slots_destroy", "kvgqa_slots_admit",
                     "kvgqa_slots_release", "kvgqa_slots_step", "kvgqa_slots_query", "kvgqa_metadata_upload",
-                    "prefill_varlen_gqa_cached_rows_out_", "decode_step_single_launch_out_")
+                    "prefill_varlen_gqa_cached_rows_out_", "decode_step_single_launch_out_",
+                    "kvgqa_check_bounded_wait")
 
 
 def library() -> ctypes.CDLL:
@@ -300,6 +303,13 @@ def kvgqa_read_status(workspace, stream=None) -> int:
     flags = ctypes.c_int32()
     _check(_lib.kvgqa_read_status(_ref(w), _stream(stream), ctypes.byref(flags)))
     return flags.value
+
+
+def kvgqa_check_bounded_wait(workspace, stream=None) -> None:
+    """Queue the bounded-wait check (include/kvgqa.h); its result is the
+    KVGQA_FLAG_TIMEOUT bit that kvgqa_read_status(workspace) then returns."""
+    w = describe(workspace)
+    _check(_lib.kvgqa_check_bounded_wait(_ref(w), _stream(stream)))
 
 
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:

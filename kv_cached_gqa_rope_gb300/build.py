@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libkvgqa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "rope_kv_store.cu", "flash_decode.cu", "flash_decode_f16.cu", "prefill_attention.cu"]
+SOURCES = ["api.cu", "rope_kv_store.cu", "flash_decode.cu", "flash_decode_f16.cu", "prefill_attention.cu",
+           "wait_check.cu"]
 
 
 def nvcc_path() -> str:

@@ -761,6 +761,16 @@ kvgqa_status kvgqa_metadata_upload(const int32_t* host_meta, int32_t capacity, c
   });
 }
 
+kvgqa_status kvgqa_check_bounded_wait(const kvgqa_tensor* workspace, void* stream) {
+  return guarded([&] {
+    View vws = check_workspace(workspace, KVGQA_STATUS_BYTES);
+    check_device({&vws}, current_device());
+    check_cuda(kvgqa::launch_bounded_wait_check(static_cast<int32_t*>(workspace->data),
+                                                static_cast<cudaStream_t>(stream)),
+               "bounded-wait check launch");
+  });
+}
+
 kvgqa_status kvgqa_read_status(const kvgqa_tensor* workspace, void* stream, int32_t* flags) {
   return guarded([&] {
     if (!flags) fail(KVGQA_EINVAL, "flags: null");

@@ -106,4 +106,8 @@ struct PrefillParams {
 
 cudaError_t launch_prefill_attention(const PrefillParams& p, cudaStream_t stream);
 
+// ------------------------------------------------------------------ bounded-wait check
+// One CTA whose only wait can never complete (kvgqa_check_bounded_wait).
+cudaError_t launch_bounded_wait_check(int32_t* status, cudaStream_t stream);
+
 }  // namespace kvgqa

@@ -30,7 +30,7 @@ typed softmax serve beside BF16); arithmetic is float64; results that the
 path stores are rounded once, directly from float64, to nearest-even in the
 storage format.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   - pair i of a head is (x[i], x[i + D/2]) and rotates by angle pos * theta^(-2i/D),
     y[i] = x[i] cos - x[i+D/2] sin, y[i+D/2] = x[i+D/2] cos + x[i] sin;
   - the decode token attends to keys 0..pos inclusive (its own K/V is stored first);
