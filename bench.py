@@ -438,8 +438,10 @@ def run_ours(args, rank, world, local):
 
     # ---- prefill: 16 prompts x 1024 tokens into empty rows
     prefill = None
+    prefill_varlen = None
     if not args.no_prefill:
         prefill = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
+        prefill_varlen = run_prefill_varlen(args, kv, dev, stream, flush, world, bf16_peak, peak_src)
         if fp16 is not None:
             fp16["prefill"] = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src,
                                           f16=True)
@@ -480,6 +482,8 @@ def run_ours(args, rank, world, local):
         line["decode_workloads"] = decode_workloads
     if prefill is not None:
         line["prefill"] = prefill
+    if prefill_varlen is not None:
+        line["prefill_varlen"] = prefill_varlen
     if fp16 is not None:
         line["fp16"] = fp16
     if not args.no_cpu_baseline and world == 1:
@@ -565,6 +569,55 @@ def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_
             "peak": bf16_peak,
             "peak_source": f"{peak_src} burst bf16_tflops" + (" (FP16 dense rate = BF16 rate, nominal ratio 1)" if f16 else ""),
             "note": "whole call: RoPE + store of all prompts, then causal attention", "gpu_launches": 2 * K}
+
+
+def varlen_flops(wl, offsets, lengths):
+    """Algorithmic FLOPs of the chunked prefill: query t of prompt a sees keys
+    0 .. off_a + t, each key costing 2*D for q.k and 2*D for p.v, per head."""
+    keys = sum(n * o + n * (n + 1) // 2 for o, n in zip(offsets, lengths))
+    return 4.0 * wl.D * wl.H_q * keys
+
+
+def run_prefill_varlen(args, kv, dev, stream, flush, world, bf16_peak, peak_src):
+    """The chunked prefill (prefill_varlen_gqa_cached_rows_out_) on a
+    serving-shaped mix of the prefill workload's shapes: 16 prompts of
+    lengths uniform in [1, 1024] (padded to 1024), each continuing a prefix
+    at an offset uniform in [0, 2048 - length] of its row."""
+    pw = W.PREFILL
+    offs, lens = W.random_offsets_lengths(pw)
+    inp = W.make_varlen_inputs(pw, offs, lens)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    off_t, len_t, rows = inp.offsets.to(dev), inp.lengths.to(dev), inp.cache_rows.to(dev)
+    kc, vc = inp.build_cache(dev)
+    out = torch.empty_like(q)
+    ws = kv.new_workspace(kv.prefill_gqa_cached_rows_workspace_size(pw.A, pw.T, pw.H_q, pw.H_kv, pw.D), dev)
+    call = kv.prepare_prefill_varlen_gqa_cached_rows_out_(q, k, v, off_t, len_t, rows, pw.theta, pw.scale, kc, vc,
+                                                          out, ws, stream)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    K = max(10, min(args.steps, 100))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    hold_gpu(K * 100.0)
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if kv.kvgqa_read_status(ws):
+        raise RuntimeError("device status flags set in the chunked prefill")
+    avg = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world)
+    flops = varlen_flops(pw, offs, lens)
+    tflops = flops / (avg / 1e3) / 1e12
+    return {"workload": pw.name + "_chunks_len_u1_1024_off_u", "tokens": int(sum(lens)),
+            "ms_per_call": round(avg, 5), "flops": flops, "tflops": round(tflops, 1),
+            "frac_of_bf16_peak": round(tflops / bf16_peak, 4), "peak": bf16_peak,
+            "peak_source": f"{peak_src} burst bf16_tflops",
+            "note": "whole call: RoPE + store of every prompt's tokens at its offset, then attention over the row "
+                    "prefix and the prompt", "gpu_launches": 2 * K}
 
 
 # ---------------------------------------------------------------------- CPU oracle

@@ -297,6 +297,15 @@ def prepare_prefill_gqa_cached_rows_out_(q, k, v, cache_rows, theta, scale, k_ca
                     (ds, q, k, v, cache_rows, k_cache, v_cache, out, workspace))
 
 
+def prepare_prefill_varlen_gqa_cached_rows_out_(q, k, v, offsets, lengths, cache_rows, theta, scale, k_cache,
+                                                v_cache, out, workspace, stream=None) -> Prepared:
+    ds = [describe(t) for t in (q, k, v, offsets, lengths, cache_rows, k_cache, v_cache, out, workspace)]
+    args = (*map(_ref, ds[:6]), ctypes.c_double(theta), ctypes.c_float(scale), *map(_ref, ds[6:]),
+            ctypes.c_void_p(_stream(stream)))
+    return Prepared(_lib.prefill_varlen_gqa_cached_rows_out_, args,
+                    (ds, q, k, v, offsets, lengths, cache_rows, k_cache, v_cache, out, workspace))
+
+
 def kvgqa_read_status(workspace, stream=None) -> int:
     """Synchronise the stream, return and clear the workspace status word."""
     w = describe(workspace)
