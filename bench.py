@@ -288,7 +288,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     if args.only == "prefill":
         res = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
-        return {"impl": "ours", "only": "prefill", "prefill": res} if rank == 0 else None
+        res_v = run_prefill_varlen(args, kv, dev, stream, flush, world, bf16_peak, peak_src)
+        return {"impl": "ours", "only": "prefill", "prefill": res, "prefill_varlen": res_v} if rank == 0 else None
     calls = [("store", store), ("attention", attend)] + ([("step", step), ("single_launch_step", single)]
                                                           if args.only is None else [])
     host_us = host_call_us(calls, n=min(200, 10 * args.steps))

@@ -273,8 +273,10 @@ kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
                                                       const kvgqa_tensor* cache_rows, float scale,
                                                       const kvgqa_tensor* out, void* stream);
 
-/* Workspace of prefill_gqa_cached_rows_out_: the status block plus the rotated
- * queries (A*T*H_q*D bf16). */
+/* Workspace of prefill_gqa_cached_rows_out_ and prefill_varlen_gqa_cached_rows_out_:
+ * the status block, the rotated queries (A*T*H_q*D 16-bit values, rounded up
+ * to 256 bytes) and, used by the varlen call, an order of its work items (one
+ * int32 per 128-query tile of each prompt). */
 kvgqa_status prefill_gqa_cached_rows_workspace_size(int64_t A, int64_t T, int64_t H_q,
                                                     int64_t H_kv, int64_t D, size_t* bytes);
 

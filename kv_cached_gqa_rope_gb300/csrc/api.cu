@@ -22,6 +22,17 @@
 
 namespace {
 
+// Prefill workspace: the status block, the rotated queries (A*T*H_q*D 16-bit
+// values, rounded up to 256 bytes), then the varlen item order (one int32 per
+// (query tile, prompt) pair).
+size_t prefill_qrot_bytes(int64_t A, int64_t T, int64_t H_q, int64_t D) {
+  return (static_cast<size_t>(A) * T * H_q * D * 2 + 255) / 256 * 256;
+}
+size_t prefill_workspace_bytes(int64_t A, int64_t T, int64_t H_q, int64_t D) {
+  return KVGQA_STATUS_BYTES + prefill_qrot_bytes(A, T, H_q, D) +
+         static_cast<size_t>(kvgqa::prefill_order_entries(A, T)) * sizeof(int32_t);
+}
+
 thread_local std::string g_last_error;
 
 struct Fail {
@@ -567,7 +578,7 @@ kvgqa_status prefill_gqa_cached_rows_workspace_size(int64_t A, int64_t T, int64_
     if (A < 0 || T < 0) fail(KVGQA_EINVAL, "negative size");
     check_head_dim(D);
     check_heads(H_q, H_kv);
-    *bytes = KVGQA_STATUS_BYTES + static_cast<size_t>(A) * T * H_q * D * 2;
+    *bytes = prefill_workspace_bytes(A, T, H_q, D);
   });
 }
 
@@ -612,8 +623,7 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
     require_shape(voff, {A});
     require_shape(vlen, {A});
   }
-  const size_t need = KVGQA_STATUS_BYTES + static_cast<size_t>(A) * T * H_q * D * 2;
-  View vws = check_workspace(workspace, need);
+  View vws = check_workspace(workspace, prefill_workspace_bytes(A, T, H_q, D));
   if (varlen) {
     check_no_alias({&vkc, &vvc, &vo, &vws}, {&vq, &vk, &vv, &vr, &voff, &vlen, &vkc, &vvc, &vo, &vws});
   } else {
@@ -629,6 +639,7 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
   kvgqa::RopeStoreParams rp{};
   unsigned char* ws = static_cast<unsigned char*>(workspace->data);
   uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + KVGQA_STATUS_BYTES);
+  int32_t* order = reinterpret_cast<int32_t*>(ws + KVGQA_STATUS_BYTES + prefill_qrot_bytes(A, T, H_q, D));
   rp.q = static_cast<const uint16_t*>(q->data);
   rp.k = static_cast<const uint16_t*>(k->data);
   rp.v = static_cast<const uint16_t*>(v->data);
@@ -637,6 +648,7 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
   rp.offsets = varlen ? static_cast<const int32_t*>(offsets->data) : nullptr;
   rp.lengths = varlen ? static_cast<const int32_t*>(lengths->data) : nullptr;
   rp.q_out = q_rot;
+  rp.item_order = varlen ? order : nullptr;
   rp.k_cache = static_cast<uint16_t*>(k_cache->data);
   rp.v_cache = static_cast<uint16_t*>(v_cache->data);
   rp.status = reinterpret_cast<int32_t*>(ws);
@@ -653,6 +665,7 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
   pp.cache_rows = rp.cache_rows;
   pp.offsets = rp.offsets;
   pp.lengths = rp.lengths;
+  pp.item_order = rp.item_order;
   pp.out = static_cast<uint16_t*>(out->data);
   pp.status = rp.status;
   pp.A = (int)A; pp.T = (int)T; pp.H_q = (int)H_q; pp.H_kv = (int)H_kv; pp.G = (int)(H_q / H_kv);

@@ -25,6 +25,7 @@ struct RopeStoreParams {
   const int32_t* offsets;    // varlen prefill [A]: position of each prompt's first token
   const int32_t* lengths;    // varlen prefill [A]: tokens of each prompt (<= T)
   uint16_t* q_out;           // rotated Q, same layout as q
+  int32_t* item_order;       // varlen prefill: (query tile, prompt) pairs, longest first (written by CTA 0)
   uint16_t* k_cache;         // [S,H_kv,max_seq,D]
   uint16_t* v_cache;
   int32_t* status;
@@ -97,6 +98,10 @@ struct PrefillParams {
   const int32_t* cache_rows;  // [A]
   const int32_t* offsets;     // [A] or nullptr (all 0): position of each prompt's first token
   const int32_t* lengths;     // [A] or nullptr (all T): tokens of each prompt
+  // Prompts at offsets: the pairs c = qt * A + a (query tile qt of prompt a)
+  // ordered by their key tiles, most first (see kPrefillTile); nullptr for
+  // the equal-length prefill, whose query tile index already orders them.
+  const int32_t* item_order;
   uint16_t* out;              // [A,T,H_q,D]
   int32_t* status;
   int A, T, H_q, H_kv, G, D, S, max_seq;
@@ -105,6 +110,11 @@ struct PrefillParams {
 };
 
 cudaError_t launch_prefill_attention(const PrefillParams& p, cudaStream_t stream);
+
+// Query and key tile of the prefill attention kernel; the varlen prefill's
+// item order has one entry per (query tile, prompt) pair.
+constexpr int kPrefillTile = 128;
+inline int64_t prefill_order_entries(int64_t A, int64_t T) { return A * ((T + kPrefillTile - 1) / kPrefillTile); }
 
 // ------------------------------------------------------------------ bounded-wait check
 // One CTA whose only wait can never complete (kvgqa_check_bounded_wait).

@@ -47,6 +47,7 @@ namespace {
 
 constexpr int BM = 128;        // query rows per tile
 constexpr int BN = 128;        // keys per tile
+static_assert(BM == kPrefillTile && BN == kPrefillTile, "the varlen item order counts tiles of this size");
 constexpr int SUB = 16384;     // one [128 rows x 64 16-bit values] swizzled sub-tile
 constexpr int NWARPS = 12;     // 2 x 4 softmax + Q/K producer + V producer + MMA + spare
 constexpr int THREADS = NWARPS * 32;
@@ -120,7 +121,9 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // The work of the persistent grid: items (query tile qt, prompt a, head pair),
-// longest first (query tile qt of prompt a covers queries [qt*BM, qt*BM+BM)
+// longest first (by query tile for the equal-length prefill, by the item
+// order the store kernel wrote for prompts at offsets; query tile qt of
+// prompt a covers queries [qt*BM, qt*BM+BM)
 // at positions off_a + t and visits the key tiles up to its last query's
 // position), dealt round-robin; every role of a CTA walks the same sequence,
 // key tile by key tile.  Prompt a holds len_a tokens at positions
@@ -138,16 +141,26 @@ struct TileWalk {
   __device__ __forceinline__ int per_tok() const { return pairs() ? p->H_q / 2 : p->H_q; }
   __device__ __forceinline__ int units() const { return p->A * per_tok(); }
   __device__ __forceinline__ int n_items() const { return (p->T + BM - 1) / BM * units(); }
-  // Prompt a of item i (the same for every query tile).
-  __device__ __forceinline__ int prompt_of(int item) const { return item % units() / per_tok(); }
+  // Prompt a of item i.
+  __device__ __forceinline__ int prompt_of(int item) const {
+    return p->item_order ? p->item_order[item / per_tok()] % p->A : item % units() / per_tok();
+  }
 
   __device__ bool load_item() {
     const int nqt = (p->T + BM - 1) / BM, u = units(), pt = per_tok(), n = nqt * u;
     while (i < n) {
-      qt = nqt - 1 - i / u;
-      const int rem = i % u;
-      a = rem / pt;
-      const int k = rem % pt;
+      int k;
+      if (p->item_order) {  // prompts at offsets: pairs (qt, a) longest first, then the head pairs
+        const int c = p->item_order[i / pt];
+        qt = c / p->A;
+        a = c % p->A;
+        k = i % pt;
+      } else {              // equal length: query tiles from the last (longest) down
+        qt = nqt - 1 - i / u;
+        const int rem = i % u;
+        a = rem / pt;
+        k = rem % pt;
+      }
       hA = pairs() ? 2 * k : k;
       hB = pairs() ? 2 * k + 1 : -1;
       const int r = p->cache_rows[a];

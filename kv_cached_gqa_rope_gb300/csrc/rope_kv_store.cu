@@ -152,6 +152,43 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
 
 constexpr int kTokenSplit = 4;     // CTAs per token (decode, prompts at offsets)
 constexpr int kTokenThreads = 128;
+constexpr int kOrderBins = 512;    // key-tile counts told apart by the item order (larger ones share a bin)
+
+// Prompts at offsets: the attention kernel deals its items (query tile qt of
+// prompt a, all head pairs) round-robin over a persistent grid, so it wants
+// them longest first, and with prefixes at offsets the query tile index no
+// longer orders them.  One CTA (the caller's) counting-sorts the pairs
+// c = qt * A + a by their key tiles (the tiles holding positions
+// 0 .. off + min(len, qt*T + T) - 1; 0 for a pair with no work or invalid
+// metadata, which the attention kernel skips) into p.item_order, most first.
+// The order of pairs with equal counts is not fixed; no result depends on it.
+__device__ void write_item_order(const RopeStoreParams& p) {
+  __shared__ int bins[kOrderBins];
+  const int nqt = (p.T + kPrefillTile - 1) / kPrefillTile;
+  const int n = p.A * nqt;
+  auto key = [&](int c) {
+    const int qt = c / p.A, a = c % p.A;
+    const int row = p.cache_rows[a], off = p.offsets[a], len = p.lengths[a];
+    const bool ok = row >= 0 && row < p.S && len >= 0 && len <= p.T && off >= 0 && off <= p.max_seq - len;
+    if (!ok || qt * kPrefillTile >= len) return 0;
+    const int kend = off + min(len, qt * kPrefillTile + kPrefillTile);
+    return min((kend + kPrefillTile - 1) / kPrefillTile, kOrderBins - 1);
+  };
+  for (int b = threadIdx.x; b < kOrderBins; b += blockDim.x) bins[b] = 0;
+  __syncthreads();
+  for (int c = threadIdx.x; c < n; c += blockDim.x) atomicAdd(&bins[key(c)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {  // start of each bin, largest count first
+    int run = 0;
+    for (int b = kOrderBins - 1; b >= 0; --b) {
+      const int cnt = bins[b];
+      bins[b] = run;
+      run += cnt;
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < n; c += blockDim.x) p.item_order[atomicAdd(&bins[key(c)], 1)] = c;
+}
 
 // One token at its own position: decode (token a at positions[a], varlen = 0)
 // or the prefill of prompts at offsets (token t of prompt a at offsets[a] + t,
@@ -171,6 +208,7 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(cons
 
   pdl_wait();     // inputs and outputs may belong to the previous kernel
   pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
+  if (varlen && p.item_order && blockIdx.x == 0) write_item_order(p);
   const int tk = blockIdx.x / kTokenSplit, part = blockIdx.x % kTokenSplit;
   const size_t tok = tk;  // index in the token-major inputs
   const int rot_items = (p.H_q + p.H_kv) * UF;

@@ -34,7 +34,8 @@ def test_abi_version():
 
 def test_workspace_sizes():
     assert kv.rope_kv_store_workspace_size() == 256
-    assert kv.prefill_gqa_cached_rows_workspace_size(16, 1024, 32, 8, 128) == 256 + 16 * 1024 * 32 * 128 * 2
+    # status block + rotated queries + one int32 per (128-query tile, prompt) pair
+    assert kv.prefill_gqa_cached_rows_workspace_size(16, 1024, 32, 8, 128) == 256 + 16 * 1024 * 32 * 128 * 2 + 16 * 8 * 4
     assert kv.prefill_gqa_cached_rows_workspace_size(0, 0, 4, 2, 64) == 256
     with pytest.raises(kv.KvgqaError) as e:
         kv.prefill_gqa_cached_rows_workspace_size(1, 1, 4, 2, 96)
@@ -194,7 +195,7 @@ def prefill_args(A=2, T=8, H_q=4, H_kv=2, D=64, S=4, L=16):
                 v=torch.zeros(A, T, H_kv, D, dtype=bf), cache_rows=torch.arange(A, dtype=torch.int32),
                 theta=1e4, scale=0.125, k_cache=torch.zeros(S, H_kv, L, D, dtype=bf),
                 v_cache=torch.zeros(S, H_kv, L, D, dtype=bf), out=torch.zeros(A, T, H_q, D, dtype=bf),
-                workspace=aligned_bytes(256 + A * T * H_q * D * 2))
+                workspace=aligned_bytes(256 + (A * T * H_q * D * 2 + 255) // 256 * 256 + A * ((T + 127) // 128) * 4))
 
 
 def test_prefill_contract():
