@@ -230,6 +230,13 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(cons
       xa = *reinterpret_cast<const uint4*>(p.v + (tok * p.H_kv + u / VU) * D + (u % VU) * 8);
     }
   };
+  // Prompts at offsets are padded to T: a token past its prompt's length
+  // has no work, and its CTAs leave before loading anything.
+  if (varlen) {
+    const int off = p.offsets[tk / p.T], len = p.lengths[tk / p.T];
+    const bool meta_ok = len >= 0 && len <= p.T && off >= 0 && off <= p.max_seq - len;
+    if (meta_ok && tk % p.T >= len) return;  // (invalid metadata is flagged below)
+  }
   uint4 xa[kBatch], xb[kBatch];
 #pragma unroll
   for (int b = 0; b < kBatch; ++b) {
