@@ -125,12 +125,16 @@ __device__ __forceinline__ float ex2(float x) {
 // order the store kernel wrote for prompts at offsets; query tile qt of
 // prompt a covers queries [qt*BM, qt*BM+BM)
 // at positions off_a + t and visits the key tiles up to its last query's
-// position), dealt round-robin; every role of a CTA walks the same sequence,
+// position), dealt in snake order (round k gives item k*grid + b to CTA b on
+// even rounds and to CTA grid-1-b on odd ones, which evens out the sums of a
+// list sorted longest first much better than plain round-robin); every role
+// of a CTA walks the same sequence,
 // key tile by key tile.  Prompt a holds len_a tokens at positions
 // off_a .. off_a+len_a-1 of its row (the equal-length prefill: off 0, len T).
 struct TileWalk {
   const PrefillParams* p;     // the launch's parameters (read in place)
-  int i, stride;
+  int i;                      // current item index
+  int cta, grid, round;       // this CTA, the grid size, the dealing round of item i
   int qt, a, hA, hB, kv_row;  // current item (hB < 0: single head)
   int off, len, nkt, kend;    // its prompt's offset and length, its key tiles, its last key + 1
   int j;                      // key tile within the item
@@ -179,14 +183,20 @@ struct TileWalk {
       }
       // prompts with an invalid row or metadata are skipped (and flagged by
       // the store kernel); query tiles past a prompt's length have no work
-      i += stride;
+      next_index();
     }
     return false;
   }
+  __device__ __forceinline__ void next_index() {
+    ++round;
+    i = round * grid + ((round & 1) ? grid - 1 - cta : cta);
+  }
   __device__ void init(const PrefillParams* params, int first, int step) {
     p = params;
+    cta = first;
+    grid = step;
+    round = 0;
     i = first;
-    stride = step;
     ok = load_item();
   }
   __device__ __forceinline__ bool first_tile() const { return j == 0; }
@@ -206,7 +216,7 @@ struct TileWalk {
   __device__ __forceinline__ int mask_lo() const { return j * BN - kstart(); }
   __device__ void advance() {
     if (j < nkt - 1) { ++j; return; }
-    i += stride;
+    next_index();
     ok = load_item();
   }
 };
