@@ -195,21 +195,17 @@ __device__ void write_item_order(const RopeStoreParams& p) {
 // t < lengths[a], varlen = 1).  CTA part s of the token rotates the pairs of
 // frequencies [s*F, s*F + F) of every Q and K head, F = D/2 / kTokenSplit, and
 // copies part s of its V bytes.
+// The work of part `part` of token tk (decode: token tk = a; prompts at
+// offsets: token tk = a*T + t).  Returns early, uniformly over the CTA, for a
+// token with no work.
 template <int D, bool F16>
-__global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(const __grid_constant__ RopeStoreParams p,
-                                                                          int varlen) {
+__device__ __forceinline__ void token_body(const RopeStoreParams& p, int varlen, int tk, int part, CosSin* cs) {
   constexpr int HALF = D / 2;
   constexpr int F = HALF / kTokenSplit;  // frequencies of this CTA
   constexpr int UF = F / 8;              // rotation units (8 pairs) per head
   constexpr int VU = D / 8;              // V copy units (16 bytes) per head
   constexpr int kBatch = 2;
   static_assert(F % 8 == 0, "a CTA's frequencies are whole 16-byte units");
-  __shared__ CosSin cs[F + F / 8];
-
-  pdl_wait();     // inputs and outputs may belong to the previous kernel
-  pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
-  if (varlen && p.item_order && blockIdx.x == 0) write_item_order(p);
-  const int tk = blockIdx.x / kTokenSplit, part = blockIdx.x % kTokenSplit;
   const size_t tok = tk;  // index in the token-major inputs
   const int rot_items = (p.H_q + p.H_kv) * UF;
   const int copy_per_part = p.H_kv * VU / kTokenSplit;
@@ -307,10 +303,47 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(cons
   }
 }
 
+// Decode: part s = blockIdx % 4 of token blockIdx / 4 (one token per CTA
+// quartet).  Prompts at offsets: a grid sized to the GPU walks the padded
+// tokens (stride gridDim / 4), so the tokens past a prompt's length cost a
+// loop step, not a CTA launch.
+template <int D, bool F16>
+__global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(const __grid_constant__ RopeStoreParams p,
+                                                                          int varlen) {
+  constexpr int F = D / 2 / kTokenSplit;
+  __shared__ CosSin cs[F + F / 8];
+  pdl_wait();     // inputs and outputs may belong to the previous kernel
+  pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
+  if (varlen && p.item_order && blockIdx.x == 0) write_item_order(p);
+  const int part = blockIdx.x % kTokenSplit;
+  const int n_tok = varlen ? p.A * p.T : p.A;
+  const int step = gridDim.x / kTokenSplit;
+  for (int tk = blockIdx.x / kTokenSplit; tk < n_tok; tk += step) {
+    token_body<D, F16>(p, varlen, tk, part, cs);
+    __syncthreads();  // cs is rewritten for the next token
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_t stream) {
-  const long long g = mode == 1 ? p.T : (mode == 0 ? p.A : static_cast<long long>(p.A) * p.T) * kTokenSplit;
+  // Prompts at offsets: four CTAs of 128 threads per token in flight, 16 CTAs
+  // per SM (a grid-stride walk over the padded tokens).
+  static int sm_count[64];
+  static std::once_flag sm_once[64];
+  int dev0 = 0;
+  cudaError_t e0 = cudaGetDevice(&dev0);
+  if (e0 != cudaSuccess) return e0;
+  if (dev0 < 0 || dev0 >= 64) return cudaErrorInvalidDevice;
+  std::call_once(sm_once[dev0], [dev0] {
+    if (cudaDeviceGetAttribute(&sm_count[dev0], cudaDevAttrMultiProcessorCount, dev0) != cudaSuccess)
+      sm_count[dev0] = 0;
+  });
+  const long long varlen_tokens = static_cast<long long>(p.A) * p.T;
+  const long long varlen_cap = 4ll * (sm_count[dev0] > 0 ? sm_count[dev0] : 1);
+  const long long g = mode == 1 ? p.T
+                                : (mode == 0 ? p.A : (varlen_tokens < varlen_cap ? varlen_tokens : varlen_cap)) *
+                                      kTokenSplit;
   if (g > 0x7fffffffll) return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(g);
   if (grid == 0) return cudaSuccess;

@@ -15,22 +15,95 @@ struct __align__(16) CosSin {
   float ch, cl, sh, sl;  // cos = ch + cl, sin = sh + sl
 };
 
-// cos and sin of pos * inv_freq, as FP32 hi+lo pairs.  The angle is formed
-// in FP64 and reduced by 2*pi with a two-constant Cody-Waite step (2*pi split
-// in two doubles, the products fused), so sincos only ever sees |r| <= pi.
+// ---------------------------------------------------------------- double-float
+// A value held as an unevaluated sum h + l of two FP32 numbers (|l| <= ulp(h)/2),
+// with the error-free sum of Knuth and the FMA-based exact product (Dekker's
+// double-length arithmetic).  Intrinsics keep the compiler from contracting
+// or reordering the error terms.
+struct DF {
+  float h, l;
+};
+
+__device__ __forceinline__ DF df_fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return DF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ DF df_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return DF{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = df_two_sum(a.h, b.h);
+  return df_fast_two_sum(s.h, __fadd_rn(s.l, __fadd_rn(a.l, b.l)));
+}
+__device__ __forceinline__ DF df_add_f(DF a, float b) {
+  const DF s = df_two_sum(a.h, b);
+  return df_fast_two_sum(s.h, __fadd_rn(s.l, a.l));
+}
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+  const float p = __fmul_rn(a.h, b.h);
+  float e = __fmaf_rn(a.h, b.h, -p);  // the product's rounding error, exactly
+  e = __fmaf_rn(a.h, b.l, e);
+  e = __fmaf_rn(a.l, b.h, e);
+  return df_fast_two_sum(p, e);
+}
+// A double as a double-float (both parts computed in FP64, then rounded).
+__host__ __device__ constexpr DF df_const(double v) {
+  return DF{static_cast<float>(v), static_cast<float>(v - static_cast<double>(static_cast<float>(v)))};
+}
+
+// cos and sin of pos * inv_freq, as FP32 hi+lo pairs (absolute error about
+// 1e-11, far below a 16-bit ulp, so a rotation built from them stays one
+// rounding away from the exact value).  Only the angle and its reduction use
+// FP64, a handful of operations: phi = pos * inv_freq, q = nearest integer to
+// phi / (pi/2), x = phi - q*pi/2 with pi/2 split in two doubles and the
+// products fused (Cody and Waite's reduction), so |x| <= pi/4.  sin x and
+// cos x are then Taylor series (coefficients 1/n!) evaluated in double-float
+// FP32 arithmetic by Horner's rule: the terms up to x^5 (sin) and x^6 (cos)
+// in double-float, the smaller ones (below 4e-5 in size) in plain FP32; the
+// first omitted terms, x^15/15! and x^14/14!, are below 3e-14 for
+// |x| <= pi/4.  The quadrant q mod 4 then maps (sin x, cos x) to
+// (sin phi, cos phi).  (FP64 runs at a small fraction of the FP32 rate on
+// this GPU; a full FP64 sincos per angle was the store kernel's long pole.)
 __device__ __forceinline__ CosSin rope_cos_sin(int pos, double inv_freq) {
-  constexpr double kTwoPiHi = 6.283185307179586232;    // nearest double to 2*pi
-  constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
+  constexpr double kPio2Hi = 1.5707963267948966;     // nearest double to pi/2
+  constexpr double kPio2Lo = 6.123233995736766e-17;  // pi/2 - kPio2Hi
+  constexpr double k2OverPi = 0.6366197723675814;    // 2/pi
   const double phi = static_cast<double>(pos) * inv_freq;
-  const double k = rint(phi * 0.15915494309189535);    // 1 / (2*pi)
-  const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, phi));
-  double s, c;
-  sincos(r, &s, &c);
+  const double q = rint(phi * k2OverPi);
+  const double xd = fma(-q, kPio2Lo, fma(-q, kPio2Hi, phi));
+  const int quad = static_cast<int>(static_cast<long long>(q) & 3);
+  const float xh = static_cast<float>(xd);
+  const DF x{xh, static_cast<float>(xd - static_cast<double>(xh))};
+  const DF y = df_mul(x, x);  // x^2
+  // sin x = x (1 + y (-1/3! + y (1/5! + y Ts))), Ts = -1/7! + y/9! - y^2/11! + y^3/13!
+  const float ts = __fmaf_rn(__fmaf_rn(__fmaf_rn(y.h, 1.0f / 6227020800.0f, -1.0f / 39916800.0f), y.h,
+                                       1.0f / 362880.0f),
+                             y.h, -1.0f / 5040.0f);
+  const DF s3 = df_add_f(df_const(1.0 / 120.0), __fmul_rn(y.h, ts));
+  const DF s2 = df_add(df_const(-1.0 / 6.0), df_mul(y, s3));
+  const DF s1 = df_add(df_const(1.0), df_mul(y, s2));
+  const DF sx = df_mul(x, s1);
+  // cos x = 1 + y (-1/2! + y (1/4! + y (-1/6! + y Tc))), Tc = 1/8! - y/10! + y^2/12!
+  const float tc = __fmaf_rn(__fmaf_rn(y.h, 1.0f / 479001600.0f, -1.0f / 3628800.0f), y.h, 1.0f / 40320.0f);
+  const DF c4 = df_add_f(df_const(-1.0 / 720.0), __fmul_rn(y.h, tc));
+  const DF c3 = df_add(df_const(1.0 / 24.0), df_mul(y, c4));
+  const DF c2 = df_add(df_const(-0.5), df_mul(y, c3));
+  const DF cx = df_add(df_const(1.0), df_mul(y, c2));
+  // phi = x + quad * pi/2
+  DF c, s;
+  switch (quad) {
+    case 0: c = cx; s = sx; break;
+    case 1: c = DF{-sx.h, -sx.l}; s = cx; break;
+    case 2: c = DF{-cx.h, -cx.l}; s = DF{-sx.h, -sx.l}; break;
+    default: c = sx; s = DF{-cx.h, -cx.l}; break;
+  }
   CosSin v;
-  v.ch = static_cast<float>(c);
-  v.cl = static_cast<float>(c - static_cast<double>(v.ch));
-  v.sh = static_cast<float>(s);
-  v.sl = static_cast<float>(s - static_cast<double>(v.sh));
+  v.ch = c.h;
+  v.cl = c.l;
+  v.sh = s.h;
+  v.sl = s.l;
   return v;
 }
 
