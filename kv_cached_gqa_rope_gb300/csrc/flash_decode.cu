@@ -581,8 +581,8 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         return reinterpret_cast<uint16_t*>(base + (row * 128 + ((chunk ^ (row & 7)) << 4) + (cc & 7) * 2));
       };
       // cos/sin depend on the row's position only: the KV heads of one row
-      // are consecutive segments, so they are evaluated (in FP64, the costly
-      // part) once per row, not once per segment.
+      // are consecutive segments, so they are evaluated (the costly part)
+      // once per row, not once per segment.
       CosSin cs[NU];
       int cs_row = -1, t_first = 0;
       for (int k = 0; cur.more(); ++k) {

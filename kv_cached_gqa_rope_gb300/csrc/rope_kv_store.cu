@@ -9,15 +9,16 @@
 // where token (a, t) sits at position t of row cache_rows[a].
 //
 // Equal-length prefill: one CTA owns one position.  It evaluates the D/2
-// angles pos * theta^(-2i/D) once, in FP64, and keeps cos/sin as FP32 hi+lo
-// pairs in shared memory; the A tokens at that position then stream their
-// heads through 16-byte vector loads and stores.  Decode and the prefill of
-// prompts at offsets (one position per token): kTokenSplit CTAs share a token,
-// each owning a quarter of the frequencies of every head (and a quarter of its
-// V bytes), so that the FP64 angle work of a token is spread over four SMs;
-// each CTA issues its loads before it evaluates its angles.  The rotation is
-// evaluated with FP32 error-free products so that the BF16 result is within
-// one rounding of the exact value even where x cos - y sin cancels.
+// cos/sin of pos * theta^(-2i/D) once (rope_cos_sin: FP64 angle reduction,
+// double-float series) and keeps them as FP32 hi+lo pairs in shared memory;
+// the A tokens at that position then stream their heads through 16-byte
+// vector loads and stores.  Decode and the prefill of prompts at offsets (one
+// position per token): kTokenSplit CTAs share a token, each owning a quarter
+// of the frequencies of every head (and a quarter of its V bytes), so that
+// the angle work of a token is spread over four SMs; each CTA issues its
+// loads before it evaluates its angles.  The rotation is evaluated with FP32
+// error-free products so that the BF16 result is within one rounding of the
+// exact value even where x cos - y sin cancels.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
