@@ -191,14 +191,12 @@ __device__ void write_item_order(const RopeStoreParams& p) {
   for (int c = threadIdx.x; c < n; c += blockDim.x) p.item_order[atomicAdd(&bins[key(c)], 1)] = c;
 }
 
-// One token at its own position: decode (token a at positions[a], varlen = 0)
-// or the prefill of prompts at offsets (token t of prompt a at offsets[a] + t,
-// t < lengths[a], varlen = 1).  CTA part s of the token rotates the pairs of
-// frequencies [s*F, s*F + F) of every Q and K head, F = D/2 / kTokenSplit, and
-// copies part s of its V bytes.
-// The work of part `part` of token tk (decode: token tk = a; prompts at
-// offsets: token tk = a*T + t).  Returns early, uniformly over the CTA, for a
-// token with no work.
+// One token at its own position: decode (token tk = a at positions[a],
+// varlen = 0) or the prefill of prompts at offsets (token tk = a*T + t at
+// offsets[a] + t, t < lengths[a], varlen = 1).  Part s of the token (one CTA)
+// rotates the pairs of frequencies [s*F, s*F + F) of every Q and K head,
+// F = D/2 / kTokenSplit, and copies part s of its V bytes.  Returns early,
+// uniformly over the CTA, for a token with no work.
 template <int D, bool F16>
 __device__ __forceinline__ void token_body(const RopeStoreParams& p, int varlen, int tk, int part, CosSin* cs) {
   constexpr int HALF = D / 2;
