@@ -95,17 +95,24 @@ View check_tensor(const char* name, const kvgqa_tensor* t, int ndim, int32_t dty
   if (t->ndim != ndim) fail(KVGQA_EINVAL, "%s: expected rank %d, got %d", name, ndim, t->ndim);
   if (t->dtype != dtype)
     fail(KVGQA_EDTYPE, "%s: expected %s, got %s", name, dtype_name(dtype), dtype_name(t->dtype));
-  int64_t expect = 1;
   for (int i = ndim - 1; i >= 0; --i) {
     if (t->shape[i] < 0) fail(KVGQA_EINVAL, "%s: negative size in dim %d", name, i);
     if (t->strides[i] < 0) fail(KVGQA_ELAYOUT, "%s: negative stride in dim %d", name, i);
+  }
+  // the byte count, refused rather than wrapped when the sizes overflow 64
+  // bits (so no element count below can overflow either)
+  int64_t bytes = elem_size(dtype);
+  for (int i = 0; i < ndim; ++i)
+    if (__builtin_mul_overflow(bytes, t->shape[i], &bytes))
+      fail(KVGQA_EINVAL, "%s: sizes overflow a 64-bit byte count", name);
+  int64_t expect = 1;
+  for (int i = ndim - 1; i >= 0; --i) {
     if (t->shape[i] > 1 && t->strides[i] != expect)
       fail(KVGQA_ELAYOUT, "%s: not contiguous row-major (dim %d stride %lld, expected %lld)", name,
            i, (long long)t->strides[i], (long long)expect);
     expect *= t->shape[i];
   }
   View v{name, t};
-  const int64_t bytes = numel(*t) * elem_size(dtype);
   if (bytes == 0) return v;
   if (!t->data) fail(KVGQA_EINVAL, "%s: null data with %lld elements", name, (long long)numel(*t));
   if (t->bytes < bytes)

@@ -278,3 +278,19 @@ def test_decode_step_contract():
     assert code_of(kv.decode_step_out_, **a) == "EUNSUPPORTED"
     # every descriptor check passes: host tensors then fail the device check
     assert code_of(kv.decode_step_out_, **step_args()) in ("ECUDA", "EDEVICE")
+
+
+def test_overflowing_sizes_are_refused():
+    """A descriptor whose sizes overflow a 64-bit byte count is refused with
+    EINVAL before any byte range is computed from it (no wrap-around into a
+    small, seemingly valid range)."""
+    a = attention_args()
+    lib = kv.library()
+    ds = {name: kv.describe(t) for name, t in a.items() if isinstance(t, torch.Tensor)}
+    ds["positions"].shape[0] = 1 << 62            # 2^62 int32 values: 2^64 bytes
+    st = lib.cached_gqa_attention_out_(*[ctypes.byref(ds[n]) for n in ("q_rot", "k_cache", "v_cache", "positions",
+                                                                        "cache_rows")],
+                                       ctypes.c_float(0.125), ctypes.byref(ds["out"]), ctypes.byref(ds["workspace"]),
+                                       None)
+    assert kv.STATUS_NAMES[st] == "EINVAL"
+    assert b"overflow" in lib.kvgqa_last_error()
