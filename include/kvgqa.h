@@ -112,6 +112,9 @@ typedef enum kvgqa_status {
  * (a zero-filled workspace is ready); kvgqa_read_status() clears it. */
 #define KVGQA_STATUS_BYTES 256
 
+/* Version of this interface (the descriptor layout, the entry points and
+ * their arguments); a caller built against another version should not call
+ * in.  Never fails. */
 int kvgqa_abi_version(void);
 
 /* Message of the last failing call on this host thread ("" if none). */
