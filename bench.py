@@ -46,7 +46,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from kv_cached_gqa_rope_gb300 import workloads as W  # noqa: E402
+import workloads as W  # noqa: E402
 
 METRIC = "decode tokens/s + KV-cache HBM GB/s (% of peak); prefill TFLOP/s (% BF16 peak)"
 UNIT = "tokens/s"
@@ -105,6 +105,17 @@ def whole_job_rate(units_per_rank: float, seconds: float, world: int) -> float:
     units, so the job's rate is all ranks' units over the slowest rank's
     time (taken across ranks)."""
     return units_per_rank * world / max_over_ranks(seconds, world)
+
+
+def spread(ms, world: int):
+    """Median of per-step device times (ms), taken as the slowest rank's
+    median, and the distribution around it on this rank: the median is what
+    every rate here is computed from; p10/p90/mean/min show the spread."""
+    a = np.asarray(ms, dtype=np.float64)
+    med = max_over_ranks(float(np.median(a)), world)
+    return med, {"median_ms": round(med, 5), "p10_ms": round(float(np.percentile(a, 10)), 5),
+                 "p90_ms": round(float(np.percentile(a, 90)), 5), "mean_ms": round(float(a.mean()), 5),
+                 "min_ms": round(float(a.min()), 5), "n": int(a.size)}
 
 
 def peaks():
@@ -334,12 +345,14 @@ def run_ours(args, rank, world, local):
     else:
         step_ms = timed(two_call_body, host_us["store"] + host_us["attention"])
     barrier(world)
-    tokens_per_s = whole_job_rate(wl.A * K, float(sum(step_ms)) / 1e3, world)
-    total_ms = wl.A * K * world / tokens_per_s * 1e3  # the slowest rank's K steps
+    step_med_ms, step_spread = spread(step_ms, world)
+    tokens_per_s = whole_job_rate(wl.A, step_med_ms / 1e3, world)
+    total_ms = step_med_ms * K  # K steps at the slowest rank's median
     attn_bytes, step_bytes, fused_bytes = decode_bytes(wl, inp.positions.numpy())
     # (2) the attention call alone: the dominant kernel, for the roofline
     attn_ms = timed(attention_body, host_us["store"] + host_us["attention"])
-    attn_avg_s = max_over_ranks(float(np.mean(attn_ms)), world) / 1e3
+    attn_med_ms, attn_spread = spread(attn_ms, world)
+    attn_avg_s = attn_med_ms / 1e3
     achieved = attn_bytes / attn_avg_s / 1e9
     if args.only == "decode":
         flags = kv.kvgqa_read_status(ws1) | kv.kvgqa_read_status(ws2)
@@ -349,12 +362,12 @@ def run_ours(args, rank, world, local):
                 "ms_per_step": round(total_ms / K, 5), "attention_gbs": round(achieved, 1)} if rank == 0 else None
     # (3) the same step as the two public calls, and in one launch
     two_ms = timed(two_call_body, host_us["store"] + host_us["attention"])
-    two_avg_ms = max_over_ranks(float(np.mean(two_ms)), world)
+    two_avg_ms, two_spread = spread(two_ms, world)
     fused_ms = timed(single_body, host_us["single_launch_step"])
     flags = kv.kvgqa_read_status(ws1) | kv.kvgqa_read_status(ws2) | kv.kvgqa_read_status(ws3)
     if flags:
         raise RuntimeError(f"device status flags {flags} after the timed region")
-    fused_avg_ms = max_over_ranks(float(np.mean(fused_ms)), world)
+    fused_avg_ms, fused_spread = spread(fused_ms, world)
 
     # ---- FP16 storage: the same step and attention call on the same workload
     # held as IEEE binary16 (the caches converted; unused cells 65504)
@@ -379,8 +392,8 @@ def run_ours(args, rank, world, local):
         def attn16_body(e):
             store16(); e[0].record(stream); attend16(); e[1].record(stream)
 
-        s16 = max_over_ranks(float(np.mean(timed(step16_body, host_us["step"]))), world)
-        a16 = max_over_ranks(float(np.mean(timed(attn16_body, host_us["store"] + host_us["attention"]))), world) / 1e3
+        s16 = spread(timed(step16_body, host_us["step"]), world)[0]
+        a16 = spread(timed(attn16_body, host_us["store"] + host_us["attention"]), world)[0] / 1e3
         if any(kv.kvgqa_read_status(w) for w in ws16):
             raise RuntimeError("device status flags set in the FP16 decode")
         fp16 = {"decode": {"step": "decode_step_out_", "step_ms": round(s16, 5),
@@ -421,21 +434,22 @@ def run_ours(args, rank, world, local):
 
     for _ in range(3):
         e2e_step()
-    e2e_total = 0.0
+    e2e_ms = []
     barrier(world)
     for _ in range(K):
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_step()
-        e2e_total += time.perf_counter() - t0
-    e2e_value = whole_job_rate(wl.A * K, e2e_total, world)
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_med_ms, e2e_spread = spread(e2e_ms, world)
+    e2e_value = whole_job_rate(wl.A, e2e_med_ms / 1e3, world)
 
     # ---- the attention call on the other decode workloads of the same path
     decode_workloads = None
     if not args.no_decode_workloads:
         decode_workloads = [run_attention_workload(args, kv, w_, dev, stream, flush, world, hbm_peak)
-                            for w_ in (W.DIVERGENT_DECODE, W.LONG_DECODE)]
+                            for w_ in (W.DIVERGENT_DECODE, W.LONG_DECODE) + W.HEAD_SHAPE_DECODE]
 
     # ---- prefill: 16 prompts x 1024 tokens into empty rows
     prefill = None
@@ -469,12 +483,15 @@ def run_ours(args, rank, world, local):
                    "kv_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm_peak, 4),
                    "single_launch_step_ms": round(fused_avg_ms, 5),
                    "single_launch_tokens_per_s": round(wl.A * world / (fused_avg_ms / 1e3), 1),
-                   "single_launch_step_bytes": fused_bytes},
+                   "single_launch_step_bytes": fused_bytes,
+                   "spread": {"step": step_spread, "two_call_step": two_spread, "attention": attn_spread,
+                              "single_launch_step": fused_spread}},
         "roofline": {"kernel": "flash_decode_splitk_kernel (the cached_gqa_attention_out_ call; split-K with the combine run by the last CTA of each cut segment)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s"},
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "spread": e2e_spread},
         "gpu_launches": 2 * K,  # rope_kv_store_kernel + flash_decode_splitk_kernel per step
         "host_us_per_call": host_us,
         "clocks": clocks,
@@ -522,12 +539,14 @@ def run_attention_workload(args, kv, wl, dev, stream, flush, world, hbm_peak):
     torch.cuda.synchronize()
     if kv.kvgqa_read_status(ws1) or kv.kvgqa_read_status(ws2):
         raise RuntimeError(f"device status flags set ({wl.name})")
-    avg_s = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world) / 1e3
+    med_ms, sp = spread([a.elapsed_time(b) for a, b in ev], world)
+    avg_s = med_ms / 1e3
     attn_bytes = decode_bytes(wl, inp.positions.numpy())[0]
     gbs = attn_bytes / avg_s / 1e9
-    return {"workload": wl.name, "attention_ms": round(avg_s * 1e3, 5), "attention_bytes": attn_bytes,
+    return {"workload": wl.name, "H_q": wl.H_q, "H_kv": wl.H_kv, "head_dim": wl.D,
+            "attention_ms": round(avg_s * 1e3, 5), "attention_bytes": attn_bytes,
             "kv_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
-            "tokens_per_s": round(wl.A * world / avg_s, 1)}
+            "tokens_per_s": round(wl.A * world / avg_s, 1), "spread": sp}
 
 
 def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src, f16=False):
@@ -559,8 +578,7 @@ def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_
         call()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
-    ms = [a.elapsed_time(b) for a, b in ev]
-    avg = max_over_ranks(float(np.mean(ms)), world)
+    avg, sp = spread([a.elapsed_time(b) for a, b in ev], world)
     flops = prefill_flops(pw)
     tflops = flops / (avg / 1e3) / 1e12
     if kv.kvgqa_read_status(ws):
@@ -569,7 +587,8 @@ def run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_
             "tflops": round(tflops, 1), "frac_of_bf16_peak": round(tflops / bf16_peak, 4),
             "peak": bf16_peak,
             "peak_source": f"{peak_src} burst bf16_tflops" + (" (FP16 dense rate = BF16 rate, nominal ratio 1)" if f16 else ""),
-            "note": "whole call: RoPE + store of all prompts, then causal attention", "gpu_launches": 2 * K}
+            "note": "whole call: RoPE + store of all prompts, then causal attention", "gpu_launches": 2 * K,
+            "spread": sp}
 
 
 def varlen_flops(wl, offsets, lengths):
@@ -610,7 +629,7 @@ def run_prefill_varlen(args, kv, dev, stream, flush, world, bf16_peak, peak_src)
     torch.cuda.synchronize()
     if kv.kvgqa_read_status(ws):
         raise RuntimeError("device status flags set in the chunked prefill")
-    avg = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world)
+    avg, sp = spread([a.elapsed_time(b) for a, b in ev], world)
     flops = varlen_flops(pw, offs, lens)
     tflops = flops / (avg / 1e3) / 1e12
     return {"workload": pw.name + "_chunks_len_u1_1024_off_u", "tokens": int(sum(lens)),
@@ -618,7 +637,7 @@ def run_prefill_varlen(args, kv, dev, stream, flush, world, bf16_peak, peak_src)
             "frac_of_bf16_peak": round(tflops / bf16_peak, 4), "peak": bf16_peak,
             "peak_source": f"{peak_src} burst bf16_tflops",
             "note": "whole call: RoPE + store of every prompt's tokens at its offset, then attention over the row "
-                    "prefix and the prompt", "gpu_launches": 2 * K}
+                    "prefix and the prompt", "gpu_launches": 2 * K, "spread": sp}
 
 
 # ---------------------------------------------------------------------- CPU oracle

@@ -157,7 +157,10 @@ kvgqa_status rope_kv_store_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
  * status block, one int32 counter per (row, KV head) and the FP32 split-K
  * partials (it depends on the device's SM count, not on max_seq or the
  * positions).  The counters must be zero before the first call (a zero-filled
- * workspace is ready); every call leaves them at zero. */
+ * workspace is ready); every call that completes leaves them at zero.  A call
+ * that gave up on a bounded wait (KVGQA_FLAG_TIMEOUT) may leave some short of
+ * their count: kvgqa_read_status() then zero-fills the workspace, which makes
+ * it ready again. */
 kvgqa_status cached_gqa_attention_workspace_size(int64_t A, int64_t H_q, int64_t H_kv,
                                                  int64_t D, int32_t device, size_t* bytes);
 
@@ -218,7 +221,8 @@ kvgqa_status decode_step_workspace_size(int64_t A, int64_t H_q, int64_t H_kv, in
  *   out [A,H_q,D] bf16 (written; rows with invalid metadata are left
  *     unwritten, their cells untouched, and a status bit is set)
  *   workspace  >= decode_step_workspace_size(...) bytes, 256-byte aligned,
- *     counters zero before the first call (left zero by every call)
+ *     counters zero before the first call (left zero by every call that
+ *     completes; after KVGQA_FLAG_TIMEOUT, kvgqa_read_status() re-zeroes)
  * Limits as cached_gqa_attention_out_.  cache_rows must be distinct.  A = 0
  * is a no-op.  There is no q_out: callers that need the rotated queries use
  * the two-call path.
@@ -260,13 +264,14 @@ kvgqa_status decode_step_single_launch_out_(const kvgqa_tensor* q, const kvgqa_t
  * The first call on a device looks up the device address of that array (once
  * per device, with that device current); make that first call before any
  * stream capture.  Sizes whose partials do not fit the array are rejected
- * with KVGQA_EUNSUPPORTED.  Every call shares the one array: it overwrites the
- * partials of the previous call before reading them, and the per-row counters
- * it keeps there start at zero when the library loads and are left at zero by
- * every call; calls whose kernels overlap on the GPU (different streams, or
- * different host threads) race on it.  Device-side range checks still skip
- * rows with invalid positions or cache rows, but this variant has no status
- * word for the caller to read.
+ * with KVGQA_EUNSUPPORTED.  Every call shares the one array: before its kernel
+ * each call clears the array's status word and per-row counters with
+ * cudaMemsetAsync on `stream` (which allocates nothing), so no call depends on
+ * what an earlier one left, not even one that gave up on a bounded wait; the
+ * kernel then overwrites the partials before reading them.  Calls whose work
+ * overlaps on the GPU (different streams, or different host threads) race on
+ * the array.  Device-side range checks still skip rows with invalid positions
+ * or cache rows, but this variant has no status word for the caller to read.
  */
 #define KVGQA_STATIC_SCRATCH_BYTES (4u << 20)
 kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
@@ -395,7 +400,10 @@ kvgqa_status kvgqa_metadata_upload(const int32_t* host_meta, int32_t capacity, c
 
 /* Opt-in: synchronise `stream`, return the status word of `workspace` in
  * *flags (KVGQA_FLAG_* bits; 0 = every device-side check passed) and clear it.
- * This is the only call that waits for the device. */
+ * When KVGQA_FLAG_TIMEOUT is among them, the whole workspace is zero-filled
+ * (a call that gave up on a wait may have left split-K counters short of
+ * their count), so it is ready for any call again.  This is the only call
+ * that waits for the device. */
 kvgqa_status kvgqa_read_status(const kvgqa_tensor* workspace, void* stream, int32_t* flags);
 
 /* Diagnostic: check on the device that the library's waits end.  Launches on

@@ -75,6 +75,16 @@ const char* dtype_name(int32_t dtype) {
   return "unknown";
 }
 
+// Whether the product of the sizes is below `limit`, computed without
+// overflow (a product that overflows is not below any limit).  Negative sizes
+// are refused later by check_tensor.
+bool product_below(std::initializer_list<int64_t> sizes, int64_t limit) {
+  int64_t p = 1;
+  for (int64_t x : sizes)
+    if (__builtin_mul_overflow(p, x, &p)) return false;
+  return p < limit;
+}
+
 int64_t numel(const kvgqa_tensor& t) {
   int64_t n = 1;
   for (int i = 0; i < t.ndim; ++i) n *= t.shape[i];
@@ -101,8 +111,11 @@ View check_tensor(const char* name, const kvgqa_tensor* t, int ndim, int32_t dty
   }
   // the byte count, refused rather than wrapped when the sizes overflow 64
   // bits (so no element count below can overflow either)
-  int64_t bytes = elem_size(dtype);
-  for (int i = 0; i < ndim; ++i)
+  // (a tensor with a zero-sized dimension is empty whatever its other sizes)
+  bool empty = false;
+  for (int i = 0; i < ndim; ++i) empty |= t->shape[i] == 0;
+  int64_t bytes = empty ? 0 : elem_size(dtype);
+  for (int i = 0; i < ndim && !empty; ++i)
     if (__builtin_mul_overflow(bytes, t->shape[i], &bytes))
       fail(KVGQA_EINVAL, "%s: sizes overflow a 64-bit byte count", name);
   int64_t expect = 1;
@@ -323,7 +336,7 @@ kvgqa_status cached_gqa_attention_out_(const kvgqa_tensor* q_rot, const kvgqa_te
     const int G = (int)(H_q / H_kv);
     if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
-    if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
+    if (!product_below({A, H_kv, max_seq}, 1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
     const int32_t elem = storage_type(q_rot, "q_rot");
     View vq = check_tensor("q_rot", q_rot, 3, elem, 16);
     View vkc = check_tensor("k_cache", k_cache, 4, elem, 16);
@@ -381,6 +394,7 @@ kvgqa_status decode_step_workspace_size(int64_t A, int64_t H_q, int64_t H_kv, in
     check_heads(H_q, H_kv);
     const int G = (int)(H_q / H_kv);
     if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
+    if (!product_below({A, H_q, D, 4}, 1ll << 62)) fail(KVGQA_EINVAL, "sizes overflow a 64-bit byte count");
     kvgqa::DecodeLayout lay;
     check_cuda(kvgqa::decode_layout(device, (int)D, kvgqa::decode_group_pad(G), A, H_kv, &lay),
                "decode kernel set-up");
@@ -407,7 +421,7 @@ void decode_step_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_
     const int G = (int)(H_q / H_kv);
     if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
-    if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
+    if (!product_below({A, H_kv, max_seq}, 1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
     const int32_t elem = storage_type(q, "q");
     View vq = check_tensor("q", q, 3, elem, 16);
     View vk = check_tensor("k", k, 3, elem, 16);
@@ -533,7 +547,7 @@ kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
     const int G = (int)(H_q / H_kv);
     if (G > 16) fail(KVGQA_EUNSUPPORTED, "group size %d: decode kernels cover G <= 16", G);
     if (A > kvgqa::kMaxActiveRows) fail(KVGQA_EUNSUPPORTED, "A=%lld exceeds %d active rows", (long long)A, kvgqa::kMaxActiveRows);
-    if (A * H_kv * max_seq >= (1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
+    if (!product_below({A, H_kv, max_seq}, 1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*H_kv*max_seq must stay below 2^31");
     const int32_t elem = storage_type(q_rot, "q_rot");
     View vq = check_tensor("q_rot", q_rot, 3, elem, 16);
     View vkc = check_tensor("k_cache", k_cache, 4, elem, 16);
@@ -558,6 +572,11 @@ kvgqa_status cached_gqa_attention_static_scratch_out_(const kvgqa_tensor* q_rot,
     void* scratch = nullptr;
     check_cuda(kvgqa::static_scratch_address(dev, &scratch), "static scratch address");
     if (A == 0) return;
+    // The status word and the per-(row, KV head) counters start every call at
+    // zero: a call whose bounded wait gave up leaves counters it never
+    // completed, and this variant has no status word for the caller to see it.
+    check_cuda(cudaMemsetAsync(scratch, 0, KVGQA_STATUS_BYTES + lay.counter_bytes, static_cast<cudaStream_t>(stream)),
+               "static scratch clear");
     kvgqa::DecodeParams p{};
     p.q = static_cast<const uint16_t*>(q_rot->data);
     p.k_cache = static_cast<const uint16_t*>(k_cache->data);
@@ -585,6 +604,7 @@ kvgqa_status prefill_gqa_cached_rows_workspace_size(int64_t A, int64_t T, int64_
     if (A < 0 || T < 0) fail(KVGQA_EINVAL, "negative size");
     check_head_dim(D);
     check_heads(H_q, H_kv);
+    if (!product_below({A, T, H_q, D, 4}, 1ll << 62)) fail(KVGQA_EINVAL, "sizes overflow a 64-bit byte count");
     *bytes = prefill_workspace_bytes(A, T, H_q, D);
   });
 }
@@ -609,7 +629,7 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
   check_theta(theta);
   if (!std::isfinite(scale)) fail(KVGQA_EINVAL, "scale must be finite");
   if (T > max_seq) fail(KVGQA_EINVAL, "T=%lld exceeds max_seq=%lld", (long long)T, (long long)max_seq);
-  if (A * T > 0x7fffffffll) fail(KVGQA_EUNSUPPORTED, "A*T must stay below 2^31");
+  if (!product_below({A, T}, 1ll << 31)) fail(KVGQA_EUNSUPPORTED, "A*T must stay below 2^31");
   const int32_t elem = storage_type(q, "q");
   View vq = check_tensor("q", q, 4, elem, 16);
   View vk = check_tensor("k", k, 4, elem, 16);
@@ -801,6 +821,12 @@ kvgqa_status kvgqa_read_status(const kvgqa_tensor* workspace, void* stream, int3
     check_cuda(cudaMemcpyAsync(&h, workspace->data, sizeof h, cudaMemcpyDeviceToHost, st), "status read");
     check_cuda(cudaMemsetAsync(workspace->data, 0, sizeof h, st), "status clear");
     check_cuda(cudaStreamSynchronize(st), "stream synchronize");
+    if (h & KVGQA_FLAG_TIMEOUT) {
+      // A call that gave up on a wait may have left split-K counters short of
+      // their count; a zero-filled workspace is ready for any call again.
+      check_cuda(cudaMemsetAsync(workspace->data, 0, static_cast<size_t>(workspace->shape[0]), st), "workspace clear");
+      check_cuda(cudaStreamSynchronize(st), "stream synchronize");
+    }
     *flags = h;
   });
 }

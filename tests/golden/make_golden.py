@@ -26,7 +26,7 @@ ROOT = os.path.dirname(os.path.dirname(HERE))
 sys.path.insert(0, ROOT)
 
 import oracle  # noqa: E402
-from kv_cached_gqa_rope_gb300 import workloads as W  # noqa: E402
+import workloads as W  # noqa: E402
 
 
 def hexs(a) -> str:

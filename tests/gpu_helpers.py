@@ -9,7 +9,7 @@ import numpy as np
 import torch
 
 import oracle
-from kv_cached_gqa_rope_gb300 import workloads as W
+import workloads as W
 
 # Attention output tolerances versus the FP64 oracle: max-abs and RMS as the
 # acceptance bar states them, plus relative RMS.  The GPU result is rounded to

@@ -382,6 +382,41 @@ def check_prefill_select_matches_full(o):
         assert np.allclose(part[a, t, h], full[a, t, h], rtol=0, atol=1e-14)
 
 
+def check_varlen_select_matches_full(o):
+    """The per-output path of the chunked prefill (``select``) gives the values
+    of the whole-prompt path for prompts at nonzero offsets and of different
+    lengths; an output past its prompt's length stays NaN in both."""
+    A, T, H_q, H_kv, D, S, L = 3, 6, 4, 2, 8, 5, 14
+    q, k, v, _, _ = _prefill_case(A, T, H_q, H_kv, D, S, L, seed=110)
+    kc = random_bf16_bits((S, H_kv, L, D), seed=111)
+    vc = random_bf16_bits((S, H_kv, L, D), seed=112)
+    rows, offs, lens = np.array([3, 0, 4]), np.array([0, 5, 8]), np.array([6, 2, 4])
+    _, full, kc1, vc1 = o.prefill_varlen_gqa_cached_rows(q, k, v, offs, lens, rows, 16.0, 0.4, kc, vc)
+    sel = [(a, t, h) for a in range(A) for t in range(T) for h in range(H_q)]
+    _, part, kc2, vc2 = o.prefill_varlen_gqa_cached_rows(q, k, v, offs, lens, rows, 16.0, 0.4, kc, vc, select=sel)
+    assert np.array_equal(kc1, kc2) and np.array_equal(vc1, vc2)
+    assert np.array_equal(np.isnan(part), np.isnan(full))
+    seen = ~np.isnan(full)
+    assert seen.sum() == int(np.sum(lens)) * H_q * D
+    assert np.allclose(part[seen], full[seen], rtol=0, atol=1e-13)
+
+
+def check_decode_heads_matches_full(o):
+    """Attention of listed (token, head) pairs (``heads``) equals those entries
+    of the call over every pair; the unlisted entries stay NaN."""
+    kc, vc = _tiny_cache(S=3, H_kv=2, L=9, D=8, seed=120)
+    q = random_bf16_bits((3, 4, 8), seed=121)
+    pos, rows = np.array([8, 0, 4]), np.array([2, 0, 1])
+    full = o.cached_gqa_attention(q, kc, vc, pos, rows, 0.3)
+    heads = [(2, 3), (0, 1), (1, 0), (0, 2)]
+    part = o.cached_gqa_attention(q, kc, vc, pos, rows, 0.3, heads=heads)
+    listed = np.zeros((3, 4), dtype=bool)
+    for a, h in heads:
+        listed[a, h] = True
+        assert np.array_equal(part[a, h], full[a, h])
+    assert np.all(np.isnan(part[~listed]))
+
+
 def check_varlen_equal_lengths_is_prefill(o):
     """Zero offsets and full lengths: the equal-length prefill."""
     q, k, v, kc, vc = _prefill_case(seed=70)
@@ -447,5 +482,5 @@ ALL_CHECKS = [
     check_brute_force_tiny, check_gqa_equals_repeated_mha, check_prefix_is_inclusive_and_bounded,
     check_prefill_rows_and_first_position, check_prefill_causal, check_prefill_matches_decode,
     check_prefill_select_matches_full, check_varlen_equal_lengths_is_prefill, check_varlen_length_one_is_decode,
-    check_varlen_chunks_compose,
+    check_varlen_chunks_compose, check_varlen_select_matches_full, check_decode_heads_matches_full,
 ]

@@ -16,7 +16,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
-from kv_cached_gqa_rope_gb300 import workloads as W  # noqa: E402
+import workloads as W  # noqa: E402
 
 BF16 = 2  # bytes per stored element
 

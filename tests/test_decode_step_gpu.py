@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from kv_cached_gqa_rope_gb300 import workloads as W
+import workloads as W
 from gpu_helpers import DecodeRun, assert_attention_close, assert_ulp, bits, oracle_attention, whole_step
 
 pytestmark = pytest.mark.gpu

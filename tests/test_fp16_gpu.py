@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from kv_cached_gqa_rope_gb300 import workloads as W
+import workloads as W
 from gpu_helpers import DecodeRun, assert_attention_close, whole_step
 
 pytestmark = pytest.mark.gpu

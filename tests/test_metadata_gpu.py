@@ -1,10 +1,17 @@
 """Decode steps driven by the host slot table: one [3, capacity] host-to-device
-copy per step, positions and cache_rows as zero-copy views of the device copy;
-the results equal the same calls on separately built metadata tensors."""
+copy per step, positions and cache_rows as zero-copy views of the device copy.
+Each step's metadata is checked against hand-derived values (lowest free row
+on admission, position = the row's length), its results against the FP64
+oracle run on the same metadata with its own cache state carried from step to
+step, and against the same calls on separately built metadata tensors."""
+import numpy as np
 import pytest
 import torch
 
 import kv_cached_gqa_rope_gb300 as kv
+import oracle
+import workloads as W
+from gpu_helpers import assert_attention_close, bits
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +38,12 @@ def test_slot_table_driven_steps_match_explicit_metadata():
     ws_a = kv.new_workspace(kv.cached_gqa_attention_workspace_size(S, H_q, H_kv, D))
     scale, theta = D ** -0.5, 10000.0
     order = [[103, 100, 102, 101], [101, 103, 100], [104, 100, 103]]
+    # rows: 100..103 take the lowest free rows 0..3 in admission order, 104
+    # (admitted before step 2, no row released yet) row 4; positions: each
+    # row's length, which every step advances by one
+    want_pos = [[61, 10, 0, 40], [41, 62, 11], [5, 12, 63]]
+    want_rows = [[3, 0, 2, 1], [1, 3, 0], [4, 0, 3]]
+    kc_o, vc_o = bits(kc0), bits(vc0)   # the oracle's own cache state
     for step, reqs in enumerate(order):
         if step == 2:
             table.admit(104, 5)                       # admission at a step boundary
@@ -38,10 +51,22 @@ def test_slot_table_driven_steps_match_explicit_metadata():
         tokens, positions, rows = meta.upload(A)
         torch.cuda.synchronize()
         assert positions.data_ptr() == meta.device[1].data_ptr()   # views, no copies
+        assert meta.host[0, :A].tolist() == [7] * A
+        assert meta.host[1, :A].tolist() == want_pos[step]
+        assert meta.host[2, :A].tolist() == want_rows[step]
         q, k, v = make_step_inputs(A, H_q, H_kv, D, seed=step)
         q_rot_a, out_a = torch.empty_like(q), torch.empty_like(q)
         kv.rope_kv_store_out_(q, k, v, positions, rows, theta, q_rot_a, kc_a, vc_a, ws_s)
         kv.cached_gqa_attention_out_(q_rot_a, kc_a, vc_a, positions, rows, scale, out_a, ws_a)
+        # the oracle on the same step: store, then attention over each row's prefix
+        pos_h, rows_h = np.array(want_pos[step]), np.array(want_rows[step])
+        q_rot_o, kc_o, vc_o = oracle.rope_kv_store(bits(q), bits(k), bits(v), pos_h, rows_h, theta, kc_o, vc_o)
+        ref = oracle.cached_gqa_attention(q_rot_o, kc_o, vc_o, pos_h, rows_h, scale)
+        torch.cuda.synchronize()
+        assert oracle.ulp_distance_bf16(bits(q_rot_a), q_rot_o).max() <= 1
+        assert oracle.ulp_distance_bf16(bits(kc_a), kc_o).max() <= 1, "K cache beyond 1 ulp of the oracle"
+        assert np.array_equal(bits(vc_a), vc_o), "V cache differs from the oracle"
+        assert_attention_close(out_a.cpu(), ref, f"slot-table step {step}")
         # the same step on explicitly built device tensors
         pos_b = torch.tensor(meta.host[1, :A].tolist(), dtype=torch.int32, device="cuda")
         rows_b = torch.tensor(meta.host[2, :A].tolist(), dtype=torch.int32, device="cuda")

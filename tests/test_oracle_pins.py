@@ -4,6 +4,7 @@ must be caught by at least one of those checks."""
 import importlib.util
 import math
 import os
+import types
 
 import numpy as np
 import pytest
@@ -20,10 +21,20 @@ def test_oracle_pin(check):
     check(oracle.kvgqa_oracle)
 
 
-def fresh_oracle():
-    spec = importlib.util.spec_from_file_location("kvgqa_oracle_mutant", ORACLE_SRC)
-    mod = importlib.util.module_from_spec(spec)
-    spec.loader.exec_module(mod)
+def fresh_oracle(patch=None):
+    """A private copy of the oracle module; ``patch`` = (old, new) replaces one
+    source fragment (it must occur exactly once) before the copy is loaded, to
+    plant a mistake inside a function rather than around it."""
+    if patch is None:
+        spec = importlib.util.spec_from_file_location("kvgqa_oracle_mutant", ORACLE_SRC)
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        return mod
+    src = open(ORACLE_SRC).read()
+    old, new = patch
+    assert src.count(old) == 1, f"patch target not unique: {old!r}"
+    mod = types.ModuleType("kvgqa_oracle_mutant")
+    exec(compile(src.replace(old, new), ORACLE_SRC, "exec"), mod.__dict__)
     return mod
 
 
@@ -189,14 +200,42 @@ MUTANTS = [mutant_rope_direction, mutant_rope_interleaved, mutant_rope_frequency
            mutant_f16_read_as_bf16]
 
 
-@pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
-def test_planted_mistake_is_caught(mutate):
-    m = fresh_oracle()
-    mutate(m)
+# Mistakes planted inside a branch of a function (source fragment -> its
+# broken form), for branches that no function-level replacement reaches.
+SOURCE_MUTANTS = {
+    # the per-output chunked prefill drops the prompt's position offset
+    "varlen_select_drops_offset": ("p = int(off[a]) + t", "p = t"),
+    # the per-output equal-length prefill stops one key early
+    "prefill_select_exclusive": ("vc[rows[a], g, :T], t, scale, fmt)", "vc[rows[a], g, :T], max(t - 1, 0), scale, fmt)"),
+    # the listed (token, head) pairs read transposed
+    "decode_heads_transposed": ("if heads is None else heads", "if heads is None else [(h, a) for a, h in heads]"),
+}
+
+
+def caught_by(m):
     caught = []
     for check in pins.ALL_CHECKS:
         try:
             check(m)
         except Exception:  # an assertion, or a crash of the broken copy
             caught.append(check.__name__)
-    assert caught, f"no pin catches {mutate.__name__}"
+    return caught
+
+
+@pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
+def test_planted_mistake_is_caught(mutate):
+    m = fresh_oracle()
+    mutate(m)
+    assert caught_by(m), f"no pin catches {mutate.__name__}"
+
+
+@pytest.mark.parametrize("name", sorted(SOURCE_MUTANTS))
+def test_planted_branch_mistake_is_caught(name):
+    m = fresh_oracle(SOURCE_MUTANTS[name])
+    assert caught_by(m), f"no pin catches {name}"
+
+
+def test_unpatched_copy_passes_every_pin():
+    """The patching loader itself changes nothing: an identity patch passes."""
+    m = fresh_oracle(("p = int(off[a]) + t", "p = int(off[a]) + t"))
+    assert caught_by(m) == []

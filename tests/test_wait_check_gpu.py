@@ -10,7 +10,7 @@ import torch
 
 import kv_cached_gqa_rope_gb300 as kv
 import oracle
-from kv_cached_gqa_rope_gb300 import workloads as W
+import workloads as W
 from gpu_helpers import DecodeRun, assert_attention_close, oracle_attention
 
 pytestmark = pytest.mark.gpu
@@ -47,3 +47,26 @@ def test_wait_check_rejects_host_workspace():
     with pytest.raises(kv.KvgqaError) as e:
         kv.kvgqa_check_bounded_wait(raw[off:off + 256])
     assert e.value.code == "EDEVICE"
+
+
+def test_timeout_status_read_restores_the_workspace():
+    """A decode call whose bounded wait gave up leaves the status word with
+    KVGQA_FLAG_TIMEOUT and may leave split-K counters short of their count.
+    That state is made on the host here (a set timeout bit and non-zero
+    counters written into the workspace): reading the status returns the
+    flag and zero-fills the workspace, after which an attention call on it
+    matches the oracle."""
+    inp = W.make_decode_inputs(W.LLAMA_DECODE, include_current=True)
+    run = DecodeRun(inp)
+    ws = run.ws_attn
+    wl = inp.wl
+    counters = ws[kv.STATUS_BYTES:kv.STATUS_BYTES + 4 * wl.A * wl.H_kv].view(torch.int32)
+    counters.fill_(1)
+    ws[:4].view(torch.int32).fill_(kv.FLAG_TIMEOUT)
+    assert kv.kvgqa_read_status(ws) == kv.FLAG_TIMEOUT
+    assert int(ws.count_nonzero()) == 0, "workspace not zero-filled after a timeout was read"
+    run.attention()
+    torch.cuda.synchronize()
+    rows = list(range(wl.A))
+    assert_attention_close(run.out.cpu(), oracle_attention(inp, rows), "attention after the workspace was restored")
+    assert kv.kvgqa_read_status(ws) == 0

@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 import torch
 
-from kv_cached_gqa_rope_gb300 import workloads as W
+import workloads as W
 from gpu_helpers import DecodeRun, assert_attention_close, oracle_attention
 
 pytestmark = pytest.mark.gpu
@@ -51,12 +51,38 @@ def test_static_scratch_matches_workspace_entry(wl):
     assert_attention_close(got.cpu()[rows], oracle_attention(inp, rows), "static scratch vs oracle")
 
 
-def test_static_scratch_rejects_oversize():
+def _zeros(*shape, dtype=torch.bfloat16):
+    return torch.zeros(*shape, dtype=dtype, device="cuda")
+
+
+def test_static_scratch_rejects_too_many_rows():
+    """More active rows than the decode kernels take: refused before the
+    scratch is considered."""
     import kv_cached_gqa_rope_gb300 as kv
-    wl = W.scaled_decode(W.TINY_DECODE, A=3000, slots=3000, max_seq=4)   # beyond the active-row limit
-    q = torch.zeros(wl.A, wl.H_q, wl.D, dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros(wl.slots, wl.H_kv, wl.max_seq, wl.D, dtype=torch.bfloat16, device="cuda")
-    pos = torch.zeros(wl.A, dtype=torch.int32, device="cuda")
+    wl = W.scaled_decode(W.TINY_DECODE, A=3000, slots=3000, max_seq=4)
+    q = _zeros(wl.A, wl.H_q, wl.D)
+    kc = _zeros(wl.slots, wl.H_kv, wl.max_seq, wl.D)
+    pos = _zeros(wl.A, dtype=torch.int32)
     with pytest.raises(kv.KvgqaError) as e:
         kv.cached_gqa_attention_static_scratch_out_(q, kc, kc.clone(), pos, pos.clone(), 0.1, q.clone())
     assert e.value.code == "EUNSUPPORTED"
+    assert "active rows" in str(e.value)
+
+
+def test_static_scratch_rejects_oversize():
+    """A legal shape inside the row limit whose counters and partials do not
+    fit the 4 MiB static array: 1024 rows x 1024 KV heads need 4 MiB of
+    counters alone.  Refused with a message naming the static scratch, and
+    nothing is launched (the output keeps its bytes)."""
+    import kv_cached_gqa_rope_gb300 as kv
+    A, H, D = 1024, 1024, 64
+    q = _zeros(A, H, D)
+    kc = _zeros(1, H, 1, D)
+    pos = _zeros(A, dtype=torch.int32)
+    out = torch.full((A, H, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kv.KvgqaError) as e:
+        kv.cached_gqa_attention_static_scratch_out_(q, kc, kc.clone(), pos, pos.clone(), 0.125, out)
+    assert e.value.code == "EUNSUPPORTED"
+    assert "static scratch" in str(e.value)
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())

@@ -104,6 +104,14 @@ PREFILL = PrefillWorkload(
     max_seq=2048, A=16, T=1024, H_q=32, H_kv=8, D=128, theta=500000.0)
 
 DECODE_WORKLOADS = (TINY_DECODE, LLAMA_DECODE, DIVERGENT_DECODE, LONG_DECODE)
+
+# The Llama-style decode workload (same seed: same slots, positions and draws)
+# with the other head shapes the kernels take: head width 64, and one query
+# head per KV head (multi-head attention, G = 1) at widths 128 and 64.
+HEAD_SHAPE_DECODE = tuple(
+    DecodeWorkload(name=f"llama_decode_s64_ms4096_a32_hq{hq}_hkv8_d{d}", index=1, slots=64, max_seq=4096, A=32,
+                   H_q=hq, H_kv=8, D=d, theta=500000.0, positions="uniform", pos_lo=1, pos_hi=4096)
+    for hq, d in ((32, 64), (8, 128), (8, 64)))
 ALL_WORKLOADS = DECODE_WORKLOADS + (PREFILL,)
 
 
