@@ -16,7 +16,31 @@ import workloads as W
 # BF16 once (relative error <= 2^-9, RMS about 2^-9/sqrt(3) of the value) and
 # accumulates in FP32 over at most 65536 keys (relative error well below
 # 1e-5), so a relative RMS above 5e-3 means a real defect.
+#
+# The output is stored in a 16-bit format, whose grid is coarser than the
+# 1e-2 max-abs bar for large values: a BF16 value in [2, 4) has neighbours
+# 2^-6 = 0.0156 apart, in [4, 8) 0.031 apart, so even the exact result,
+# rounded once to BF16 as the method prescribes, can be 0.0156 away from the
+# FP64 value.  There the bar is one unit in the last place of the format at
+# the oracle's value: the GPU value must be one of the two grid points around
+# the exact value (a faithful rounding).  Below |out| = 2 (BF16) the grid is
+# finer than 1e-2 and the 1e-2 bar holds as stated.
 MAX_ABS, RMS, REL_RMS = 1e-2, 2e-3, 5e-3
+
+
+def grid_spacing(ref: np.ndarray, fmt: str = "bf16") -> np.ndarray:
+    """Distance between neighbouring values of the storage format at |ref|
+    (normal range): 2^(e - 7) for BF16 and 2^(e - 10) for binary16, where
+    2^e <= |ref| < 2^(e+1)."""
+    frac_bits = {"bf16": 7, "f16": 10}[fmt]
+    _, e = np.frexp(np.abs(ref))              # |ref| = m * 2^e, m in [0.5, 1)
+    return np.ldexp(1.0, e - 1 - frac_bits)
+
+
+def max_abs_bound(ref: np.ndarray, fmt: str = "bf16") -> np.ndarray:
+    """Per-element max-abs bar: 1e-2, or one grid step of the output format
+    where that step is larger."""
+    return np.maximum(MAX_ABS, grid_spacing(ref, fmt))
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -28,7 +52,9 @@ def assert_ulp(gpu_bf16: torch.Tensor, oracle_bits: np.ndarray, what: str, max_u
     assert d.max() <= max_ulp, f"{what}: {int((d > max_ulp).sum())} values beyond {max_ulp} ulp (max {int(d.max())})"
 
 
-def attention_errors(gpu_bf16: torch.Tensor, ref: np.ndarray, mask=None):
+def attention_errors(gpu_bf16: torch.Tensor, ref: np.ndarray, mask=None, fmt: str = "bf16"):
+    """(max-abs error, RMS error, relative RMS, largest error / its element's
+    max-abs bar) of a 16-bit GPU output against the FP64 oracle."""
     g = gpu_bf16.detach().float().cpu().numpy().astype(np.float64)
     if mask is not None:
         g, ref = g[mask], ref[mask]
@@ -36,13 +62,14 @@ def attention_errors(gpu_bf16: torch.Tensor, ref: np.ndarray, mask=None):
     err = g - ref
     rms_ref = math.sqrt(float(np.mean(ref * ref)))
     rms = math.sqrt(float(np.mean(err * err)))
-    return float(np.max(np.abs(err))), rms, rms / rms_ref
+    worst = float(np.max(np.abs(err) / max_abs_bound(ref, fmt)))
+    return float(np.max(np.abs(err))), rms, rms / rms_ref, worst
 
 
-def assert_attention_close(gpu_bf16, ref, what, mask=None):
-    mx, rms, rel = attention_errors(gpu_bf16, ref, mask)
-    assert mx <= MAX_ABS and rms <= RMS and rel <= REL_RMS, \
-        f"{what}: max-abs {mx:.3e} rms {rms:.3e} rel-rms {rel:.3e}"
+def assert_attention_close(gpu_bf16, ref, what, mask=None, fmt: str = "bf16"):
+    mx, rms, rel, worst = attention_errors(gpu_bf16, ref, mask, fmt)
+    assert worst <= 1.0 and rms <= RMS and rel <= REL_RMS, \
+        f"{what}: max-abs {mx:.3e} ({worst:.2f} of its element's bar) rms {rms:.3e} rel-rms {rel:.3e}"
     return mx, rms, rel
 
 

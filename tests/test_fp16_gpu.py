@@ -44,7 +44,7 @@ def test_f16_decode_tiny_against_oracle():
     assert oracle.ulp_distance_bf16(b16(run.k_cache), kc).max() <= 1
     assert np.array_equal(b16(run.v_cache), vc)
     ref = oracle.cached_gqa_attention(q_rot, kc, vc, pos, rows, wl.scale, fmt=F16)
-    assert_attention_close(run.out.cpu(), ref, "f16 decode tiny")
+    assert_attention_close(run.out.cpu(), ref, "f16 decode tiny", fmt="f16")
     assert run.status() == (0, 0)
 
 
@@ -119,7 +119,7 @@ def test_f16_prefill_against_oracle(kw):
                                                       wl.scale, kc0, vc0, fmt=F16)
     assert oracle.ulp_distance_bf16(b16(kc), kco).max() <= 1
     assert np.array_equal(b16(vc), vco)
-    assert_attention_close(out.cpu(), ref, f"f16 prefill {kw}")
+    assert_attention_close(out.cpu(), ref, f"f16 prefill {kw}", fmt="f16")
     assert kv.kvgqa_read_status(ws) == 0
 
 
@@ -144,5 +144,5 @@ def test_f16_varlen_against_oracle():
     mask = np.zeros(out.shape, dtype=bool)
     for a in range(wl.A):
         mask[a, : int(inp.lengths[a])] = True
-    assert_attention_close(out.cpu(), np.nan_to_num(ref), "f16 varlen", mask=mask)
+    assert_attention_close(out.cpu(), np.nan_to_num(ref), "f16 varlen", mask=mask, fmt="f16")
     assert kv.kvgqa_read_status(ws) == 0
