@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -302,10 +303,16 @@ __device__ __forceinline__ void token_body(const RopeStoreParams& p, int varlen,
   }
 }
 
+// Prompts at offsets with at most this many prompts run in the kernel below,
+// which walks only their real tokens; with more prompts the per-token kernel
+// walks the padded tokens.
+constexpr int kScanPrompts = 2048;
+constexpr int kVarlenBatch = 16;  // tokens per CTA and step (prompts at offsets)
+
 // Decode: part s = blockIdx % 4 of token blockIdx / 4 (one token per CTA
-// quartet).  Prompts at offsets: a grid sized to the GPU walks the padded
-// tokens (stride gridDim / 4), so the tokens past a prompt's length cost a
-// loop step, not a CTA launch.
+// quartet).  Prompts at offsets (more than kScanPrompts of them): a grid sized
+// to the GPU walks the padded tokens (stride gridDim / 4), so the tokens past
+// a prompt's length cost a loop step, not a CTA launch.
 template <int D, bool F16>
 __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(const __grid_constant__ RopeStoreParams p,
                                                                           int varlen) {
@@ -320,6 +327,141 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(cons
   for (int tk = blockIdx.x / kTokenSplit; tk < n_tok; tk += step) {
     token_body<D, F16>(p, varlen, tk, part, cs);
     __syncthreads();  // cs is rewritten for the next token
+  }
+}
+
+// Prompts at offsets (at most kScanPrompts of them), real tokens only.  Every
+// CTA scans the valid prompts' lengths into shared memory (an invalid prompt
+// counts zero tokens; CTA 0 flags it) with their offsets and rows, and maps a
+// running token index to (prompt, token) by binary search.  CTA quartets take
+// kVarlenBatch tokens per step (part s of each token, as token_body): the
+// step first evaluates all their angles (the FP64 chain is the long pole of a
+// token), then streams their Q/K/V units, several loads in flight per thread,
+// holding nothing in registers across the two phases.
+template <int D, bool F16>
+__global__ void __launch_bounds__(kTokenThreads) rope_kv_store_varlen_kernel(const __grid_constant__ RopeStoreParams p) {
+  constexpr int HALF = D / 2;
+  constexpr int F = HALF / kTokenSplit;  // frequencies of this CTA
+  constexpr int CSN = F + F / 8;         // padded cos/sin entries per token
+  constexpr int UF = F / 8;              // rotation units (8 pairs) per head
+  constexpr int VU = D / 8;              // V copy units (16 bytes) per head
+  constexpr int NB = kVarlenBatch;
+  constexpr int kLoads = 4;              // units in flight per thread
+  __shared__ CosSin cs[NB * CSN];
+  __shared__ int tk_s[NB], pos_s[NB], row_s[NB];
+  extern __shared__ int scan[];  // start[A + 1], then off[A], row[A]
+  int* start = scan;
+  int* off_s = scan + p.A + 1;
+  int* rows_s = off_s + p.A;
+  pdl_wait();
+  pdl_trigger();
+  if (p.item_order && blockIdx.x == 0) write_item_order(p);
+  const int part = blockIdx.x % kTokenSplit;
+  const int quartet = blockIdx.x / kTokenSplit, n_quartets = gridDim.x / kTokenSplit;
+  for (int a = threadIdx.x; a < p.A; a += kTokenThreads) {
+    const int off = p.offsets[a], len = p.lengths[a], row = p.cache_rows[a];
+    const bool meta_ok = len >= 0 && len <= p.T && off >= 0 && off <= p.max_seq - len;
+    const bool row_ok = row >= 0 && row < p.S;
+    start[a + 1] = meta_ok && row_ok ? len : 0;
+    off_s[a] = off;
+    rows_s[a] = row;
+    if (blockIdx.x == 0 && !(meta_ok && row_ok))
+      atomicOr(p.status, (meta_ok ? 0 : KVGQA_FLAG_POSITION_RANGE) | (row_ok ? 0 : KVGQA_FLAG_ROW_RANGE));
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // exclusive scan by one warp, 32 prompts per step
+    int carry = 0;
+    for (int base = 0; base < p.A; base += 32) {
+      const int a = base + threadIdx.x;
+      int v = a < p.A ? start[a + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (threadIdx.x >= o) v += n;
+      }
+      if (a < p.A) start[a + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (threadIdx.x == 0) start[0] = 0;
+  }
+  __syncthreads();
+  const int n_real = start[p.A];
+  const int rot_items = (p.H_q + p.H_kv) * UF;
+  const int copy_per_part = p.H_kv * VU / kTokenSplit;
+  const int n_items = rot_items + copy_per_part;
+  // running indices quartet + (k * NB + b) * n_quartets: token b of step k
+  for (int k0 = 0; quartet + k0 * n_quartets < n_real; k0 += NB) {
+    if (threadIdx.x < NB) {
+      const int idx = quartet + (k0 + threadIdx.x) * n_quartets;
+      int t = -1, a = 0;
+      if (idx < n_real) {
+        int lo = 0, hi = p.A;  // the prompt a with start[a] <= idx < start[a + 1]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (start[mid] <= idx) lo = mid;
+          else hi = mid;
+        }
+        a = lo;
+        t = idx - start[lo];
+      }
+      tk_s[threadIdx.x] = t < 0 ? -1 : a * p.T + t;
+      pos_s[threadIdx.x] = t < 0 ? 0 : off_s[a] + t;
+      row_s[threadIdx.x] = rows_s[a];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < NB * F; i += kTokenThreads) {
+      const int b = i / F, f = i % F;
+      if (tk_s[b] >= 0) cs[b * CSN + cs_slot(f)] = rope_cos_sin(pos_s[b], p.inv_freq[part * F + f]);
+    }
+    __syncthreads();
+    const int total = NB * n_items;
+    for (int it0 = threadIdx.x; it0 < total; it0 += kLoads * kTokenThreads) {
+      uint4 xa[kLoads], xb[kLoads];
+      int bb[kLoads], jj[kLoads];
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int it = it0 + u * kTokenThreads;
+        bb[u] = -1;
+        if (it >= total) continue;
+        const int b = it / n_items, j = it % n_items;
+        const int tk = tk_s[b];
+        if (tk < 0) continue;
+        bb[u] = b;
+        jj[u] = j;
+        const size_t tok = tk;
+        if (j < rot_items) {
+          const int h = j / UF, c = part * UF + j % UF;
+          const uint16_t* src = h < p.H_q ? p.q + (tok * p.H_q + h) * D : p.k + (tok * p.H_kv + (h - p.H_q)) * D;
+          xa[u] = *reinterpret_cast<const uint4*>(src + c * 8);
+          xb[u] = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
+        } else {
+          const int v = part * copy_per_part + (j - rot_items);
+          xa[u] = *reinterpret_cast<const uint4*>(p.v + (tok * p.H_kv + v / VU) * D + (v % VU) * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int b = bb[u];
+        if (b < 0) continue;
+        const int j = jj[u];
+        const size_t tok = tk_s[b];
+        const int pos = pos_s[b], row = row_s[b];
+        if (j < rot_items) {
+          const int h = j / UF, cl = j % UF, c = part * UF + cl;
+          uint16_t* dst = h < p.H_q ? p.q_out + (tok * p.H_q + h) * D
+                                    : p.k_cache + ((static_cast<size_t>(row) * p.H_kv + (h - p.H_q)) * p.max_seq + pos) * D;
+          uint4 ya, yb;
+          rotate8<F16>(xa[u], xb[u], cs + b * CSN + cs_slot(cl * 8), ya, yb);
+          *reinterpret_cast<uint4*>(dst + c * 8) = ya;
+          *reinterpret_cast<uint4*>(dst + HALF + c * 8) = yb;
+        } else {
+          const int v = part * copy_per_part + (j - rot_items);
+          *reinterpret_cast<uint4*>(p.v_cache + ((static_cast<size_t>(row) * p.H_kv + v / VU) * p.max_seq + pos) * D +
+                                    (v % VU) * 8) = xa[u];
+        }
+      }
+    }
+    __syncthreads();  // cs and the token slots are rewritten for the next step
   }
 }
 
@@ -338,11 +480,31 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
     if (cudaDeviceGetAttribute(&sm_count[dev0], cudaDevAttrMultiProcessorCount, dev0) != cudaSuccess)
       sm_count[dev0] = 0;
   });
-  const long long varlen_tokens = static_cast<long long>(p.A) * p.T;
-  const long long varlen_cap = 4ll * (sm_count[dev0] > 0 ? sm_count[dev0] : 1);
+  // Prompts at offsets: as many CTAs as are resident at once (the walk over
+  // the tokens is a grid-stride loop), in whole quartets.
+  static int varlen_ctas[64][4];  // per SM, for (D, storage) = (128|64, bf16|f16)
+  static std::once_flag varlen_once[64];
+  std::call_once(varlen_once[dev0], [dev0] {
+    const void* fns[4] = {reinterpret_cast<const void*>(rope_kv_store_varlen_kernel<128, false>),
+                          reinterpret_cast<const void*>(rope_kv_store_varlen_kernel<64, false>),
+                          reinterpret_cast<const void*>(rope_kv_store_varlen_kernel<128, true>),
+                          reinterpret_cast<const void*>(rope_kv_store_varlen_kernel<64, true>)};
+    for (int i = 0; i < 4; ++i)
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&varlen_ctas[dev0][i], fns[i], kTokenThreads,
+                                                        (3 * kScanPrompts + 1) * sizeof(int)) != cudaSuccess ||
+          varlen_ctas[dev0][i] <= 0)
+        varlen_ctas[dev0][i] = 4;
+  });
+  const int vk = (p.D == 128 ? 0 : 1) + (p.f16 ? 2 : 0);
+  const long long varlen_grid =
+      std::max(1ll, static_cast<long long>(sm_count[dev0] > 0 ? sm_count[dev0] : 1) * varlen_ctas[dev0][vk] /
+                        kTokenSplit) * kTokenSplit;
+  const bool scan = mode == 2 && p.A <= kScanPrompts;  // real tokens only
+  const long long varlen_cap = 4ll * (sm_count[dev0] > 0 ? sm_count[dev0] : 1) * kTokenSplit;  // padded walk
   const long long g = mode == 1 ? p.T
-                                : (mode == 0 ? p.A : (varlen_tokens < varlen_cap ? varlen_tokens : varlen_cap)) *
-                                      kTokenSplit;
+                    : mode == 0 ? static_cast<long long>(p.A) * kTokenSplit
+                    : scan ? varlen_grid
+                           : std::min(varlen_cap, static_cast<long long>(p.A) * p.T * kTokenSplit);
   if (g > 0x7fffffffll) return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(g);
   if (grid == 0) return cudaSuccess;
@@ -353,6 +515,9 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(mode == 1 ? 256 : kTokenThreads);
+  // the prompts' scan (prompts at offsets) in dynamic shared memory, so that
+  // the decode store keeps its small footprint
+  cfg.dynamicSmemBytes = scan ? static_cast<size_t>(3 * p.A + 1) * sizeof(int) : 0;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -383,8 +548,9 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
   auto go = [&](auto d, auto f16) {
     constexpr int kD = decltype(d)::value;
     constexpr bool kF16 = decltype(f16)::value;
-    return mode == 1 ? cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<kD, kF16>, p)
-                     : cudaLaunchKernelEx(&cfg, rope_kv_store_token_kernel<kD, kF16>, p, varlen);
+    if (mode == 1) return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<kD, kF16>, p);
+    if (scan) return cudaLaunchKernelEx(&cfg, rope_kv_store_varlen_kernel<kD, kF16>, p);
+    return cudaLaunchKernelEx(&cfg, rope_kv_store_token_kernel<kD, kF16>, p, varlen);
   };
   using T = std::true_type;
   using F = std::false_type;
