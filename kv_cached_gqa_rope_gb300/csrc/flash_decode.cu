@@ -25,17 +25,21 @@
 // segment's partials, writes the output (storage type) and resets the counter to zero.
 //
 // Inside a CTA, per tile of up to 128 keys of one segment:
-//   warp 4     TMA producer: K and V tiles (128B swizzle, 32-row boxes, so a
-//              short tail reads at most 31 rows past the prefix) and the
-//              group's query rows (16 rows: the G heads, the rest padding) into
-//              a 3-stage ring;
+//   warp 4     TMA producer: K and V tiles (128B swizzle; a whole tile in one
+//              128-row box per 64-column half, a short tail in 32-row boxes so
+//              it reads at most 31 rows past the prefix) and the group's query
+//              rows (16 rows: the G heads, the rest padding) into a 3-stage
+//              ring (fewer TMA instructions per tile: the producer's issue
+//              time was part of each tile's period);
 //   warp 5     one thread issues tcgen05.mma: S^T = K Q_g^T (M = 128 keys,
 //              N = 16 heads) into one of two TMEM buffers, then
 //              O^T += V^T P^T (M = D, N = 16; V is an MN-major operand) into a
 //              TMEM accumulator;
 //   warps 0-3  one thread per key: S^T row from TMEM, FP32 online softmax per
-//              head (warp shuffles + a 4-warp exchange for the tile maximum
-//              and sum), P^T in the storage type into 128B-swizzled shared memory; the O^T
+//              head (a warp reduction instruction + a 4-warp exchange for the
+//              tile maximum; each thread keeps its keys' share of the row sums,
+//              summed over the CTA once, at the segment end), P^T in the
+//              storage type into 128B-swizzled shared memory; the O^T
 //              rescale (TMEM load/scale/store, one lane per d) happens only when
 //              a head's maximum grew by more than 2^8; at a segment end each
 //              lane d writes O^T[d][h] / l[h] (or the partial).
@@ -104,8 +108,8 @@ struct Cfg {
   static constexpr int QB_OFF = NS * STAGE;            // fused: query tiles [QR][16 x D]
   static constexpr int QBUF = NSUB * QSUB;
   static constexpr int P_OFF = QB_OFF + QR * QBUF;             // P^T x2 buffers, [16 x 128 keys] each
-  static constexpr int RED_OFF = P_OFF + 2 * 2 * QSUB;         // [2][4 warps][16] floats
-  static constexpr int PREFIX_OFF = RED_OFF + 2 * 4 * NQ * 4;  // [kMaxActiveRows + 1] ints
+  static constexpr int RED_OFF = P_OFF + 2 * 2 * QSUB;         // [3][4 warps][16] floats: maxima x2, sums
+  static constexpr int PREFIX_OFF = RED_OFF + 3 * 4 * NQ * 4;  // [kMaxActiveRows + 1] ints
   static constexpr int NKEYS_OFF = PREFIX_OFF + (kMaxActiveRows + 1) * 4;  // [kMaxActiveRows] ints
   static constexpr int BAR_OFF = align_up(NKEYS_OFF + kMaxActiveRows * 4, 16);
   // kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], q_free[QR],
@@ -121,6 +125,8 @@ struct Cfg {
 struct DecodeMaps {
   CUtensorMap kc;  // cache [S*H_kv][max_seq][D], box {64, 32, 1}
   CUtensorMap vc;
+  CUtensorMap kcf;  // the same with box {64, 128, 1}: a whole tile per sub-tile
+  CUtensorMap vcf;
   CUtensorMap q;   // q_rot [A*H_q][D], box {64, 16}
 };
 
@@ -295,7 +301,8 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* ptr, int v) {
 template <int D, int GP, bool FUSED, bool EARLY>
 __global__ void __launch_bounds__(threads_of(FUSED), 1)
 flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap map_k,
-                           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_q) {
+                           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_q,
+                           const __grid_constant__ CUtensorMap map_kf, const __grid_constant__ CUtensorMap map_vf) {
   static_assert(!(FUSED && EARLY), "the fused step has no store kernel before it");
   using C = Cfg<D, FUSED>;
   extern __shared__ unsigned char smem_raw[];
@@ -327,7 +334,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 1);
+      mbar_init(&p_full[b], 4);  // one arrival per softmax warp
       mbar_init(&o_done[b], 1);
     }
     for (int b = 0; b < C::QR; ++b) {
@@ -394,7 +401,12 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
             mbar_arrive_expect_tx(&kv_full[n_early], static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + QSUB));
 #pragma unroll 1
-            for (int sub = 0; sub < C::NSUB; ++sub)
+            for (int sub = 0; sub < C::NSUB; ++sub) {
+              if (nb * BOX_ROWS == BN) {  // a whole tile: one box each
+                tma_load_3d(st + C::K_OFF + sub * SUB, &map_kf, sub * 64, cur.k0(), kv_row, &kv_full[n_early], pol_kv);
+                tma_load_3d(st + C::V_OFF + sub * SUB, &map_vf, sub * 64, cur.k0(), kv_row, &kv_full[n_early], pol_kv);
+                continue;
+              }
 #pragma unroll 1
               for (int b = 0; b < nb; ++b) {
                 tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
@@ -402,6 +414,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
                 tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
                             kv_row, &kv_full[n_early], pol_kv);
               }
+            }
             qrow[n_early] = cur.a * p.H_q + cur.g * p.G;
           }
           pdl_wait();
@@ -422,11 +435,16 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
           const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
           mbar_arrive_expect_tx(&kv_full[s], bytes);
           for (int sub = 0; sub < C::NSUB; ++sub) {
-            for (int b = 0; b < nb; ++b) {
-              tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
-                          kv_row, &kv_full[s], pol_kv);
-              tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
-                          kv_row, &kv_full[s], pol_kv);
+            if (nb * BOX_ROWS == BN) {  // a whole tile: one box each
+              tma_load_3d(st + C::K_OFF + sub * SUB, &map_kf, sub * 64, cur.k0(), kv_row, &kv_full[s], pol_kv);
+              tma_load_3d(st + C::V_OFF + sub * SUB, &map_vf, sub * 64, cur.k0(), kv_row, &kv_full[s], pol_kv);
+            } else {
+              for (int b = 0; b < nb; ++b) {
+                tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
+                            kv_row, &kv_full[s], pol_kv);
+                tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
+                            kv_row, &kv_full[s], pol_kv);
+              }
             }
             tma_load_3d(st + C::Q_OFF + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, &kv_full[s],
                         pol_q);
@@ -673,9 +691,15 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     // ---------------------------------------------------------- softmax (warps 0-3)
     const int r = threadIdx.x;  // key row of the tile == TMEM lane == d of O^T
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float* red_max = reinterpret_cast<float*>(smem + C::RED_OFF);
-    float* red_sum = red_max + 4 * NQ;
+    // Per-warp maxima of a tile, in one of two buffers by tile parity: a warp
+    // writes tile t+2's into the buffer of tile t only after passing tile
+    // t+1's exchange, which every warp reaches after reading tile t's.
+    float* red_max2 = reinterpret_cast<float*>(smem + C::RED_OFF);
+    float* red_sum = red_max2 + 2 * 4 * NQ;
     unsigned char* pt0 = smem + C::P_OFF;
+    // m_ref: the reference maximum of each head (the same in every thread);
+    // l: this thread's share of each head's row sum (its keys' weights), all
+    // rescaled together and summed over the CTA once, at the segment end.
     float m_ref[GP], l[GP];
 #pragma unroll
     for (int h = 0; h < GP; ++h) { m_ref[h] = -INFINITY; l[h] = 0.f; }
@@ -688,14 +712,14 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       uint32_t u[16];
       tmem_ld16(tmem + lane_base + (it & 1) * NQ, u);
       tmem_wait_ld();
+      float* red_max = red_max2 + (it & 1) * 4 * NQ;
       const bool valid = r < nt;
       float x[GP], mt[GP];
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
         x[h] = (valid && h < p.G) ? __uint_as_float(u[h]) * p.scale_log2 : -INFINITY;
-        float m = x[h];
-#pragma unroll
-        for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+        float m;  // the warp's maximum in one instruction
+        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(x[h]));
         if (lane == 0) red_max[warp * NQ + h] = m;
       }
       named_bar_sync(1, BN);
@@ -740,10 +764,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         if (h < GP) {
           const float pv = x[h] == -INFINITY ? 0.f : exp2f(x[h] - m_ref[h]);
           b = E::from_f32(pv);
-          float ps = E::to_f32(b);
-#pragma unroll
-          for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(FULL, ps, off);
-          if (lane == 0) red_sum[warp * NQ + h] = ps;
+          l[h] += E::to_f32(b);  // the weight P.V actually uses
         }
         *reinterpret_cast<uint16_t*>(pt + sub * QSUB + h * 128 + ((chunk ^ (h & 7)) << 4) + e * 2) = b;
       }
@@ -754,19 +775,28 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
 #pragma unroll
           for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + sb * SUB + c * 16) = make_uint4(0, 0, 0, 0);
       }
-      // Every thread's P^T stores and TMEM reads are done and fenced before the
-      // group synchronises; then one thread arrives (a single arrival instead
-      // of 128 serialised ones on the same barrier).
+      // Each warp's P^T stores and TMEM reads are done and fenced before it
+      // synchronises; then one lane arrives (four arrivals in all, instead
+      // of a CTA-wide barrier or 128 serialised ones).
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(1, BN);
-      if (r == 0) mbar_arrive(&p_full[it & 1]);
-#pragma unroll
-      for (int h = 0; h < GP; ++h)
-        l[h] += (red_sum[h] + red_sum[NQ + h]) + (red_sum[2 * NQ + h] + red_sum[3 * NQ + h]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[it & 1]);
 
       if (cur.last()) {
         // ---------------------------------------------------- segment end
+        // the row sums of the whole segment part: summed over the CTA's keys
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          float ps = l[h];
+#pragma unroll
+          for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(FULL, ps, off);
+          if (lane == 0) red_sum[warp * NQ + h] = ps;
+        }
+        named_bar_sync(1, BN);
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+          l[h] = (red_sum[h] + red_sum[NQ + h]) + (red_sum[2 * NQ + h] + red_sum[3 * NQ + h]);
         if (!__all_sync(FULL, mbar_wait_bounded(&o_done[it & 1], (it >> 1) & 1, abort_flag, p.status))) break;
         tc_fence_after();
         uint32_t o[16];
@@ -826,11 +856,11 @@ cudaError_t make_decode_maps(const DecodeParams& p, DecodeMaps* m) {
   const cuuint64_t D = p.D;
   cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(p.max_seq), static_cast<cuuint64_t>(p.S) * p.H_kv};
   cuuint64_t strides[2] = {D * 2, D * 2 * static_cast<cuuint64_t>(p.max_seq)};
-  cuuint32_t box[3] = {64, BOX_ROWS, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  for (int t = 0; t < 2; ++t) {
-    if (enc(t == 0 ? &m->kc : &m->vc, kTmaElem, 3,
-            const_cast<uint16_t*>(t == 0 ? p.k_cache : p.v_cache), dims, strides, box, es,
+  for (int t = 0; t < 4; ++t) {
+    cuuint32_t bx[3] = {64, t < 2 ? static_cast<cuuint32_t>(BOX_ROWS) : static_cast<cuuint32_t>(BN), 1};
+    CUtensorMap* dst = t == 0 ? &m->kc : t == 1 ? &m->vc : t == 2 ? &m->kcf : &m->vcf;
+    if (enc(dst, kTmaElem, 3, const_cast<uint16_t*>((t & 1) == 0 ? p.k_cache : p.v_cache), dims, strides, bx, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -883,7 +913,7 @@ struct Kernels {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP, FUSED, EARLY>, p, m.kc, m.vc, m.q);
+    return cudaLaunchKernelEx(&cfg, flash_decode_splitk_kernel<D, GP, FUSED, EARLY>, p, m.kc, m.vc, m.q, m.kcf, m.vcf);
   }
   static cudaError_t launch(const DecodeParams& p, const DecodeMaps& m, cudaStream_t stream) {
     if (p.fused) return launch_mode<true, false>(p, m, stream);
