@@ -32,7 +32,9 @@
 //              ring (fewer TMA instructions per tile: the producer's issue
 //              time was part of each tile's period);
 //   warp 5     one thread issues tcgen05.mma: S^T = K Q_g^T (M = 128 keys,
-//              N = 16 heads) into one of two TMEM buffers, then
+//              N = 16 heads) into one of two TMEM buffers (the next tile's
+//              while the softmax works on this one; in the attention call only
+//              if that tile has landed, else after this tile's P.V), then
 //              O^T += V^T P^T (M = D, N = 16; V is an MN-major operand) into a
 //              TMEM accumulator;
 //   warps 0-3  one thread per key: S^T row from TMEM, FP32 online softmax per
@@ -514,12 +516,11 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       constexpr uint32_t V_LBO = D == 128 ? SUB : 0;  // D = 64: the second M half repeats the first
       const uint32_t p_addr = sbase + C::P_OFF;
       bool issued = false;
-      // S^T of tile t.  Attention call: the query tile rides in the tile's
+      // S^T of tile t, its K/V (and query) tile already landed.  Attention call: the query tile rides in the tile's
       // stage.  Fused step: it is ring slot kq % QR of segment kq, rotated by
       // the prep warp; the slot is released after the segment's last S, and a
       // tile that holds the new key waits for the prep warp's patch.
-      auto issue_s = [&](int t, int kq, bool seg_first, bool seg_last, bool new_key) -> bool {
-        if (!mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, abort_flag, p.status)) return false;
+      auto issue_s_ready = [&](int t, int kq, bool seg_first, bool seg_last, bool new_key) -> bool {
         if constexpr (FUSED) {
           if (seg_first && !mbar_wait_bounded(&prep_done[kq % C::QR], (kq / C::QR) & 1, abort_flag, p.status))
             return false;
@@ -543,7 +544,14 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         issued = true;
         return true;
       };
+      auto issue_s = [&](int t, int kq, bool seg_first, bool seg_last, bool new_key) -> bool {
+        if (!mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, abort_flag, p.status)) return false;
+        return issue_s_ready(t, kq, seg_first, seg_last, new_key);
+      };
       int it = 0, kseg = -1;
+      bool s_next = false;  // S of the next tile is still to be issued (its tile was late)
+      int s_kq = 0;
+      bool s_first = false, s_last = false, s_key = false;
       for (; cur.more(); cur.advance(), ++it) {
         if (cur.first()) ++kseg;
         if (it == 0 && !issue_s(0, 0, true, cur.last(), cur.last() && cur.x_end == cur.n)) break;
@@ -560,7 +568,23 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             n_last = nx.last();
             n_key = n_last && nx.x_end == nx.n;
           }
-          if (!issue_s(it + 1, cur.last() ? kseg + 1 : kseg, cur.last(), n_last, n_key)) break;
+          // Issued now only if its tile has landed; otherwise after this
+          // tile's P.V, which is not held up behind the copy (a late P.V
+          // delays the refill of its stage and the end of a segment).
+          // (The attention call only: the whole step's early-start and fused
+          // forms measured faster issuing S first.)
+          constexpr bool kDeferLateS = !EARLY && !FUSED;
+          if (!kDeferLateS) {
+            if (!issue_s(it + 1, cur.last() ? kseg + 1 : kseg, cur.last(), n_last, n_key)) break;
+          } else if (mbar_test(&kv_full[(it + 1) % C::NS], ((it + 1) / C::NS) & 1)) {
+            if (!issue_s_ready(it + 1, cur.last() ? kseg + 1 : kseg, cur.last(), n_last, n_key)) break;
+          } else {
+            s_next = true;
+            s_kq = cur.last() ? kseg + 1 : kseg;
+            s_first = cur.last();
+            s_last = n_last;
+            s_key = n_key;
+          }
         }
         if (!mbar_wait_bounded(&p_full[it & 1], (it >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -575,6 +599,10 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         }
         umma_commit(&o_done[it & 1]);
         umma_commit(&kv_empty[it % C::NS]);
+        if (s_next) {
+          s_next = false;
+          if (!issue_s(it + 1, s_kq, s_first, s_last, s_key)) break;
+        }
       }
       if (*abort_flag && issued) {
         umma_commit(drain);
