@@ -65,8 +65,11 @@ def parse_args():
     ap.add_argument("--no-decode-workloads", action="store_true",
                     help="skip the attention call on the divergent-length and long-context decode workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
-    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
-                    help="run just the timed decode steps or just the prefill calls (for profiler captures)")
+    ap.add_argument("--only", choices=["decode", "prefill", "prefill-varlen"], default=None,
+                    help="run just the timed decode steps, just the prefill calls, or just the chunked prefill call "
+                         "(for profiler captures)")
+    ap.add_argument("--decode-workload", choices=["llama", "divergent", "long", "d64", "g1", "g1d64"],
+                    default="llama", help="with --only decode: the decode workload to run")
     return ap.parse_args()
 
 
@@ -272,6 +275,10 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
     wl = W.LLAMA_DECODE
+    if args.only == "decode":
+        wl = {"llama": W.LLAMA_DECODE, "divergent": W.DIVERGENT_DECODE, "long": W.LONG_DECODE,
+              "d64": W.HEAD_SHAPE_DECODE[0], "g1": W.HEAD_SHAPE_DECODE[1],
+              "g1d64": W.HEAD_SHAPE_DECODE[2]}[args.decode_workload]
     inp = W.make_decode_inputs(wl)
     q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
     pos, rows = inp.positions.to(dev), inp.cache_rows.to(dev)
@@ -301,6 +308,9 @@ def run_ours(args, rank, world, local):
         res = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
         res_v = run_prefill_varlen(args, kv, dev, stream, flush, world, bf16_peak, peak_src)
         return {"impl": "ours", "only": "prefill", "prefill": res, "prefill_varlen": res_v} if rank == 0 else None
+    if args.only == "prefill-varlen":
+        res_v = run_prefill_varlen(args, kv, dev, stream, flush, world, bf16_peak, peak_src)
+        return {"impl": "ours", "only": "prefill-varlen", "prefill_varlen": res_v} if rank == 0 else None
     calls = [("store", store), ("attention", attend)] + ([("step", step), ("single_launch_step", single)]
                                                           if args.only is None else [])
     host_us = host_call_us(calls, n=min(200, 10 * args.steps))
