@@ -137,7 +137,8 @@ kvgqa_status rope_kv_store_workspace_size(size_t* bytes);
  * boundary": even D, nonnegative position, positive base).
  *
  *   q [A,H_q,D] bf16, k/v [A,H_kv,D] bf16, positions/cache_rows [A] int32  (read)
- *   theta  RoPE base, finite and > 0
+ *   theta  RoPE base, finite and > 0, with every theta^(-2i/D) finite (else
+ *          KVGQA_EINVAL; the same holds for every entry point taking theta)
  *   q_out [A,H_q,D] bf16  (written)
  *   k_cache, v_cache [S,H_kv,max_seq,D] bf16  (one cell per token written)
  *   workspace  >= rope_kv_store_workspace_size() bytes, 256-byte aligned

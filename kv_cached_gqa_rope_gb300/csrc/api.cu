@@ -208,8 +208,45 @@ void check_theta(double theta) {
   if (!(theta > 0.0) || !std::isfinite(theta)) fail(KVGQA_EINVAL, "RoPE base theta must be finite and > 0");
 }
 
-void fill_inv_freq(double* out, int D, double theta) {
-  for (int i = 0; i < D / 2; ++i) out[i] = std::pow(theta, -2.0 * i / D);
+// 2/pi to 256 bits: floor(2/pi * 2^256), least significant 64-bit word
+// first (the binary expansion of 2/pi, evaluated with integer arithmetic
+// from Machin's formula for pi).
+constexpr uint64_t kTwoOverPi256[4] = {0xfe5163abdebbc561ull, 0xdb6295993c439041ull, 0xfc2757d1f534ddc0ull,
+                                       0xa2f9836e4e441529ull};
+
+// The RoPE frequencies f_i = theta^(-2i/D) (doubles) as quarter turns per
+// position step, f_i * 2/pi: the exact product of f_i's 53-bit significand
+// with the 256-bit constant, from which the 64 bits after the binary point
+// (rounded down) and the two bits before it are taken.  The kernels reduce
+// pos * f_i modulo pi/2 from these with integer arithmetic.
+void fill_rope_freqs(kvgqa::RopeFreqs* out, int D, double theta) {
+  for (int i = 0; i < D / 2; ++i) {
+    const double f = std::pow(theta, -2.0 * i / D);
+    if (!std::isfinite(f) || f < 0.0) fail(KVGQA_EINVAL, "RoPE base theta %g gives a frequency out of range", theta);
+    int e = 0;
+    const double m = std::frexp(f, &e);  // f = m * 2^e, m in [0.5, 1) (or f = 0)
+    const uint64_t M = static_cast<uint64_t>(std::ldexp(m, 53));  // exact: f = M * 2^(e - 53)
+    uint64_t P[5];  // M * kTwoOverPi256, so f * 2/pi = P * 2^(e - 53 - 256)
+    unsigned __int128 c = 0;
+    for (int w = 0; w < 4; ++w) {
+      c += static_cast<unsigned __int128>(M) * kTwoOverPi256[w];
+      P[w] = static_cast<uint64_t>(c);
+      c >>= 64;
+    }
+    P[4] = static_cast<uint64_t>(c);
+    // bits [lo, lo + 64) of P (zero outside it), i.e. floor(P / 2^lo) mod 2^64
+    auto bits = [&](int lo) -> uint64_t {
+      const int w = lo >= 0 ? lo / 64 : -((-lo + 63) / 64);
+      const int sh = lo - 64 * w;
+      auto word = [&](int k) -> uint64_t { return k >= 0 && k < 5 ? P[k] : 0; };
+      uint64_t r = word(w) >> sh;
+      if (sh) r |= word(w + 1) << (64 - sh);
+      return r;
+    };
+    // f * 2/pi * 2^64 = P * 2^(e - 245)
+    out->frac[i] = bits(245 - e);
+    out->quad[i] = static_cast<uint8_t>(bits(245 - e + 64) & 3);
+  }
 }
 
 View check_workspace(const kvgqa_tensor* ws, size_t need) {
@@ -298,7 +335,7 @@ kvgqa_status rope_kv_store_out_(const kvgqa_tensor* q, const kvgqa_tensor* k,
     p.A = (int)A; p.T = 1; p.H_q = (int)H_q; p.H_kv = (int)H_kv; p.D = (int)D;
     p.S = (int)S; p.max_seq = (int)max_seq;
     p.f16 = elem == KVGQA_F16;
-    fill_inv_freq(p.inv_freq, (int)D, theta);
+    fill_rope_freqs(&p.freqs, (int)D, theta);
     check_cuda(kvgqa::launch_rope_kv_store(p, 0, static_cast<cudaStream_t>(stream)),
                "rope_kv_store launch");
   });
@@ -470,7 +507,7 @@ void decode_step_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_
       p.v_new = static_cast<const uint16_t*>(v->data);
       p.k_cache_w = static_cast<uint16_t*>(k_cache->data);
       p.v_cache_w = static_cast<uint16_t*>(v_cache->data);
-      fill_inv_freq(p.inv_freq, (int)D, theta);
+      fill_rope_freqs(&p.freqs, (int)D, theta);
       check_cuda(kvgqa::launch_cached_gqa_attention(p, st), "decode_step launch");
       return;
     }
@@ -488,7 +525,7 @@ void decode_step_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_
     rp.A = (int)A; rp.T = 1; rp.H_q = (int)H_q; rp.H_kv = (int)H_kv; rp.D = (int)D;
     rp.S = (int)S; rp.max_seq = (int)max_seq;
     rp.f16 = elem == KVGQA_F16;
-    fill_inv_freq(rp.inv_freq, (int)D, theta);
+    fill_rope_freqs(&rp.freqs, (int)D, theta);
     check_cuda(kvgqa::launch_rope_kv_store(rp, 0, st), "decode_step store launch");
     // 2. the attention, started while the store kernel runs: it streams the
     // cache tiles without a new cell before waiting for it
@@ -682,7 +719,7 @@ void prefill_body(const kvgqa_tensor* q, const kvgqa_tensor* k, const kvgqa_tens
   rp.A = (int)A; rp.T = (int)T; rp.H_q = (int)H_q; rp.H_kv = (int)H_kv; rp.D = (int)D;
   rp.S = (int)S; rp.max_seq = (int)max_seq;
   rp.f16 = elem == KVGQA_F16;
-  fill_inv_freq(rp.inv_freq, (int)D, theta);
+  fill_rope_freqs(&rp.freqs, (int)D, theta);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   check_cuda(kvgqa::launch_rope_kv_store(rp, varlen ? 2 : 1, st), "prefill rope_kv_store launch");
   kvgqa::PrefillParams pp{};

@@ -651,7 +651,8 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         }
         if (cur.a != cs_row) {
 #pragma unroll
-          for (int u = 0; u < NU; ++u) cs[u] = rope_cos_sin(pos, p.inv_freq[lane + 32 * u]);
+          for (int u = 0; u < NU; ++u)
+            cs[u] = rope_cos_sin(pos, p.freqs.frac[lane + 32 * u], p.freqs.quad[lane + 32 * u]);
           cs_row = cur.a;
         }
         // the raw query tile arrives with the segment's first tile (on the

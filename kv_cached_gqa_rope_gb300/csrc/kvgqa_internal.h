@@ -16,6 +16,16 @@ constexpr int kMaxHeadDim = 128;
 constexpr int kMaxActiveRows = 1024;  // decode attention keeps per-row tables of A+1 ints in smem
 
 // ------------------------------------------------------------------ RoPE + store
+// The RoPE frequencies f_i = theta^(-2i/D) (each a double computed on the
+// host), stored as the angle a position step adds in quarter turns,
+// f_i * 2/pi: its fraction as a 64-bit fixed-point number (rounded down) and
+// its integer part mod 4.  pos * f_i then reduces modulo pi/2 with integer
+// arithmetic (rope_math.cuh).
+struct RopeFreqs {
+  uint64_t frac[kMaxHeadDim / 2];
+  uint8_t quad[kMaxHeadDim / 2];
+};
+
 struct RopeStoreParams {
   const uint16_t* q;         // decode [A,H_q,D]; prefill [A,T,H_q,D]
   const uint16_t* k;         // decode [A,H_kv,D]; prefill [A,T,H_kv,D]
@@ -31,7 +41,7 @@ struct RopeStoreParams {
   int32_t* status;
   int A, T, H_q, H_kv, D, S, max_seq;
   int f16;                   // storage: 0 BF16, 1 IEEE binary16
-  double inv_freq[kMaxHeadDim / 2];  // theta^(-2i/D), computed on the host in double
+  RopeFreqs freqs;           // the D/2 frequencies theta^(-2i/D)
 };
 
 // mode 0: decode (token a at positions[a]); 1: equal-length prefill (one CTA
@@ -67,7 +77,7 @@ struct DecodeParams {
   const uint16_t* v_new;      // [A,H_kv,D]
   uint16_t* k_cache_w;        // the same caches, written
   uint16_t* v_cache_w;
-  double inv_freq[kMaxHeadDim / 2];  // theta^(-2i/D), computed on the host in double
+  RopeFreqs freqs;            // the D/2 frequencies theta^(-2i/D)
 };
 
 // Padded group size used by the decode kernels: the next power of two >= G.

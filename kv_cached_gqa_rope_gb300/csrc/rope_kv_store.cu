@@ -9,16 +9,18 @@
 // where token (a, t) sits at position t of row cache_rows[a].
 //
 // Equal-length prefill: one CTA owns one position.  It evaluates the D/2
-// cos/sin of pos * theta^(-2i/D) once (rope_cos_sin: FP64 angle reduction,
-// double-float series) and keeps them as FP32 hi+lo pairs in shared memory;
-// the A tokens at that position then stream their heads through 16-byte
-// vector loads and stores.  Decode and the prefill of prompts at offsets (one
-// position per token): kTokenSplit CTAs share a token, each owning a quarter
-// of the frequencies of every head (and a quarter of its V bytes), so that
-// the angle work of a token is spread over four SMs; each CTA issues its
-// loads before it evaluates its angles.  The rotation is evaluated with FP32
-// error-free products so that the BF16 result is within one rounding of the
-// exact value even where x cos - y sin cancels.
+// cos/sin of pos * theta^(-2i/D) once (rope_cos_sin: integer reduction
+// modulo pi/2, double-float series) and keeps them as FP32 hi+lo pairs in
+// shared memory; the A tokens at that position then stream their heads
+// through 16-byte vector loads and stores.  Decode: kTokenSplit CTAs share a
+// token, each owning a quarter of the frequencies of every head (and a
+// quarter of its V bytes), so that the angle work of a token is spread over
+// four SMs; each CTA issues its loads before it evaluates its angles.  The
+// prefill of prompts at offsets (one position per token): CTAs take groups of
+// consecutive real tokens whole, like the equal-length kernel with per-token
+// angles.  The rotation is evaluated with FP32 error-free products so that
+// the BF16 result is within one rounding of the exact value even where
+// x cos - y sin cancels.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -73,7 +75,8 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
   const int pos = blockIdx.x;  // position t, shared by all A prompts
   const int ntok = p.A;
 
-  for (int i = threadIdx.x; i < HALF; i += blockDim.x) cs[cs_slot(i)] = rope_cos_sin(pos, p.inv_freq[i]);
+  for (int i = threadIdx.x; i < HALF; i += blockDim.x)
+    cs[cs_slot(i)] = rope_cos_sin(pos, p.freqs.frac[i], p.freqs.quad[i]);
   __syncthreads();
 
   // The work of this position: every token's rotation units (8 pairs of Q or
@@ -265,7 +268,8 @@ __device__ __forceinline__ void token_body(const RopeStoreParams& p, int varlen,
     return;
   }
 
-  for (int i = threadIdx.x; i < F; i += kTokenThreads) cs[cs_slot(i)] = rope_cos_sin(pos, p.inv_freq[part * F + i]);
+  for (int i = threadIdx.x; i < F; i += kTokenThreads)
+    cs[cs_slot(i)] = rope_cos_sin(pos, p.freqs.frac[part * F + i], p.freqs.quad[part * F + i]);
   __syncthreads();
 
   auto store = [&](int j, const uint4& va, const uint4& vb) {
@@ -307,7 +311,8 @@ __device__ __forceinline__ void token_body(const RopeStoreParams& p, int varlen,
 // which walks only their real tokens; with more prompts the per-token kernel
 // walks the padded tokens.
 constexpr int kScanPrompts = 2048;
-constexpr int kVarlenBatch = 16;  // tokens per CTA and step (prompts at offsets)
+constexpr int kVarlenGroup = 8;     // tokens per CTA and step (prompts at offsets)
+constexpr int kVarlenThreads = 256;
 
 // Decode: part s = blockIdx % 4 of token blockIdx / 4 (one token per CTA
 // quartet).  Prompts at offsets (more than kScanPrompts of them): a grid sized
@@ -332,21 +337,22 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(cons
 
 // Prompts at offsets (at most kScanPrompts of them), real tokens only.  Every
 // CTA scans the valid prompts' lengths into shared memory (an invalid prompt
-// counts zero tokens; CTA 0 flags it) with their offsets and rows, and maps a
-// running token index to (prompt, token) by binary search.  CTA quartets take
-// kVarlenBatch tokens per step (part s of each token, as token_body): the
-// step first evaluates all their angles (the FP64 chain is the long pole of a
-// token), then streams their Q/K/V units, several loads in flight per thread,
-// holding nothing in registers across the two phases.
+// counts zero tokens; CTA 0 flags it) with their offsets and rows.  The real
+// tokens, in prompt order, form groups of kVarlenGroup; a CTA takes whole
+// groups (grid stride), maps each token to (prompt, token) by binary search,
+// evaluates the D/2 angles of each of the group's tokens into shared memory,
+// then streams the group's rotation and copy units as the equal-length kernel
+// does, kBatch loads in flight per thread.  A group's tokens are mostly
+// consecutive positions of one prompt, so its cache writes are contiguous
+// per head, and every head's units are read and written as whole rows.
 template <int D, bool F16>
-__global__ void __launch_bounds__(kTokenThreads) rope_kv_store_varlen_kernel(const __grid_constant__ RopeStoreParams p) {
+__global__ void __launch_bounds__(kVarlenThreads, 3) rope_kv_store_varlen_kernel(const __grid_constant__ RopeStoreParams p) {
   constexpr int HALF = D / 2;
-  constexpr int F = HALF / kTokenSplit;  // frequencies of this CTA
-  constexpr int CSN = F + F / 8;         // padded cos/sin entries per token
-  constexpr int UF = F / 8;              // rotation units (8 pairs) per head
-  constexpr int VU = D / 8;              // V copy units (16 bytes) per head
-  constexpr int NB = kVarlenBatch;
-  constexpr int kLoads = 4;              // units in flight per thread
+  constexpr int CSN = HALF + HALF / 8;  // padded cos/sin entries per token
+  constexpr int RU = D / 16;            // rotation units per head: 8 pairs each
+  constexpr int VU = D / 8;             // copy units per head: 16 bytes each
+  constexpr int NB = kVarlenGroup;
+  constexpr int kBatch = 4;
   __shared__ CosSin cs[NB * CSN];
   __shared__ int tk_s[NB], pos_s[NB], row_s[NB];
   extern __shared__ int scan[];  // start[A + 1], then off[A], row[A]
@@ -356,9 +362,7 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_varlen_kernel(con
   pdl_wait();
   pdl_trigger();
   if (p.item_order && blockIdx.x == 0) write_item_order(p);
-  const int part = blockIdx.x % kTokenSplit;
-  const int quartet = blockIdx.x / kTokenSplit, n_quartets = gridDim.x / kTokenSplit;
-  for (int a = threadIdx.x; a < p.A; a += kTokenThreads) {
+  for (int a = threadIdx.x; a < p.A; a += blockDim.x) {
     const int off = p.offsets[a], len = p.lengths[a], row = p.cache_rows[a];
     const bool meta_ok = len >= 0 && len <= p.T && off >= 0 && off <= p.max_seq - len;
     const bool row_ok = row >= 0 && row < p.S;
@@ -386,13 +390,11 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_varlen_kernel(con
   }
   __syncthreads();
   const int n_real = start[p.A];
-  const int rot_items = (p.H_q + p.H_kv) * UF;
-  const int copy_per_part = p.H_kv * VU / kTokenSplit;
-  const int n_items = rot_items + copy_per_part;
-  // running indices quartet + (k * NB + b) * n_quartets: token b of step k
-  for (int k0 = 0; quartet + k0 * n_quartets < n_real; k0 += NB) {
+  const int rot_units = (p.H_q + p.H_kv) * RU;
+  const int copy_units = p.H_kv * VU;
+  for (int g0 = blockIdx.x * NB; g0 < n_real; g0 += gridDim.x * NB) {
     if (threadIdx.x < NB) {
-      const int idx = quartet + (k0 + threadIdx.x) * n_quartets;
+      const int idx = g0 + threadIdx.x;
       int t = -1, a = 0;
       if (idx < n_real) {
         int lo = 0, hi = p.A;  // the prompt a with start[a] <= idx < start[a + 1]
@@ -409,59 +411,68 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_varlen_kernel(con
       row_s[threadIdx.x] = rows_s[a];
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < NB * F; i += kTokenThreads) {
-      const int b = i / F, f = i % F;
-      if (tk_s[b] >= 0) cs[b * CSN + cs_slot(f)] = rope_cos_sin(pos_s[b], p.inv_freq[part * F + f]);
+    const int nb = min(NB, n_real - g0);  // tokens of this group (the last group may be short)
+    for (int i = threadIdx.x; i < nb * HALF; i += blockDim.x) {
+      const int b = i / HALF, f = i % HALF;
+      cs[b * CSN + cs_slot(f)] = rope_cos_sin(pos_s[b], p.freqs.frac[f], p.freqs.quad[f]);
     }
     __syncthreads();
-    const int total = NB * n_items;
-    for (int it0 = threadIdx.x; it0 < total; it0 += kLoads * kTokenThreads) {
-      uint4 xa[kLoads], xb[kLoads];
-      int bb[kLoads], jj[kLoads];
+    const int n_rot = nb * rot_units;
+    for (int base = threadIdx.x; base < n_rot; base += kBatch * blockDim.x) {
+      uint4 xa[kBatch], xb[kBatch];
+      uint16_t* dst[kBatch];
+      int cc[kBatch], bb[kBatch];
 #pragma unroll
-      for (int u = 0; u < kLoads; ++u) {
-        const int it = it0 + u * kTokenThreads;
-        bb[u] = -1;
-        if (it >= total) continue;
-        const int b = it / n_items, j = it % n_items;
-        const int tk = tk_s[b];
-        if (tk < 0) continue;
-        bb[u] = b;
-        jj[u] = j;
-        const size_t tok = tk;
-        if (j < rot_items) {
-          const int h = j / UF, c = part * UF + j % UF;
-          const uint16_t* src = h < p.H_q ? p.q + (tok * p.H_q + h) * D : p.k + (tok * p.H_kv + (h - p.H_q)) * D;
-          xa[u] = *reinterpret_cast<const uint4*>(src + c * 8);
-          xb[u] = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
+      for (int u = 0; u < kBatch; ++u) {
+        const int r = base + u * blockDim.x;
+        dst[u] = nullptr;
+        if (r >= n_rot) continue;
+        const int b = r / rot_units, rr = r % rot_units;
+        const size_t tok = tk_s[b];
+        const int h = rr / RU, c = rr % RU;
+        const uint16_t* src;
+        if (h < p.H_q) {
+          src = p.q + (tok * p.H_q + h) * D;
+          dst[u] = p.q_out + (tok * p.H_q + h) * D;
         } else {
-          const int v = part * copy_per_part + (j - rot_items);
-          xa[u] = *reinterpret_cast<const uint4*>(p.v + (tok * p.H_kv + v / VU) * D + (v % VU) * 8);
+          const int g = h - p.H_q;
+          src = p.k + (tok * p.H_kv + g) * D;
+          dst[u] = p.k_cache + ((static_cast<size_t>(row_s[b]) * p.H_kv + g) * p.max_seq + pos_s[b]) * D;
         }
+        cc[u] = c;
+        bb[u] = b;
+        xa[u] = *reinterpret_cast<const uint4*>(src + c * 8);
+        xb[u] = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
       }
 #pragma unroll
-      for (int u = 0; u < kLoads; ++u) {
-        const int b = bb[u];
-        if (b < 0) continue;
-        const int j = jj[u];
-        const size_t tok = tk_s[b];
-        const int pos = pos_s[b], row = row_s[b];
-        if (j < rot_items) {
-          const int h = j / UF, cl = j % UF, c = part * UF + cl;
-          uint16_t* dst = h < p.H_q ? p.q_out + (tok * p.H_q + h) * D
-                                    : p.k_cache + ((static_cast<size_t>(row) * p.H_kv + (h - p.H_q)) * p.max_seq + pos) * D;
-          uint4 ya, yb;
-          rotate8<F16>(xa[u], xb[u], cs + b * CSN + cs_slot(cl * 8), ya, yb);
-          *reinterpret_cast<uint4*>(dst + c * 8) = ya;
-          *reinterpret_cast<uint4*>(dst + HALF + c * 8) = yb;
-        } else {
-          const int v = part * copy_per_part + (j - rot_items);
-          *reinterpret_cast<uint4*>(p.v_cache + ((static_cast<size_t>(row) * p.H_kv + v / VU) * p.max_seq + pos) * D +
-                                    (v % VU) * 8) = xa[u];
-        }
+      for (int u = 0; u < kBatch; ++u) {
+        if (!dst[u]) continue;
+        uint4 ya, yb;
+        rotate8<F16>(xa[u], xb[u], cs + bb[u] * CSN + cs_slot(cc[u] * 8), ya, yb);
+        *reinterpret_cast<uint4*>(dst[u] + cc[u] * 8) = ya;
+        *reinterpret_cast<uint4*>(dst[u] + HALF + cc[u] * 8) = yb;
       }
     }
-    __syncthreads();  // cs and the token slots are rewritten for the next step
+    const int n_copy = nb * copy_units;
+    for (int base = threadIdx.x; base < n_copy; base += kBatch * blockDim.x) {
+      uint4 x[kBatch];
+      uint16_t* dst[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int r = base + u * blockDim.x;
+        dst[u] = nullptr;
+        if (r >= n_copy) continue;
+        const int b = r / copy_units, rr = r % copy_units;
+        const size_t tok = tk_s[b];
+        const int g = rr / VU, c = rr % VU;
+        dst[u] = p.v_cache + ((static_cast<size_t>(row_s[b]) * p.H_kv + g) * p.max_seq + pos_s[b]) * D + c * 8;
+        x[u] = *reinterpret_cast<const uint4*>(p.v + (tok * p.H_kv + g) * D + c * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = x[u];
+    }
+    __syncthreads();  // cs and the token slots are rewritten for the next group
   }
 }
 
@@ -481,7 +492,7 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
       sm_count[dev0] = 0;
   });
   // Prompts at offsets: as many CTAs as are resident at once (the walk over
-  // the tokens is a grid-stride loop), in whole quartets.
+  // the token groups is a grid-stride loop).
   static int varlen_ctas[64][4];  // per SM, for (D, storage) = (128|64, bf16|f16)
   static std::once_flag varlen_once[64];
   std::call_once(varlen_once[dev0], [dev0] {
@@ -490,15 +501,14 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
                           reinterpret_cast<const void*>(rope_kv_store_varlen_kernel<128, true>),
                           reinterpret_cast<const void*>(rope_kv_store_varlen_kernel<64, true>)};
     for (int i = 0; i < 4; ++i)
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&varlen_ctas[dev0][i], fns[i], kTokenThreads,
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&varlen_ctas[dev0][i], fns[i], kVarlenThreads,
                                                         (3 * kScanPrompts + 1) * sizeof(int)) != cudaSuccess ||
           varlen_ctas[dev0][i] <= 0)
         varlen_ctas[dev0][i] = 4;
   });
   const int vk = (p.D == 128 ? 0 : 1) + (p.f16 ? 2 : 0);
   const long long varlen_grid =
-      std::max(1ll, static_cast<long long>(sm_count[dev0] > 0 ? sm_count[dev0] : 1) * varlen_ctas[dev0][vk] /
-                        kTokenSplit) * kTokenSplit;
+      std::max(1ll, static_cast<long long>(sm_count[dev0] > 0 ? sm_count[dev0] : 1) * varlen_ctas[dev0][vk]);
   const bool scan = mode == 2 && p.A <= kScanPrompts;  // real tokens only
   const long long varlen_cap = 4ll * (sm_count[dev0] > 0 ? sm_count[dev0] : 1) * kTokenSplit;  // padded walk
   const long long g = mode == 1 ? p.T
@@ -514,7 +524,7 @@ cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(mode == 1 ? 256 : kTokenThreads);
+  cfg.blockDim = dim3(mode == 1 ? 256 : scan ? kVarlenThreads : kTokenThreads);
   // the prompts' scan (prompts at offsets) in dynamic shared memory, so that
   // the decode store keeps its small footprint
   cfg.dynamicSmemBytes = scan ? static_cast<size_t>(3 * p.A + 1) * sizeof(int) : 0;

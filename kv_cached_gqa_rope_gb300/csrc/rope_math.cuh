@@ -53,29 +53,37 @@ __host__ __device__ constexpr DF df_const(double v) {
   return DF{static_cast<float>(v), static_cast<float>(v - static_cast<double>(static_cast<float>(v)))};
 }
 
-// cos and sin of pos * inv_freq, as FP32 hi+lo pairs (absolute error about
-// 1e-11, far below a 16-bit ulp, so a rotation built from them stays one
-// rounding away from the exact value).  Only the angle and its reduction use
-// FP64, a handful of operations: phi = pos * inv_freq, q = nearest integer to
-// phi / (pi/2), x = phi - q*pi/2 with pi/2 split in two doubles and the
-// products fused (Cody and Waite's reduction), so |x| <= pi/4.  sin x and
-// cos x are then Taylor series (coefficients 1/n!) evaluated in double-float
-// FP32 arithmetic by Horner's rule: the terms up to x^5 (sin) and x^6 (cos)
-// in double-float, the smaller ones (below 4e-5 in size) in plain FP32; the
-// first omitted terms, x^15/15! and x^14/14!, are below 3e-14 for
-// |x| <= pi/4.  The quadrant q mod 4 then maps (sin x, cos x) to
-// (sin phi, cos phi).  (FP64 runs at a small fraction of the FP32 rate on
-// this GPU; a full FP64 sincos per angle was the store kernel's long pole.)
-__device__ __forceinline__ CosSin rope_cos_sin(int pos, double inv_freq) {
-  constexpr double kPio2Hi = 1.5707963267948966;     // nearest double to pi/2
-  constexpr double kPio2Lo = 6.123233995736766e-17;  // pi/2 - kPio2Hi
-  constexpr double k2OverPi = 0.6366197723675814;    // 2/pi
-  const double phi = static_cast<double>(pos) * inv_freq;
-  const double q = rint(phi * k2OverPi);
-  const double xd = fma(-q, kPio2Lo, fma(-q, kPio2Hi, phi));
-  const int quad = static_cast<int>(static_cast<long long>(q) & 3);
-  const float xh = static_cast<float>(xd);
-  const DF x{xh, static_cast<float>(xd - static_cast<double>(xh))};
+// cos and sin of pos * f, f one of the RoPE frequencies given as f * 2/pi
+// (quarter turns per position step: fraction `frac` in 64-bit fixed point,
+// integer part mod 4 `quad`), as FP32 hi+lo pairs with an absolute error of
+// a few 1e-14.  The reduction modulo pi/2 is Payne and Hanek's: with the
+// frequency already scaled by 2/pi to 64 fractional bits, pos * f in quarter
+// turns is an exact integer product (a position is below 2^31), whose upper
+// bits count whole quarter turns and whose lower 64 bits are the fraction.
+// Rounding to the nearest quarter turn leaves a signed fraction of at most
+// one half, which becomes the reduced angle |x| <= pi/4 as a double-float
+// (its top 48 bits, exactly, times pi/2 * 2^-48).  The reduction thus costs a
+// few integer operations instead of FP64 arithmetic, which runs at a small
+// fraction of the FP32 rate on this GPU.  sin x and cos x are then Taylor
+// series (coefficients 1/n!) evaluated in double-float FP32 arithmetic by
+// Horner's rule: the terms up to x^5 (sin) and x^6 (cos) in double-float, the
+// smaller ones (below 4e-5 in size) in plain FP32; the first omitted terms,
+// x^15/15! and x^14/14!, are below 3e-14 for |x| <= pi/4.  The quadrant then
+// maps (sin x, cos x) to (sin, cos) of the whole angle.
+__device__ __forceinline__ CosSin rope_cos_sin(int pos, uint64_t frac, uint32_t quad) {
+  const uint32_t n = static_cast<uint32_t>(pos);  // 0 <= pos < 2^31
+  const uint64_t lo = static_cast<uint64_t>(n) * static_cast<uint32_t>(frac);
+  const uint64_t hi = static_cast<uint64_t>(n) * static_cast<uint32_t>(frac >> 32);
+  const uint64_t f64 = lo + (hi << 32);  // n * frac mod 2^64: the fraction of a quarter turn
+  const uint32_t whole = static_cast<uint32_t>(hi >> 32) + (f64 < lo ? 1u : 0u) + n * quad;
+  // a fraction of one half or more rounds up to the next quarter turn, and
+  // its signed reading (f64 - 2^64) is then the remainder
+  const uint32_t q = (whole + static_cast<uint32_t>(f64 >> 63)) & 3u;
+  const int64_t r = static_cast<int64_t>(f64) >> 16;  // |r| <= 2^47, units of 2^-48 quarter turns
+  const DF rd = df_two_sum(static_cast<float>(static_cast<int32_t>(r >> 24)) * 16777216.0f,  // both exact
+                           static_cast<float>(static_cast<int32_t>(r & 0xffffff)));
+  constexpr DF kQuarterTurn48 = df_const(1.5707963267948966 / 281474976710656.0);  // pi/2 * 2^-48
+  const DF x = df_mul(rd, kQuarterTurn48);
   const DF y = df_mul(x, x);  // x^2
   // sin x = x (1 + y (-1/3! + y (1/5! + y Ts))), Ts = -1/7! + y/9! - y^2/11! + y^3/13!
   const float ts = __fmaf_rn(__fmaf_rn(__fmaf_rn(y.h, 1.0f / 6227020800.0f, -1.0f / 39916800.0f), y.h,
@@ -91,9 +99,9 @@ __device__ __forceinline__ CosSin rope_cos_sin(int pos, double inv_freq) {
   const DF c3 = df_add(df_const(1.0 / 24.0), df_mul(y, c4));
   const DF c2 = df_add(df_const(-0.5), df_mul(y, c3));
   const DF cx = df_add(df_const(1.0), df_mul(y, c2));
-  // phi = x + quad * pi/2
+  // the angle is x + q * pi/2
   DF c, s;
-  switch (quad) {
+  switch (q) {
     case 0: c = cx; s = sx; break;
     case 1: c = DF{-sx.h, -sx.l}; s = cx; break;
     case 2: c = DF{-cx.h, -cx.l}; s = DF{-sx.h, -sx.l}; break;

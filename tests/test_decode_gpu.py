@@ -245,3 +245,18 @@ def test_host_errors_on_device_tensors():
         kv.cached_gqa_attention_out_(run.q, run.k_cache, run.v_cache, run.positions, run.cache_rows, 0.1,
                                      run.out, small)
     assert e.value.code == "EWORKSPACE"
+
+
+def test_theta_with_an_infinite_frequency_is_refused():
+    """A positive, finite base so small that theta^(-2i/D) overflows: refused
+    on the host before anything is queued (the cache keeps its bytes)."""
+    import kv_cached_gqa_rope_gb300 as kv
+    inp = W.make_decode_inputs(W.TINY_DECODE)
+    run = DecodeRun(inp)
+    before = run.k_cache.clone()
+    with pytest.raises(kv.KvgqaError) as e:
+        kv.rope_kv_store_out_(run.q, run.k, run.v, run.positions, run.cache_rows, 1e-320,
+                              run.q_out, run.k_cache, run.v_cache, run.ws_store)
+    assert e.value.code == "EINVAL"
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int16), run.k_cache.view(torch.int16))
