@@ -10,11 +10,13 @@
 // precision softmax keeps FP32 reductions and rounds only the caller output.
 //
 // Work split.  Segment (a, g) is the prefix of KV head g in row cache_rows[a]:
-// n_a = positions[a] + 1 keys, contiguous in memory.  A tile costs about the
-// same whether it holds 128 keys or a short tail (its softmax and P.V round
-// trip dominate), so work is balanced in a virtual key space where segment
-// (a, g) occupies ceil(n_a / 128) * 128 + SEG_V keys: its n_a real keys first,
-// then padding that stands for the cost of its tail tile and its end.  CTA b
+// n_a = positions[a] + 1 keys, contiguous in memory.  A tile holds up to TK
+// keys (128, or 256 at head width 64: 64 KB of K and V either way).  A tile
+// costs about the same whether it is whole or a short tail (its softmax and
+// P.V round trip dominate), so work is balanced in a
+// virtual key space where segment (a, g) occupies ceil(n_a / TK) * TK + SEG_V
+// * TK / 128 keys: its n_a real keys first, then padding that stands for the
+// cost of its tail tile and its end.  CTA b
 // of the persistent grid (one CTA per SM) takes the virtual range
 // [b*W, (b+1)*W), W = ceil(V_tot / grid), and processes the real keys in it.
 // A segment whose real keys lie inside one CTA is finished there (output in the storage type
@@ -24,7 +26,9 @@
 // in a per-segment counter, and the one that completes the count merges the
 // segment's partials, writes the output (storage type) and resets the counter to zero.
 //
-// Inside a CTA, per tile of up to 128 keys of one segment:
+// Inside a CTA, per tile of up to TK keys of one segment (below for TK = 128;
+// a 256-key tile is two 128-key blocks, each its own S MMA chain into its own
+// TMEM columns and one key per softmax thread, and one P.V over both):
 //   warp 4     TMA producer: K and V tiles (128B swizzle; a whole tile in one
 //              128-row box per 64-column half, a short tail in 32-row boxes so
 //              it reads at most 31 rows past the prefix) and the group's query
@@ -73,16 +77,15 @@ constexpr bool kF16 = KVGQA_DECODE_F16 != 0;
 using E = Elem<kF16>;
 constexpr CUtensorMapDataType kTmaElem = kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
-constexpr int BN = 128;                 // keys per tile (= TMEM lanes = softmax threads)
+constexpr int BN = 128;                 // keys per block (= MMA M = TMEM lanes = softmax threads)
 constexpr int NQ = 16;                  // MMA N: query heads of a group, padded
 constexpr int BOX_ROWS = 32;            // rows per TMA box of a K or V tile
-constexpr int SUB = BN * 128;           // one [128 rows x 64 16-bit values] swizzled sub-tile
+constexpr int SUB = BN * 128;           // one [128 rows x 64 16-bit values] swizzled block
 constexpr int QSUB = NQ * 128;          // one [16 rows x 64 16-bit values] swizzled sub-tile
 // 4 softmax warps + producer + MMA, plus the query/cell prep warp of the fused step
 __host__ __device__ constexpr int threads_of(bool fused) { return fused ? 224 : 192; }
-constexpr int TMEM_COLS = 64;           // S^T x2 (16 cols each) + O^T (16 cols)
-constexpr int W_MIN = 256;              // fewest (virtual) keys a CTA is given
-constexpr int SEG_V = 128;              // virtual keys charged for a segment end
+constexpr int W_MIN = 256;              // fewest (virtual) keys a CTA is given, per 128-key block of a tile
+constexpr int SEG_V = 128;              // virtual keys charged for a segment end, per block of a tile
 constexpr unsigned FULL = 0xffffffffu;
 
 // One split-K partial result: o[GP][D], then m[GP], then l[GP] (each of the
@@ -95,22 +98,32 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 template <int D, bool FUSED>
 struct Cfg {
   static constexpr int NSUB = D / 64;
-  static constexpr int NS = D == 128 ? 3 : 4;          // stages
+  // Keys per tile: one 128-key block, or two at D = 64, so that a tile
+  // carries 64 KB of K and V at either width (the per-tile chain of S MMA,
+  // softmax and P.V, not the bytes, bounded 32 KB tiles).  A block is one
+  // M = 128 MMA and one key per softmax thread.  Every form of the call (the
+  // attention call, the early-start and the fused step) uses the same tiles,
+  // so that their FP32 sums, and hence their outputs, are bit-identical.
+  static constexpr int KB = D == 64 ? 2 : 1;
+  static constexpr int TK = KB * BN;
+  static constexpr int SUBK = KB * SUB;                // one [TK rows x 64 values] swizzled sub-tile
+  static constexpr int NS = D == 128 || KB == 2 ? 3 : 4;  // stages
   static constexpr int K_OFF = 0;                      // inside a stage
-  static constexpr int V_OFF = NSUB * SUB;
+  static constexpr int V_OFF = NSUB * SUBK;
   // Attention call: each stage also carries the segment's (rotated) query
   // tile, loaded with every K/V tile.  Fused step: the query tile is rotated
   // in shared memory once per segment, in a ring of QR buffers, one more than
   // the stages, so the producer (at most NS tiles, hence NS segments, ahead)
   // never waits for a query buffer and no per-segment barrier of the ring can
   // run two phases ahead of its waiter.
-  static constexpr int Q_OFF = 2 * NSUB * SUB;
-  static constexpr int STAGE = FUSED ? 2 * NSUB * SUB : 2 * NSUB * SUB + NSUB * QSUB;  // multiple of 1024
+  static constexpr int Q_OFF = 2 * NSUB * SUBK;
+  static constexpr int STAGE = FUSED ? 2 * NSUB * SUBK : 2 * NSUB * SUBK + NSUB * QSUB;  // multiple of 1024
   static constexpr int QR = FUSED ? NS + 1 : 0;
   static constexpr int QB_OFF = NS * STAGE;            // fused: query tiles [QR][16 x D]
   static constexpr int QBUF = NSUB * QSUB;
-  static constexpr int P_OFF = QB_OFF + QR * QBUF;             // P^T x2 buffers, [16 x 128 keys] each
-  static constexpr int RED_OFF = P_OFF + 2 * 2 * QSUB;         // [3][4 warps][16] floats: maxima x2, sums
+  static constexpr int PBUF = TK / 64 * QSUB;                 // P^T [16 x TK keys]: 64-key swizzled sub-tiles
+  static constexpr int P_OFF = QB_OFF + QR * QBUF;             // P^T x2 buffers
+  static constexpr int RED_OFF = P_OFF + 2 * PBUF;             // [3][4 warps][16] floats: maxima x2, sums
   static constexpr int PREFIX_OFF = RED_OFF + 3 * 4 * NQ * 4;  // [kMaxActiveRows + 1] ints
   static constexpr int NKEYS_OFF = PREFIX_OFF + (kMaxActiveRows + 1) * 4;  // [kMaxActiveRows] ints
   static constexpr int BAR_OFF = align_up(NKEYS_OFF + kMaxActiveRows * 4, 16);
@@ -120,6 +133,8 @@ struct Cfg {
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 8;
   static constexpr int SMEM = FLAG_OFF + 16 + 1024;            // + alignment slack
+  static constexpr int TMEM_COLS = KB == 1 ? 64 : 128;        // S^T x2 (KB x 16 cols each) + O^T (16 cols)
+  static constexpr int O_COL = 2 * KB * NQ;                    // TMEM column of O^T
   static_assert(STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -132,11 +147,14 @@ struct DecodeMaps {
   CUtensorMap q;   // q_rot [A*H_q][D], box {64, 16}
 };
 
-// Virtual length of a segment of n real keys (0 for an invalid row).
-__device__ __forceinline__ int seg_vlen(int n) { return n == 0 ? 0 : (n + BN - 1) / BN * BN + SEG_V; }
+// Virtual length of a segment of n real keys in tiles of TK keys (0 for an
+// invalid row).
+template <int TK>
+__device__ __forceinline__ int seg_vlen(int n) { return n == 0 ? 0 : (n + TK - 1) / TK * TK + SEG_V * (TK / BN); }
 
 // Running sum over rows of H_kv * seg_vlen(n_a): prefix[a] is the virtual
 // start of row a's first segment.  Invalid metadata -> an empty row.
+template <int TK>
 __device__ void build_prefix(const DecodeParams& p, int* prefix, int* nkeys, bool flag) {
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
@@ -149,7 +167,7 @@ __device__ void build_prefix(const DecodeParams& p, int* prefix, int* nkeys, boo
         const int row = p.cache_rows[a];
         const bool pos_ok = pos >= 0 && pos < p.max_seq;
         const bool row_ok = row >= 0 && row < p.S;
-        if (pos_ok && row_ok) n = seg_vlen(pos + 1) * p.H_kv;
+        if (pos_ok && row_ok) n = seg_vlen<TK>(pos + 1) * p.H_kv;
         nkeys[a] = pos_ok && row_ok ? pos + 1 : 0;
         bad |= (pos_ok ? 0 : KVGQA_FLAG_POSITION_RANGE) | (row_ok ? 0 : KVGQA_FLAG_ROW_RANGE);
       }
@@ -169,13 +187,15 @@ __device__ void build_prefix(const DecodeParams& p, int* prefix, int* nkeys, boo
   __syncthreads();
 }
 
+template <int TK>
 __device__ __forceinline__ int keys_per_cta(int k_tot, int num_ctas) {
   const int w = (k_tot + num_ctas - 1) / num_ctas;
-  return w < W_MIN ? W_MIN : w;
+  return w < W_MIN * (TK / BN) ? W_MIN * (TK / BN) : w;
 }
 
 // Walks the tiles of one CTA's virtual range [v0, v1): segment by segment, the
-// real keys of each in tiles of at most BN.  Every role runs its own copy.
+// real keys of each in tiles of at most TK.  Every role runs its own copy.
+template <int TK>
 struct Cursor {
   const int* prefix;
   const int* nkeys;
@@ -226,7 +246,7 @@ struct Cursor {
   bool done_ = false;
   __device__ __forceinline__ bool more() const { return !done_; }
   __device__ __forceinline__ int k0() const { return x; }
-  __device__ __forceinline__ int nt() const { return min(BN, x_end - x); }
+  __device__ __forceinline__ int nt() const { return min(TK, x_end - x); }
   __device__ __forceinline__ bool first() const { return x == k_first; }
   __device__ __forceinline__ bool last() const { return x + nt() == x_end; }
   __device__ __forceinline__ bool whole() const { return vlo >= v0 && vlo + n <= v1; }
@@ -360,18 +380,18 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   // of the whole step, which its store kernel does not write.
   if constexpr (!EARLY) pdl_wait();
   pdl_trigger();  // the next kernel in the stream may launch and set itself up
-  build_prefix(p, prefix, nkeys, blockIdx.x == 0);  // ends with __syncthreads
+  build_prefix<C::TK>(p, prefix, nkeys, blockIdx.x == 0);  // ends with __syncthreads
 
   const int v_tot = prefix[p.A];
-  const int W = keys_per_cta(v_tot, p.num_ctas);
+  const int W = keys_per_cta<C::TK>(v_tot, p.num_ctas);
   const int v0 = blockIdx.x * W;
   const int v1 = min(v0 + W, v_tot);
-  Cursor cur;
+  Cursor<C::TK> cur;
   if (v0 < v_tot) cur.init(prefix, nkeys, p.H_kv, p.A, v0, v1);
   if (v0 >= v_tot || !cur.more()) return;  // uniform: nothing allocated yet
 
   if (warp == 5) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -404,17 +424,22 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             mbar_arrive_expect_tx(&kv_full[n_early], static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + QSUB));
 #pragma unroll 1
             for (int sub = 0; sub < C::NSUB; ++sub) {
-              if (nb * BOX_ROWS == BN) {  // a whole tile: one box each
-                tma_load_3d(st + C::K_OFF + sub * SUB, &map_kf, sub * 64, cur.k0(), kv_row, &kv_full[n_early], pol_kv);
-                tma_load_3d(st + C::V_OFF + sub * SUB, &map_vf, sub * 64, cur.k0(), kv_row, &kv_full[n_early], pol_kv);
+              if (nb * BOX_ROWS == C::TK) {  // a whole tile: one box per 128-key block
+#pragma unroll 1
+                for (int kb = 0; kb < C::KB; ++kb) {
+                  tma_load_3d(st + C::K_OFF + sub * C::SUBK + kb * SUB, &map_kf, sub * 64, cur.k0() + kb * BN, kv_row,
+                              &kv_full[n_early], pol_kv);
+                  tma_load_3d(st + C::V_OFF + sub * C::SUBK + kb * SUB, &map_vf, sub * 64, cur.k0() + kb * BN, kv_row,
+                              &kv_full[n_early], pol_kv);
+                }
                 continue;
               }
 #pragma unroll 1
               for (int b = 0; b < nb; ++b) {
-                tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
-                            kv_row, &kv_full[n_early], pol_kv);
-                tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
-                            kv_row, &kv_full[n_early], pol_kv);
+                tma_load_3d(st + C::K_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_k, sub * 64,
+                            cur.k0() + b * BOX_ROWS, kv_row, &kv_full[n_early], pol_kv);
+                tma_load_3d(st + C::V_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_v, sub * 64,
+                            cur.k0() + b * BOX_ROWS, kv_row, &kv_full[n_early], pol_kv);
               }
             }
             qrow[n_early] = cur.a * p.H_q + cur.g * p.G;
@@ -437,15 +462,20 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
           const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
           mbar_arrive_expect_tx(&kv_full[s], bytes);
           for (int sub = 0; sub < C::NSUB; ++sub) {
-            if (nb * BOX_ROWS == BN) {  // a whole tile: one box each
-              tma_load_3d(st + C::K_OFF + sub * SUB, &map_kf, sub * 64, cur.k0(), kv_row, &kv_full[s], pol_kv);
-              tma_load_3d(st + C::V_OFF + sub * SUB, &map_vf, sub * 64, cur.k0(), kv_row, &kv_full[s], pol_kv);
+            if (nb * BOX_ROWS == C::TK) {  // a whole tile: one box per 128-key block
+#pragma unroll
+              for (int kb = 0; kb < C::KB; ++kb) {
+                tma_load_3d(st + C::K_OFF + sub * C::SUBK + kb * SUB, &map_kf, sub * 64, cur.k0() + kb * BN, kv_row,
+                            &kv_full[s], pol_kv);
+                tma_load_3d(st + C::V_OFF + sub * C::SUBK + kb * SUB, &map_vf, sub * 64, cur.k0() + kb * BN, kv_row,
+                            &kv_full[s], pol_kv);
+              }
             } else {
               for (int b = 0; b < nb; ++b) {
-                tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
-                            kv_row, &kv_full[s], pol_kv);
-                tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
-                            kv_row, &kv_full[s], pol_kv);
+                tma_load_3d(st + C::K_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_k, sub * 64,
+                            cur.k0() + b * BOX_ROWS, kv_row, &kv_full[s], pol_kv);
+                tma_load_3d(st + C::V_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_v, sub * 64,
+                            cur.k0() + b * BOX_ROWS, kv_row, &kv_full[s], pol_kv);
               }
             }
             tma_load_3d(st + C::Q_OFF + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, &kv_full[s],
@@ -489,10 +519,10 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
           }
           for (int sub = 0; sub < C::NSUB; ++sub) {
             for (int b = 0; b < nb; ++b) {
-              tma_load_3d(st + C::K_OFF + sub * SUB + b * BOX_ROWS * 128, &map_k, sub * 64, cur.k0() + b * BOX_ROWS,
-                          kv_row, bar, pol_kv);
-              tma_load_3d(st + C::V_OFF + sub * SUB + b * BOX_ROWS * 128, &map_v, sub * 64, cur.k0() + b * BOX_ROWS,
-                          kv_row, bar, pol_kv);
+              tma_load_3d(st + C::K_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_k, sub * 64,
+                          cur.k0() + b * BOX_ROWS, kv_row, bar, pol_kv);
+              tma_load_3d(st + C::V_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_v, sub * 64,
+                          cur.k0() + b * BOX_ROWS, kv_row, bar, pol_kv);
             }
             if (load_q) tma_load_3d(qb + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, bar, pol_q);
           }
@@ -513,7 +543,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_f16kind_f32(E::kMmaFormat, BN, NQ, 0, 0);
       constexpr uint32_t IDESC_O = idesc_f16kind_f32(E::kMmaFormat, BN, NQ, 0, 1);
-      constexpr uint32_t V_LBO = D == 128 ? SUB : 0;  // D = 64: the second M half repeats the first
+      constexpr uint32_t V_LBO = D == 128 ? C::SUBK : 0;  // D = 64: the second M half repeats the first
       const uint32_t p_addr = sbase + C::P_OFF;
       bool issued = false;
       // S^T of tile t, its K/V (and query) tile already landed.  Attention call: the query tile rides in the tile's
@@ -531,11 +561,14 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         const uint32_t st = sbase + (t % C::NS) * C::STAGE;
         const uint32_t qb = FUSED ? sbase + C::QB_OFF + (kq % C::QR) * C::QBUF : st + C::Q_OFF;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (ks / 4) * SUB + (ks % 4) * 32;
-          const uint32_t qoff = (ks / 4) * QSUB + (ks % 4) * 32;
-          umma_f16_ss(tmem + (t & 1) * NQ, smem_desc_sw128(st + C::K_OFF + koff, 16, 1024),
-                      smem_desc_sw128(qb + qoff, 16, 1024), IDESC_S, ks > 0);
+        for (int kb = 0; kb < C::KB; ++kb) {  // one M = 128 MMA chain per block of 128 keys
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = (ks / 4) * C::SUBK + kb * SUB + (ks % 4) * 32;
+            const uint32_t qoff = (ks / 4) * QSUB + (ks % 4) * 32;
+            umma_f16_ss(tmem + ((t & 1) * C::KB + kb) * NQ, smem_desc_sw128(st + C::K_OFF + koff, 16, 1024),
+                        smem_desc_sw128(qb + qoff, 16, 1024), IDESC_S, ks > 0);
+          }
         }
         umma_commit(&s_full[t & 1]);
         if constexpr (FUSED) {
@@ -560,10 +593,10 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         if (cur.has_next()) {
           bool n_last, n_key;
           if (!cur.last()) {
-            n_last = cur.x_end - (cur.x + cur.nt()) <= BN;
+            n_last = cur.x_end - (cur.x + cur.nt()) <= C::TK;
             n_key = n_last && cur.x_end == cur.n;
           } else {
-            Cursor nx = cur;
+            Cursor<C::TK> nx = cur;
             nx.advance();
             n_last = nx.last();
             n_key = n_last && nx.x_end == nx.n;
@@ -589,11 +622,11 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         if (!mbar_wait_bounded(&p_full[it & 1], (it >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t v_addr = sbase + (it % C::NS) * C::STAGE + C::V_OFF;
-        const uint32_t pb_addr = p_addr + (it & 1) * 2 * QSUB;
+        const uint32_t pb_addr = p_addr + (it & 1) * C::PBUF;
         const uint32_t acc0 = cur.first() ? 0u : 1u;
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          umma_f16_ss(tmem + 2 * NQ, smem_desc_sw128(v_addr + ks * 2048, V_LBO, 1024),
+        for (int ks = 0; ks < C::TK / 16; ++ks) {
+          umma_f16_ss(tmem + C::O_COL, smem_desc_sw128(v_addr + ks * 2048, V_LBO, 1024),
                       smem_desc_sw128(pb_addr + (ks / 4) * QSUB + (ks % 4) * 32, 16, 1024), IDESC_O,
                       ks > 0 ? 1u : acc0);
         }
@@ -634,7 +667,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       for (int k = 0; cur.more(); ++k) {
         const int b = k % C::QR, ph = (k / C::QR) & 1;
         const int pos = nkeys[cur.a] - 1;
-        Cursor c = cur;  // find the segment's last tile in this CTA
+        Cursor<C::TK> c = cur;  // find the segment's last tile in this CTA
         int t_last = t_first;
         while (!c.last()) { c.advance(); ++t_last; }
         const bool new_key = cur.x_end == cur.n;
@@ -700,13 +733,13 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
 #pragma unroll
           for (int u = 0; u < NU; ++u) {
             const int j = lane + 32 * u;
-            *cell(st + C::K_OFF + (j >> 6) * SUB, row, j) = kr[2 * u];
-            *cell(st + C::K_OFF + ((j + HALF) >> 6) * SUB, row, j + HALF) = kr[2 * u + 1];
+            *cell(st + C::K_OFF + (j >> 6) * C::SUBK, row, j) = kr[2 * u];
+            *cell(st + C::K_OFF + ((j + HALF) >> 6) * C::SUBK, row, j + HALF) = kr[2 * u + 1];
           }
 #pragma unroll
           for (int e = 0; e < D / 32; ++e) {
             const int j = lane + 32 * e;
-            *cell(st + C::V_OFF + (j >> 6) * SUB, row, j) = vn[e];
+            *cell(st + C::V_OFF + (j >> 6) * C::SUBK, row, j) = vn[e];
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -738,17 +771,23 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       const bool first = cur.first();
       if (!__all_sync(FULL, mbar_wait_bounded(&s_full[it & 1], (it >> 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      uint32_t u[16];
-      tmem_ld16(tmem + lane_base + (it & 1) * NQ, u);
+      // key kb * 128 + r of the tile, for each 128-key block kb
+      uint32_t u[C::KB][16];
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb) tmem_ld16(tmem + lane_base + ((it & 1) * C::KB + kb) * NQ, u[kb]);
       tmem_wait_ld();
       float* red_max = red_max2 + (it & 1) * 4 * NQ;
-      const bool valid = r < nt;
-      float x[GP], mt[GP];
+      float x[C::KB][GP], mt[GP];
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
-        x[h] = (valid && h < p.G) ? __uint_as_float(u[h]) * p.scale_log2 : -INFINITY;
+        float xm = -INFINITY;
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+          x[kb][h] = (kb * BN + r < nt && h < p.G) ? __uint_as_float(u[kb][h]) * p.scale_log2 : -INFINITY;
+          xm = fmaxf(xm, x[kb][h]);
+        }
         float m;  // the warp's maximum in one instruction
-        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(x[h]));
+        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(xm));
         if (lane == 0) red_max[warp * NQ + h] = m;
       }
       named_bar_sync(1, BN);
@@ -776,33 +815,38 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       tc_fence_after();
       if (grow_any) {  // uniform across the CTA: every thread saw the same maxima
         uint32_t o[16];
-        tmem_ld16(tmem + lane_base + 2 * NQ, o);
+        tmem_ld16(tmem + lane_base + C::O_COL, o);
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < GP; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-        tmem_st16(tmem + lane_base + 2 * NQ, o);
+        tmem_st16(tmem + lane_base + C::O_COL, o);
         tmem_wait_st();
       }
-      // P^T[h][r] in the storage type (K-major B operand: 16 rows of 128 keys, two 64-key
-      // swizzled sub-tiles); padded heads and invalid keys are zero.
-      const int sub = r >> 6, chunk = (r & 63) >> 3, e = r & 7;
-      unsigned char* pt = pt0 + (it & 1) * 2 * QSUB;
+      // P^T[h][key] in the storage type (K-major B operand: 16 rows of TK keys in
+      // 64-key swizzled sub-tiles); padded heads and invalid keys are zero.
+      const int chunk = (r & 63) >> 3, e = r & 7;
+      unsigned char* pt = pt0 + (it & 1) * C::PBUF;
 #pragma unroll
-      for (int h = 0; h < NQ; ++h) {
-        uint16_t b = 0;
-        if (h < GP) {
-          const float pv = x[h] == -INFINITY ? 0.f : exp2f(x[h] - m_ref[h]);
-          b = E::from_f32(pv);
-          l[h] += E::to_f32(b);  // the weight P.V actually uses
+      for (int kb = 0; kb < C::KB; ++kb) {
+        const int sub = (kb * BN + r) >> 6;
+#pragma unroll
+        for (int h = 0; h < NQ; ++h) {
+          uint16_t b = 0;
+          if (h < GP) {
+            const float pv = x[kb][h] == -INFINITY ? 0.f : exp2f(x[kb][h] - m_ref[h]);
+            b = E::from_f32(pv);
+            l[h] += E::to_f32(b);  // the weight P.V actually uses
+          }
+          *reinterpret_cast<uint16_t*>(pt + sub * QSUB + h * 128 + ((chunk ^ (h & 7)) << 4) + e * 2) = b;
         }
-        *reinterpret_cast<uint16_t*>(pt + sub * QSUB + h * 128 + ((chunk ^ (h & 7)) << 4) + e * 2) = b;
-      }
-      if (!valid) {  // rows past the tile's keys: zero V so P = 0 meets no stale NaN
-        unsigned char* vrow = smem + (it % C::NS) * C::STAGE + C::V_OFF + r * 128;
+        if (kb * BN + r >= nt) {  // rows past the tile's keys: zero V so P = 0 meets no stale NaN
+          unsigned char* vrow = smem + (it % C::NS) * C::STAGE + C::V_OFF + (kb * BN + r) * 128;
 #pragma unroll
-        for (int sb = 0; sb < C::NSUB; ++sb)
+          for (int sb = 0; sb < C::NSUB; ++sb)
 #pragma unroll
-          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + sb * SUB + c * 16) = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(vrow + sb * C::SUBK + c * 16) = make_uint4(0, 0, 0, 0);
+        }
       }
       // Each warp's P^T stores and TMEM reads are done and fenced before it
       // synchronises; then one lane arrives (four arrivals in all, instead
@@ -829,7 +873,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
         if (!__all_sync(FULL, mbar_wait_bounded(&o_done[it & 1], (it >> 1) & 1, abort_flag, p.status))) break;
         tc_fence_after();
         uint32_t o[16];
-        tmem_ld16(tmem + lane_base + 2 * NQ, o);
+        tmem_ld16(tmem + lane_base + C::O_COL, o);
         tmem_wait_ld();
         const int d = r;
         if (d < D) {
@@ -876,7 +920,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 cudaError_t make_decode_maps(const DecodeParams& p, DecodeMaps* m) {
