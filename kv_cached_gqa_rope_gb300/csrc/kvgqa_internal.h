@@ -117,6 +117,7 @@ struct PrefillParams {
   int A, T, H_q, H_kv, G, D, S, max_seq;
   float scale_log2;
   int f16;                    // storage: 0 BF16, 1 IEEE binary16
+  int out_32b;                // out is 32-byte aligned (set by the launcher): whole-sector stores
 };
 
 cudaError_t launch_prefill_attention(const PrefillParams& p, cudaStream_t stream);

@@ -66,12 +66,16 @@ template <int D>
 struct PCfg {
   static constexpr int NSUB = D / 64;               // 64-wide sub-tiles per row
   static constexpr int TILE = NSUB * SUB;           // one Q, K or V tile
-  static constexpr int NK = D == 128 ? 3 : 4;       // K stages
+  static constexpr int NK = D == 128 ? 2 : 4;       // K stages
   static constexpr int NV = D == 128 ? 2 : 4;       // V stages
   static constexpr int Q_OFF = 0;                   // Q_A, Q_B
   static constexpr int K_OFF = 2 * TILE;
   static constexpr int V_OFF = K_OFF + NK * TILE;
-  static constexpr int BAR_OFF = V_OFF + NV * TILE;
+  // Output staging: one [32 rows x 64 values] 128B-swizzled box per softmax
+  // warp, written by the warp and stored by the TMA unit.
+  static constexpr int STG = 32 * 128;
+  static constexpr int STG_OFF = V_OFF + NV * TILE;
+  static constexpr int BAR_OFF = STG_OFF + 8 * STG;
   // q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
   // s_full[2], p_full[2], o_done[2], turn[2], drain (index [2] = head A / B)
   static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 9;
@@ -85,6 +89,7 @@ struct PrefillMaps {
   CUtensorMap q;  // [A][T][H_q][D] rotated queries
   CUtensorMap k;  // cache [S*H_kv][T(bounded)][D]
   CUtensorMap v;
+  CUtensorMap o;  // [A][T][H_q][D] output, box of 32 rows x 64 values
 };
 
 
@@ -110,6 +115,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// One 32-byte store (eight 32-bit words, a whole sector) to global memory,
+// 32-byte aligned, marked as streaming (written once, not read again here).
+// Each softmax thread writes its own output row, so a warp's 16-byte stores
+// would each fill half of 32 different sectors: whole sectors halved the
+// cost of the item epilogue's stores.
+__device__ __forceinline__ void stg256_stream(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 // 2^x on the special-function unit (flushes results below 2^-126 to zero,
@@ -224,7 +240,8 @@ struct TileWalk {
 template <int D, bool F16>
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap map_q,
-                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
+                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                         const __grid_constant__ CUtensorMap map_o) {
   using C = PCfg<D>;
   using E = Elem<F16>;  // storage type of Q, K, V, P and the output
   extern __shared__ unsigned char smem_raw[];
@@ -546,21 +563,47 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
         const int tq = walk.qt * BM + r;
         const float inv = 1.f / l;
         const int h = x ? walk.hB : walk.hA;
+        // This warp's 32 rows go out through shared memory and a TMA store
+        // (coalesced, and off the softmax's path) when all of them lie inside
+        // the prompt; in a query tile that reaches past the prompt's end the
+        // rows take direct stores, and those past the end stay unwritten.
+        const int row0 = walk.qt * BM + (warp & 3) * 32;
+        const bool via_tma = row0 + 32 <= walk.len;
+        unsigned char* stg = smem + C::STG_OFF + warp * C::STG;
         uint16_t* dst = p.out + ((static_cast<size_t>(walk.a) * p.T + tq) * p.H_q + h) * D;
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t u[32];
-          tmem_ld32(o_col + q * 32, u);  // warp-wide: rows past the prompt load too, only their store is skipped
+        for (int sub = 0; sub < C::NSUB; ++sub) {  // 64 output values of the row at a time
+          uint32_t u[64];
+          tmem_ld32(o_col + sub * 64, *reinterpret_cast<uint32_t(*)[32]>(u));  // warp-wide
+          tmem_ld32(o_col + sub * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
           tmem_wait_ld();
-          if (tq < walk.len) {
+          uint32_t w[32];
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-              uint4 o;
-              o.x = E::pack2(__uint_as_float(u[q8 * 8 + 0]) * inv, __uint_as_float(u[q8 * 8 + 1]) * inv);
-              o.y = E::pack2(__uint_as_float(u[q8 * 8 + 2]) * inv, __uint_as_float(u[q8 * 8 + 3]) * inv);
-              o.z = E::pack2(__uint_as_float(u[q8 * 8 + 4]) * inv, __uint_as_float(u[q8 * 8 + 5]) * inv);
-              o.w = E::pack2(__uint_as_float(u[q8 * 8 + 6]) * inv, __uint_as_float(u[q8 * 8 + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + q * 32 + q8 * 8) = o;
+          for (int k = 0; k < 32; ++k) w[k] = E::pack2(__uint_as_float(u[2 * k]) * inv, __uint_as_float(u[2 * k + 1]) * inv);
+          if (via_tma) {
+            if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c)  // 16-byte chunk c of row `lane` at its 128B-swizzled place
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                  make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_4d(&map_o, stg, sub * 64, h, row0, walk.a);
+              bulk_commit_group();
+            }
+          } else if (tq < walk.len) {
+#pragma unroll
+            for (int q16 = 0; q16 < 4; ++q16) {  // 16 values: a whole 32-byte sector
+              uint16_t* o = dst + sub * 64 + q16 * 16;
+              const uint32_t(&w8)[8] = *reinterpret_cast<const uint32_t(*)[8]>(w + 8 * q16);
+              if (p.out_32b) {
+                stg256_stream(o, w8);
+              } else {
+                *reinterpret_cast<uint4*>(o) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+                *reinterpret_cast<uint4*>(o + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+              }
             }
           }
         }
@@ -568,6 +611,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
     }
   }
 
+  if (warp < 8 && lane == 0) bulk_wait_group<0>();  // this warp's output stores are complete
   __syncwarp();  // the role warps reconverge (their lane 0 worked alone)
   tc_fence_before();
   __syncthreads();
@@ -607,6 +651,17 @@ cudaError_t make_maps(const PrefillParams& p, PrefillMaps* m) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  {
+    cuuint64_t odims[4] = {D, static_cast<cuuint64_t>(p.H_q), static_cast<cuuint64_t>(p.T),
+                           static_cast<cuuint64_t>(p.A)};
+    cuuint64_t ostrides[3] = {D * 2, D * 2 * p.H_q, D * 2 * p.H_q * p.T};
+    cuuint32_t obox[4] = {64, 1, 32, 1};
+    cuuint32_t oes[4] = {1, 1, 1, 1};
+    if (enc(&m->o, elem_type, 4, p.out, odims, ostrides, obox, oes, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   return cudaSuccess;
 }
 
@@ -637,7 +692,7 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t 
   const int per_tok = p.G % 2 == 0 ? p.H_q / 2 : p.H_q;  // head pairs when the group size is even
   const long long items = static_cast<long long>((p.T + BM - 1) / BM) * p.A * per_tok;
   const unsigned grid = static_cast<unsigned>(items < sms[dev] ? items : sms[dev]);  // one CTA per SM
-  prefill_attention_kernel<D, F16><<<grid, THREADS, PCfg<D>::SMEM, stream>>>(p, m.q, m.k, m.v);
+  prefill_attention_kernel<D, F16><<<grid, THREADS, PCfg<D>::SMEM, stream>>>(p, m.q, m.k, m.v, m.o);
   return cudaGetLastError();
 }
 
@@ -657,8 +712,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
   return fn;
 }
 
-cudaError_t launch_prefill_attention(const PrefillParams& p, cudaStream_t stream) {
-  if (p.A == 0 || p.T == 0) return cudaSuccess;
+cudaError_t launch_prefill_attention(const PrefillParams& params, cudaStream_t stream) {
+  if (params.A == 0 || params.T == 0) return cudaSuccess;
+  PrefillParams p = params;
+  p.out_32b = reinterpret_cast<uintptr_t>(p.out) % 32 == 0;  // every output row then starts on 32 bytes too
   PrefillMaps m;
   cudaError_t e = make_maps(p, &m);
   if (e != cudaSuccess) return e;

@@ -128,3 +128,22 @@ def test_prefill_invalid_row_flagged():
     k0 = run.k0
     k0[r0, :, : wl.T] = run.k_cache[r0, :, : wl.T]
     assert torch.equal(k0.view(torch.int16), run.k_cache.view(torch.int16))
+
+
+def test_prefill_output_16_byte_aligned():
+    """The output only needs 16-byte alignment: an output that starts 16 bytes
+    past a 32-byte boundary (whose rows then take 16-byte stores instead of
+    whole 32-byte sectors) gets the same bytes as an aligned one, and nothing
+    around it is written."""
+    pw = W.scaled_prefill(W.PREFILL, A=2, T=200, H_q=8, H_kv=2, D=128, slots=3, max_seq=256)
+    pin = W.make_prefill_inputs(pw)
+    a = PrefillRun(pin)
+    a.run()
+    b = PrefillRun(pin)
+    n = a.out.numel()
+    big = torch.full((n + 32,), 7.0, dtype=torch.bfloat16, device="cuda")
+    b.out = big[8:8 + n].view(a.out.shape)  # 16 bytes past the allocation's start
+    assert b.out.data_ptr() % 32 == 16
+    b.run()
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert bool((big[:8] == 7.0).all()) and bool((big[8 + n:] == 7.0).all())
