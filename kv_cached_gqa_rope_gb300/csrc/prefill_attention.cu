@@ -13,20 +13,22 @@
 // pair of query heads of one KV group), longest first, dealt round-robin.
 // Both heads of a pair read the same K/V tiles, so each tile staged in shared
 // memory feeds four MMAs.  Per item:
-//   warp 8      TMA: the two Q tiles, then 128-key K tiles (3-stage ring);
+//   warp 8      TMA: the two Q tiles, then 128-key K tiles (2-stage ring);
 //   warp 9      TMA: the matching V tiles (2-stage ring);
 //   warp 10     one thread issues tcgen05.mma: S_x = Q_x K^T into TMEM and
 //               O_x += P_x V with P_x read from TMEM (x = A, B);
 //   warps 0-3   softmax of head A, warps 4-7 softmax of head B, one thread
-//               per query row: S row from TMEM, scale and diagonal causal mask,
-//               FP32 online softmax, P as BF16 (FP16 storage: FP16) pairs written back over the S
-//               columns, O rescaled in TMEM only when the row maximum grew by
-//               more than 2^8 (otherwise the old base is kept; O / l stays
-//               exact); at the item end O / l is rounded to the storage type and stored.
-// The two softmax groups alternate with the tensor core: while one works on
-// its head's scores, the MMAs of the other head run.  MMAs issued by one
-// thread complete in order and a commit covers every earlier MMA, so S_x of
-// tile t being ready means P_x of tile t-1 has been consumed.
+//               per query row: S row from TMEM, scale and causal mask (on the
+//               tiles that reach past the row's query), FP32 online softmax, P
+//               in the storage type written back over the S columns, O
+//               rescaled in TMEM only when the row maximum grew by more than
+//               2^8 (otherwise the old base is kept; O / l stays exact); at the
+//               item end O / l is rounded to the storage type, staged in shared
+//               memory per warp and stored by the TMA unit.
+// While one head's softmax group works on its scores, the MMAs of the other
+// head run.  MMAs issued by one thread complete in order and a commit covers
+// every earlier MMA, so S_x of tile t being ready means P_x of tile t-1 has
+// been consumed.
 // Key tiles past the diagonal are never visited; tensor maps bound the key and
 // query ranges by T so rows past the prompt read as zeros.  With an odd group
 // size, items hold one head (the B group idles).
@@ -77,8 +79,8 @@ struct PCfg {
   static constexpr int STG_OFF = V_OFF + NV * TILE;
   static constexpr int BAR_OFF = STG_OFF + 8 * STG;
   // q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-  // s_full[2], p_full[2], o_done[2], turn[2], drain (index [2] = head A / B)
-  static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 9;
+  // s_full[2], p_full[2], o_done[2], drain (index [2] = head A / B)
+  static constexpr int NBAR = 4 + 2 * NK + 2 * NV + 7;
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 8;
   static constexpr int SMEM = FLAG_OFF + 16 + 1024;  // + alignment slack
@@ -257,8 +259,7 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   uint64_t* s_full = v_empty + C::NV;  // [head]
   uint64_t* p_full = s_full + 2;       // [head]
   uint64_t* o_done = p_full + 2;       // [head]
-  uint64_t* turn = o_done + 2;         // [head]: that head's softmax group finished a tile
-  uint64_t* drain = turn + 2;
+  uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -290,7 +291,6 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
       mbar_init(&s_full[x], 1);
       mbar_init(&p_full[x], 4);  // one arrival per softmax warp
       mbar_init(&o_done[x], 1);
-      mbar_init(&turn[x], 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -466,13 +466,6 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
       const int mbase = walk.mask_base(), mlo = walk.mask_lo();
       if (!__all_sync(FULLMASK, mbar_wait_bounded(&s_full[x], t & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      // With head pairs the two groups take turns (A0 B0 A1 B1 ...): each runs
-      // its softmax alone on the SM's issue slots while the tensor core
-      // works for the other head.
-      if (walk.pairs() && (x == 1 || t > 0)) {
-        const int k = x == 0 ? t - 1 : t;  // completion of the other group to wait for
-        if (!__all_sync(FULLMASK, mbar_wait_bounded(&turn[1 - x], k & 1, abort_flag, p.status))) break;
-      }
       // Scores enter the softmax as s * ce with ce > 0 (a non-positive scale is
       // folded into the scores first, a path no usual caller takes).  On the
       // tiles that reach past a query's position (the diagonal), keys after
@@ -553,7 +546,6 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&p_full[x]);
-        if (walk.pairs()) mbar_arrive(&turn[x]);
       }
 
       if (last) {
