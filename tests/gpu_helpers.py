@@ -13,9 +13,10 @@ import workloads as W
 
 # Attention output tolerances versus the FP64 oracle: max-abs and RMS as the
 # acceptance bar states them, plus relative RMS.  The GPU result is rounded to
-# BF16 once (relative error <= 2^-9, RMS about 2^-9/sqrt(3) of the value) and
-# accumulates in FP32 over at most 65536 keys (relative error well below
-# 1e-5), so a relative RMS above 5e-3 means a real defect.
+# BF16 once (8 significant bits: relative error <= 2^-8, RMS about
+# 2^-8/sqrt(3) ~ 2.3e-3 of the value) and accumulates in FP32 over at most
+# 65536 keys (relative error well below 1e-5), so a relative RMS above 5e-3
+# means a real defect.
 #
 # The output is stored in a 16-bit format, whose grid is coarser than the
 # 1e-2 max-abs bar for large values: a BF16 value in [2, 4) has neighbours
