@@ -74,3 +74,15 @@ def test_varlen_flops(spans):
 def test_varlen_with_zero_offsets_is_the_equal_length_prefill():
     wl = W.scaled_prefill(W.PREFILL, A=4, T=50, H_q=8, H_kv=2, D=32)
     assert bench.varlen_flops(wl, [0] * 4, [50] * 4) == bench.prefill_flops(wl)
+
+
+def test_e2e_entry_prefers_the_checked_graph_and_keeps_the_plain_loop():
+    import bench
+    graph = {"value": 2.0, "unit": bench.UNIT, "h2d_bytes_per_step": 10, "d2h_bytes_per_step": 20,
+             "spread": {"median_ms": 1.0}, "note": "one CUDA graph per step"}
+    e = bench.e2e_line(1.0, {"median_ms": 2.0}, graph, 10, 20)
+    assert e["value"] == 2.0 and e["mode"].startswith("cuda_graph")
+    assert e["plain"]["value"] == 1.0 and e["plain"]["h2d_bytes_per_step"] == 10
+    assert e["h2d_bytes_per_step"] == 10 and e["d2h_bytes_per_step"] == 20
+    e = bench.e2e_line(1.0, {"median_ms": 2.0}, {"unavailable": "capture refused"}, 10, 20)
+    assert e["value"] == 1.0 and e["mode"].startswith("plain") and e["graph"] == {"unavailable": "capture refused"}
