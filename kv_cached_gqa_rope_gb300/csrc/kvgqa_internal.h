@@ -46,8 +46,10 @@ struct RopeStoreParams {
 
 // mode 0: decode (token a at positions[a]); 1: equal-length prefill (one CTA
 // per position 0..T-1, all prompts); 2: varlen prefill (token t of prompt a at
-// offsets[a] + t, t < lengths[a]).  Modes 0 and 2 give each token four CTAs,
-// each with a quarter of the frequencies (H_kv * D / 8 must divide by 4).
+// offsets[a] + t, t < lengths[a]).  Mode 0 gives each token four CTAs, each
+// with a quarter of the frequencies (H_kv * D / 8 must divide by 4); mode 2
+// walks the real tokens in groups of 8 per CTA (up to 2048 prompts; with
+// more, the padded tokens with four CTAs each, as mode 0).
 cudaError_t launch_rope_kv_store(const RopeStoreParams& p, int mode, cudaStream_t stream);
 
 // ------------------------------------------------------------------ decode attention

@@ -123,3 +123,34 @@ def test_step_repeats_are_idempotent(single):
     torch.cuda.synchronize()
     assert torch.equal(first_out.view(torch.int16), run.out.view(torch.int16))
     assert torch.equal(first_k.view(torch.int16), run.k_cache.view(torch.int16))
+
+
+@pytest.mark.parametrize("single", [False, True], ids=["two_launch", "single_launch"])
+def test_step_captured_in_a_cuda_graph(single):
+    """The whole step, prepared on a stream of its own and captured once as a
+    CUDA graph (its programmatic launches included), replays to the same
+    caches and output as direct calls, and leaves no status flag."""
+    import kv_cached_gqa_rope_gb300 as kv
+    inp = W.make_decode_inputs(W.LLAMA_DECODE)
+    wl = inp.wl
+    a = DecodeRun(inp)
+    whole_step(a, single_launch=single)
+    torch.cuda.synchronize()
+    b = DecodeRun(inp)
+    ws = kv.new_workspace(kv.decode_step_workspace_size(wl.A, wl.H_q, wl.H_kv, wl.D))
+    s = torch.cuda.Stream()
+    call = kv.prepare_decode_step_out_(b.q, b.k, b.v, b.positions, b.cache_rows, wl.theta, wl.scale,
+                                       b.k_cache, b.v_cache, b.out, ws, s, single_launch=single)
+    with torch.cuda.stream(s):
+        call()  # first use outside the capture
+    torch.cuda.synchronize()
+    b.out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+        call()
+    for _ in range(2):
+        with torch.cuda.stream(s):
+            g.replay()
+    torch.cuda.synchronize()
+    assert_same_bytes(a, b, "graph replay")
+    assert kv.kvgqa_read_status(ws) == 0
