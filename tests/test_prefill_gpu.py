@@ -64,6 +64,7 @@ SMALL = [
     dict(A=2, T=129, H_q=8, H_kv=1, D=128, slots=3, max_seq=200),
     dict(A=1, T=255, H_q=16, H_kv=2, D=128, slots=2, max_seq=256),
     dict(A=2, T=300, H_q=6, H_kv=2, D=64, slots=4, max_seq=320),
+    dict(A=2, T=160, H_q=8, H_kv=2, D=64, slots=3, max_seq=192),  # D = 64 with head pairs
     dict(A=1, T=1, H_q=4, H_kv=2, D=64, slots=2, max_seq=8),
 ]
 
