@@ -83,7 +83,8 @@ def sampled_rows(inp, k):
     return sorted(order[idx].tolist())
 
 
-@pytest.mark.parametrize("wl,k", [(W.LLAMA_DECODE, 32), (W.DIVERGENT_DECODE, 128), (W.LONG_DECODE, 8)],
+@pytest.mark.parametrize("wl,k", [(W.LLAMA_DECODE, 32), (W.DIVERGENT_DECODE, 128), (W.LONG_DECODE, 8)]
+                         + [(w, 32) for w in W.HEAD_SHAPE_DECODE],
                          ids=lambda x: getattr(x, "name", str(x)))
 def test_attention_workloads(wl, k):
     """Every active row (k = A) and every query head of the decode workloads

@@ -48,7 +48,7 @@ def test_f16_decode_tiny_against_oracle():
     assert run.status() == (0, 0)
 
 
-@pytest.mark.parametrize("wl", [W.LLAMA_DECODE, W.DIVERGENT_DECODE], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [W.LLAMA_DECODE, W.DIVERGENT_DECODE, W.HEAD_SHAPE_DECODE[0]], ids=lambda w: w.name)
 def test_f16_decode_workloads_sampled(wl):
     """Full-size decode workloads: the new cells of every active row against
     the oracle's rotation, the output of sampled (row, head) pairs against the

@@ -253,3 +253,25 @@ def test_varlen_full_size():
     check_caches(run, prompts, kc, vc)
     check_outputs(run, prompts, ref, "chunked prefill, full size")
     assert run.kv.kvgqa_read_status(run.ws) == 0
+
+
+def test_varlen_more_prompts_than_the_scan_holds():
+    """2100 prompts (more than the 2048 whose lengths the store kernel scans
+    in shared memory): the store walks the padded tokens instead; caches and
+    outputs against the oracle as for the small cases, with empty prompts,
+    prompts ending at max_seq and one with an out-of-range row among them."""
+    rng = np.random.default_rng(11)
+    A, T, max_seq = 2100, 3, 8
+    lengths = rng.integers(0, T + 1, A)
+    offsets = np.array([rng.integers(0, max_seq - n + 1) for n in lengths])
+    kw = dict(A=A, T=T, H_q=2, H_kv=1, D=64, slots=A, max_seq=max_seq,
+              offsets=[int(o) for o in offsets], lengths=[int(n) for n in lengths])
+    inp = make(kw)
+    inp.cache_rows[7] = A  # one prompt with a row out of range: skipped and flagged
+    run = VarlenRun(inp).run()
+    prompts = valid_prompts(inp)
+    assert len(prompts) == A - 1
+    _, ref, kc, vc = oracle_varlen(run, prompts)
+    check_caches(run, prompts, kc, vc)
+    check_outputs(run, prompts, ref, "varlen 2100 prompts")
+    assert run.kv.kvgqa_read_status(run.ws) == FLAG_ROW_RANGE
