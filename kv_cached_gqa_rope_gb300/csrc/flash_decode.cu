@@ -518,11 +518,21 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             nk_recent = kseg;
           }
           for (int sub = 0; sub < C::NSUB; ++sub) {
-            for (int b = 0; b < nb; ++b) {
-              tma_load_3d(st + C::K_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_k, sub * 64,
-                          cur.k0() + b * BOX_ROWS, kv_row, bar, pol_kv);
-              tma_load_3d(st + C::V_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_v, sub * 64,
-                          cur.k0() + b * BOX_ROWS, kv_row, bar, pol_kv);
+            if (nb * BOX_ROWS == C::TK) {  // a whole tile: one box per 128-key block
+#pragma unroll
+              for (int kb = 0; kb < C::KB; ++kb) {
+                tma_load_3d(st + C::K_OFF + sub * C::SUBK + kb * SUB, &map_kf, sub * 64, cur.k0() + kb * BN, kv_row,
+                            bar, pol_kv);
+                tma_load_3d(st + C::V_OFF + sub * C::SUBK + kb * SUB, &map_vf, sub * 64, cur.k0() + kb * BN, kv_row,
+                            bar, pol_kv);
+              }
+            } else {
+              for (int b = 0; b < nb; ++b) {
+                tma_load_3d(st + C::K_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_k, sub * 64,
+                            cur.k0() + b * BOX_ROWS, kv_row, bar, pol_kv);
+                tma_load_3d(st + C::V_OFF + sub * C::SUBK + b * BOX_ROWS * 128, &map_v, sub * 64,
+                            cur.k0() + b * BOX_ROWS, kv_row, bar, pol_kv);
+              }
             }
             if (load_q) tma_load_3d(qb + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, bar, pol_q);
           }
