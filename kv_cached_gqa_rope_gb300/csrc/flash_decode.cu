@@ -128,8 +128,8 @@ struct Cfg {
   static constexpr int NKEYS_OFF = PREFIX_OFF + (kMaxActiveRows + 1) * 4;  // [kMaxActiveRows] ints
   static constexpr int BAR_OFF = align_up(NKEYS_OFF + kMaxActiveRows * 4, 16);
   // kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], q_free[QR],
-  // prep_done[QR], patch_done[QR], last_full[QR], drain
-  static constexpr int NBAR = 2 * NS + 7 + 4 * QR;
+  // prep_done[QR], patch_done[QR], last_full[QR], q_full[QR], drain
+  static constexpr int NBAR = 2 * NS + 7 + 5 * QR;
   static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 8;
   static constexpr int SMEM = FLAG_OFF + 16 + 1024;            // + alignment slack
@@ -343,7 +343,8 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   uint64_t* prep_done = q_free + C::QR;    // fused step: its query tile is rotated
   uint64_t* patch_done = prep_done + C::QR;  // fused step: the new key is in its last tile
   uint64_t* last_full = patch_done + C::QR;  // fused step: the TMA of the tile with the new key landed
-  uint64_t* drain = last_full + C::QR;
+  uint64_t* q_full = last_full + C::QR;    // fused step: the segment's raw query tile landed
+  uint64_t* drain = q_full + C::QR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
   volatile int* merge_flag = abort_flag + 1;
@@ -364,6 +365,7 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
       mbar_init(&prep_done[b], 1);
       mbar_init(&patch_done[b], 1);
       mbar_init(&last_full[b], 1);
+      mbar_init(&q_full[b], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -488,15 +490,17 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             mbar_wait_bounded(&kv_full[t % C::NS], (t / C::NS) & 1, &none, nullptr);
         }
       } else {
-        // The segment's raw query tile comes with its first tile, into ring
-        // slot kseg % QR once the S MMAs of segment kseg - QR are done; the prep
-        // warp rotates it in place.  The tile that holds the new key lands on
+        // The segment's raw query tile is loaded ahead of its first K/V tile,
+        // on its own barrier, into ring slot kseg % QR once the S MMAs of
+        // segment kseg - QR are done; the prep warp rotates it in place,
+        // usually before the K/V tile lands.  The tile that holds the new key lands on
         // the segment's own barrier (last_full), which the prep warp waits for
         // before patching the key in (kv_full of a stage could be several
         // phases ahead of it); kv_full[s] gets a plain arrival so its phases
         // stay in step, and the MMA warp waits for the patch instead.
         int it = 0, kseg = -1;
         int nk_recent = -1;  // the most recent segment whose new-key tile was issued
+        int q_recent = -1;   // the most recent segment whose query tile was issued
         for (; cur.more(); cur.advance(), ++it) {
           const int s = it % C::NS;
           if (cur.first()) ++kseg;
@@ -506,10 +510,17 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
               !mbar_wait_bounded(&q_free[kseg % C::QR], (kseg / C::QR - 1) & 1, abort_flag, p.status))
             break;
           const int nb = (cur.nt() + BOX_ROWS - 1) / BOX_ROWS;
-          const uint32_t bytes = static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u + (load_q ? QSUB : 0u));
+          const uint32_t bytes = static_cast<uint32_t>(C::NSUB) * (2u * nb * BOX_ROWS * 128u);
           unsigned char* st = smem + s * C::STAGE;
           unsigned char* qb = smem + C::QB_OFF + (kseg % C::QR) * C::QBUF;
           const int kv_row = p.cache_rows[cur.a] * p.H_kv + cur.g;
+          if (load_q) {
+            uint64_t* qbar = &q_full[kseg % C::QR];
+            mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(C::NSUB) * QSUB);
+            for (int sub = 0; sub < C::NSUB; ++sub)
+              tma_load_3d(qb + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, qbar, pol_q);
+            q_recent = kseg;
+          }
           const bool newkey_tile = cur.last() && cur.x_end == cur.n;
           uint64_t* bar = newkey_tile ? &last_full[kseg % C::QR] : &kv_full[s];
           mbar_arrive_expect_tx(bar, bytes);
@@ -534,7 +545,6 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
                             cur.k0() + b * BOX_ROWS, kv_row, bar, pol_kv);
               }
             }
-            if (load_q) tma_load_3d(qb + sub * QSUB, &map_q, sub * 64, cur.a * p.H_q + cur.g * p.G, 0, bar, pol_q);
           }
         }
         if (*abort_flag) {
@@ -545,6 +555,9 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
           // new-key segments, which are consecutive
           for (int k = nk_recent; k >= 0 && k > nk_recent - C::NS; --k)
             mbar_wait_bounded(&last_full[k % C::QR], (k / C::QR) & 1, &none, nullptr);
+          // and the query tiles of the last (at most QR) segments
+          for (int k = q_recent; k >= 0 && k > q_recent - C::QR; --k)
+            mbar_wait_bounded(&q_full[k % C::QR], (k / C::QR) & 1, &none, nullptr);
         }
       }
     }
@@ -698,13 +711,8 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
             cs[u] = rope_cos_sin(pos, p.freqs.frac[lane + 32 * u], p.freqs.quad[lane + 32 * u]);
           cs_row = cur.a;
         }
-        // the raw query tile arrives with the segment's first tile (on the
-        // segment's own barrier when that tile also holds the new key)
-        const bool q_on_last = new_key && t_last == t_first;
-        if (!__all_sync(FULL, q_on_last ? mbar_wait_bounded(&last_full[b], ph, abort_flag, p.status)
-                                        : mbar_wait_bounded(&kv_full[t_first % C::NS], (t_first / C::NS) & 1,
-                                                            abort_flag, p.status)))
-          break;
+        // the raw query tile, on its own barrier
+        if (!__all_sync(FULL, mbar_wait_bounded(&q_full[b], ph, abort_flag, p.status))) break;
         unsigned char* qb = smem + C::QB_OFF + b * C::QBUF;
         for (int h = 0; h < p.G; ++h) {
 #pragma unroll
