@@ -669,8 +669,8 @@ flash_decode_splitk_kernel(const __grid_constant__ DecodeParams p, const __grid_
   } else if (FUSED && warp == 6) {
     // ---------------------------------------------------------- query / cell prep (fused step)
     // Per segment of this CTA, in order: rotate the group's G raw query rows
-    // (loaded with the segment's first tile into query buffer k % QR, 128B
-    // swizzled, K-major) in place at the row's position; and if this CTA
+    // (loaded ahead of the segment's first tile into query buffer k % QR,
+    // 128B swizzled, K-major) in place at the row's position; and if this CTA
     // holds the segment's last key, rotate the new K, store it with the new V
     // into the row's cell at that position, and write the same row into the
     // last K/V tile in shared memory (the TMA loaded the stale cell).  Lane l
