@@ -33,6 +33,12 @@
  *    of it is read or written) and a flag is set in the workspace status block,
  *    which kvgqa_read_status() returns on request.  The default path never
  *    synchronises the stream.
+ *  - A call that queues work only launches kernels on the given stream (some
+ *    with programmatic dependent launch): it can be captured into a CUDA
+ *    graph on a non-default stream and replayed, the replay using the
+ *    pointers and sizes of the captured call.  The no-allocation entry point
+ *    looks up its static array's address at its first call on a device, which
+ *    should therefore precede any capture.
  *
  * Data types: Q, K, V, the caches and the outputs are BF16, or all IEEE
  * binary16 (FP16 cached rows; one storage type per call, taken from its first
