@@ -264,6 +264,11 @@ prefill_attention_kernel(const __grid_constant__ PrefillParams p, const __grid_c
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Launched behind the store kernel with programmatic dependent launch: the
+  // CTA starts while the store's last CTAs drain and waits here before it
+  // reads anything that kernel writes (the item order, the rotated queries
+  // and the cache cells).
+  pdl_wait();
   TileWalk walk;
   walk.init(&p, blockIdx.x, gridDim.x);
   if (!walk.ok) {  // uniform: this CTA has no valid item
@@ -684,8 +689,17 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& m, cudaStream_t 
   const int per_tok = p.G % 2 == 0 ? p.H_q / 2 : p.H_q;  // head pairs when the group size is even
   const long long items = static_cast<long long>((p.T + BM - 1) / BM) * p.A * per_tok;
   const unsigned grid = static_cast<unsigned>(items < sms[dev] ? items : sms[dev]);  // one CTA per SM
-  prefill_attention_kernel<D, F16><<<grid, THREADS, PCfg<D>::SMEM, stream>>>(p, m.q, m.k, m.v, m.o);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = PCfg<D>::SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_attention_kernel<D, F16>, p, m.q, m.k, m.v, m.o);
 }
 
 }  // namespace

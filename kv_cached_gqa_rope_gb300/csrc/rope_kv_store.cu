@@ -70,8 +70,12 @@ __global__ void __launch_bounds__(256, 4) rope_kv_store_kernel(const __grid_cons
   constexpr int VU = D / 8;   // copy units per head: 8 elements (16 bytes) each
   __shared__ CosSin cs[HALF + HALF / 8];
 
-  pdl_wait();     // inputs and outputs may belong to the previous kernel
-  pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
+  // Inputs and outputs may belong to the previous kernel.  The prefill
+  // attention kernel launched behind this one (programmatic dependent launch)
+  // may start once every CTA here has exited: it needs every SM's whole
+  // register file, so an earlier signal would only let it take SMs this
+  // kernel's later CTAs still need.
+  pdl_wait();
   const int pos = blockIdx.x;  // position t, shared by all A prompts
   const int ntok = p.A;
 
@@ -323,8 +327,8 @@ __global__ void __launch_bounds__(kTokenThreads) rope_kv_store_token_kernel(cons
                                                                           int varlen) {
   constexpr int F = D / 2 / kTokenSplit;
   __shared__ CosSin cs[F + F / 8];
-  pdl_wait();     // inputs and outputs may belong to the previous kernel
-  pdl_trigger();  // the attention kernel may launch and set itself up meanwhile
+  pdl_wait();               // inputs and outputs may belong to the previous kernel
+  if (!varlen) pdl_trigger();  // decode: the attention kernel may launch and set itself up meanwhile
   if (varlen && p.item_order && blockIdx.x == 0) write_item_order(p);
   const int part = blockIdx.x % kTokenSplit;
   const int n_tok = varlen ? p.A * p.T : p.A;
@@ -359,8 +363,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 3) rope_kv_store_varlen_kernel
   int* start = scan;
   int* off_s = scan + p.A + 1;
   int* rows_s = off_s + p.A;
-  pdl_wait();
-  pdl_trigger();
+  pdl_wait();  // (no early signal to the attention kernel behind it: see rope_kv_store_kernel)
   if (p.item_order && blockIdx.x == 0) write_item_order(p);
   for (int a = threadIdx.x; a < p.A; a += blockDim.x) {
     const int off = p.offsets[a], len = p.lengths[a], row = p.cache_rows[a];
