@@ -68,7 +68,7 @@ def parse_args():
     ap.add_argument("--no-decode-workloads", action="store_true",
                     help="skip the attention call on the divergent-length and long-context decode workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
-    ap.add_argument("--only", choices=["decode", "prefill", "prefill-varlen"], default=None,
+    ap.add_argument("--only", choices=["decode", "decode-single", "prefill", "prefill-varlen"], default=None,
                     help="run just the timed decode steps, just the prefill calls, or just the chunked prefill call "
                          "(for profiler captures)")
     ap.add_argument("--decode-workload", choices=["llama", "divergent", "long", "d64", "g1", "g1d64"],
@@ -319,12 +319,29 @@ def run_ours(args, rank, world, local):
                                          single_launch=True)
 
     for _ in range(max(args.warmup, 3)):
+        if args.only == "decode-single":  # profiler run of the single-launch step: nothing else
+            single()
+            continue
         store()
         attend()
         if args.only is None:  # profiler runs (--only) launch only the kernels they capture
             step()
             single()
     torch.cuda.synchronize()
+    if args.only == "decode-single":
+        K = max(3, args.steps)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            single()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if kv.kvgqa_read_status(ws3):
+            raise RuntimeError("device status flags set in the single-launch step")
+        med, sp = spread([a.elapsed_time(b) for a, b in ev], world)
+        return {"impl": "ours", "only": "decode-single", "single_launch_step_ms": round(med, 5),
+                "tokens_per_s": round(whole_job_rate(wl.A, med / 1e3, world), 1), "spread": sp} if rank == 0 else None
     if args.only == "prefill":
         res = run_prefill(args, kv, dev, stream, flush, world, bf16_peak, bf16_sust, peak_src)
         res_v = run_prefill_varlen(args, kv, dev, stream, flush, world, bf16_peak, peak_src)
