@@ -582,6 +582,11 @@ def run_ours(args, rank, world, local):
         "roofline": {"kernel": "flash_decode_splitk_kernel (the cached_gqa_attention_out_ call; split-K with the combine run by the last CTA of each cut segment)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     # achieved is from the median launch (CUDA events on the launching stream, L2
+                     # flushed before each launch); the same at the mean launch duration beside it
+                     "launch_ms": {"median": attn_spread["median_ms"], "mean": attn_spread["mean_ms"],
+                                   "n": attn_spread["n"]},
+                     "achieved_at_mean": round(attn_bytes / (attn_spread["mean_ms"] / 1e3) / 1e9, 1),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s"},
         "e2e": e2e_line(e2e_value, e2e_spread, e2e_graph, h2d, d2h),
         "gpu_launches": 2 * K,  # rope_kv_store_kernel + flash_decode_splitk_kernel per step
