@@ -6,7 +6,6 @@
 // positive base.  Pair i is (x[i], x[i + D/2]) at angle pos * theta^(-2i/D).
 #pragma once
 
-#include <cuda_bf16.h>
 #include <cstdint>
 
 namespace kvgqa {
@@ -136,15 +135,6 @@ __device__ __forceinline__ float rot_second(float x1, float x2, const CosSin& cs
   const float qe = __fmaf_rn(x1, cs.sh, -q);
   const float lo = __fmaf_rn(x2, cs.cl, __fmaf_rn(x1, cs.sl, __fadd_rn(pe, qe)));
   return __fadd_rn(__fadd_rn(p, q), lo);
-}
-
-__device__ __forceinline__ uint16_t bf16_rn_bits(float v) {
-  const __nv_bfloat16 b = __float2bfloat16_rn(v);  // round to nearest even
-  return *reinterpret_cast<const uint16_t*>(&b);
-}
-
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
-  return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
 }  // namespace kvgqa
