@@ -1,5 +1,6 @@
-// Inline-PTX building blocks for sm_103a: mbarriers, bulk (TMA) copies,
-// bounded waits and packed FP32 arithmetic.  Internal to libkvgqa.
+// Inline-PTX building blocks for sm_103a: mbarriers and bounded waits, L2
+// cache policies, programmatic dependent launch, named barriers and packed
+// FP32 arithmetic.  Internal to libkvgqa.
 #pragma once
 
 #include <cstdint>
@@ -94,18 +95,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-// ------------------------------------------------------------------ bulk copy
-// One contiguous global -> shared copy by the TMA unit; completion is counted
-// in bytes on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
+// ------------------------------------------------------------------ L2 policies
 // L2 policy for data read once (the streamed K/V prefix).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
@@ -133,23 +123,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// ------------------------------------------------------------------ shared loads
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ float4 lds128f(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
-}
-
 // ------------------------------------------------------------------ packed FP32
 // Blackwell executes two FP32 FMAs per instruction on a 64-bit register pair.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -162,15 +135,6 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  float2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;"
-      : "=l"(*reinterpret_cast<unsigned long long*>(&d))
-      : "l"(*reinterpret_cast<unsigned long long*>(&a)),
-        "l"(*reinterpret_cast<unsigned long long*>(&b)));
-  return d;
-}
-
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   float2 d;
   asm("add.rn.f32x2 %0, %1, %2;"
@@ -178,11 +142,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
       : "l"(*reinterpret_cast<unsigned long long*>(&a)),
         "l"(*reinterpret_cast<unsigned long long*>(&b)));
   return d;
-}
-
-// Two BF16 values packed in a 32-bit word -> two FP32 values (exact).
-__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 }  // namespace kvgqa
