@@ -253,31 +253,35 @@ def step_args(A=2, H_q=4, H_kv=2, D=64, S=4, L=32):
                 out=torch.zeros(A, H_q, D, dtype=bf), workspace=aligned_bytes(256))
 
 
-def test_decode_step_contract():
+@pytest.mark.parametrize("call", [kv.decode_step_out_, kv.decode_step_single_launch_out_],
+                         ids=["two_kernels", "single_launch"])
+def test_decode_step_contract(call):
+    """Both forms of the whole step share the host contract: every refusal
+    below happens before anything is queued."""
     a = step_args()
     a["out"] = a["q"]
-    assert code_of(kv.decode_step_out_, **a) == "EALIAS"
+    assert code_of(call, **a) == "EALIAS"
     a = step_args()
     a["out"] = a["k_cache"].view(-1)[: 2 * 4 * 64].view(2, 4, 64)
-    assert code_of(kv.decode_step_out_, **a) == "EALIAS"
+    assert code_of(call, **a) == "EALIAS"
     a = step_args()
     a["theta"] = -1.0
-    assert code_of(kv.decode_step_out_, **a) == "EINVAL"
+    assert code_of(call, **a) == "EINVAL"
     a = step_args()
     a["scale"] = float("inf")
-    assert code_of(kv.decode_step_out_, **a) == "EINVAL"
+    assert code_of(call, **a) == "EINVAL"
     a = step_args(H_q=64, H_kv=2)               # G = 32 has no decode kernel
-    assert code_of(kv.decode_step_out_, **a) == "EUNSUPPORTED"
+    assert code_of(call, **a) == "EUNSUPPORTED"
     a = step_args()
     a["v"] = torch.zeros(2, 3, 64, dtype=torch.bfloat16)
-    assert code_of(kv.decode_step_out_, **a) == "EINVAL"
+    assert code_of(call, **a) == "EINVAL"
     a = step_args()
     a["k"] = torch.zeros(2, 2, 64, dtype=torch.float32)
-    assert code_of(kv.decode_step_out_, **a) == "EDTYPE"
+    assert code_of(call, **a) == "EDTYPE"
     a = step_args(A=1100)
-    assert code_of(kv.decode_step_out_, **a) == "EUNSUPPORTED"
+    assert code_of(call, **a) == "EUNSUPPORTED"
     # every descriptor check passes: host tensors then fail the device check
-    assert code_of(kv.decode_step_out_, **step_args()) in ("ECUDA", "EDEVICE")
+    assert code_of(call, **step_args()) in ("ECUDA", "EDEVICE")
 
 
 def test_overflowing_sizes_are_refused():
